@@ -1,0 +1,207 @@
+"""Seeded synthetic inputs for paged KV attention.
+
+This module only draws random numbers and lays them out as plain arrays.  It
+holds none of the method's arithmetic: no slot or position arithmetic, no
+softmax, no gather.  Both the float64 oracle (``oracle/``) and the CUDA path
+(``paged_kv_attention_17_gb300``) consume what it returns, each turning the
+schedule into kernel metadata with its own code.
+
+A workload is the state a model runner hands to the attention layer for one
+step ("Model execution", section "Flattening a step"):
+
+* a schedule: per request, how many tokens are already in the cache
+  (``computed``), how many are scheduled this step (``scheduled``) and its
+  block table (physical block IDs of its context, in logical order);
+* a KV pool of ``num_blocks`` blocks of 16 slots whose cached-prefix contents
+  are random (prefix K/V are placed straight into the pool);
+* Q, and the new tokens' K and V, for the flat batch of all scheduled tokens.
+
+Values are N(0, 1) drawn from ``numpy.random.Generator(PCG64(seed))``; bf16
+inputs are the float32 draws rounded to nearest-even bf16 and are stored as
+their raw 16-bit patterns (numpy has no bf16 type).  Physical blocks are handed
+out from ``rng.permutation(pool)``, context lengths from ``rng.integers``.
+
+Named workloads follow the five shapes the attention pages are about: a tiny
+three-request step like the pages' worked example, batch-1 long-context decode
+(the FlashDecoding case), batched decode, a mixed chunked-prefill step and a
+T = 8192 causal prefill.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK_SIZE = 16
+
+
+@dataclass
+class Request:
+    """One request of a step: cached tokens, new tokens and block table."""
+
+    computed: int
+    scheduled: int
+    blocks: list[int]
+
+
+@dataclass
+class Workload:
+    name: str
+    dtype: str                      # "f32" or "bf16"
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    num_blocks: int                 # pool size in blocks
+    requests: list[Request]
+    q: np.ndarray                   # [N, Hq, D]  float32 or uint16 (bf16 bits)
+    k_new: np.ndarray               # [N, Hkv, D]
+    v_new: np.ndarray               # [N, Hkv, D]
+    k_pool: np.ndarray              # [num_blocks, 16, Hkv, D]
+    v_pool: np.ndarray              # [num_blocks, 16, Hkv, D]
+    softmax_scale: float
+    causal: bool = True
+    block_size: int = BLOCK_SIZE
+    # Extra schedules with the same shape on disjoint blocks of the same pool
+    # (index 0 is ``requests``); used to keep repeated timed steps L2-cold.
+    replicas: list[list[Request]] = field(default_factory=list)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(sum(r.scheduled for r in self.requests))
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.requests)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest, ties to even); return the 16-bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    return ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+
+
+def _values(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    return x if dtype == "f32" else f32_to_bf16_bits(x)
+
+
+def _blocks_needed(tokens: int, block_size: int) -> int:
+    # number of whole blocks that hold `tokens` tokens (pool sizing only)
+    return -(-tokens // block_size)
+
+
+def _assign(perm: np.ndarray, start: int, shape: list[tuple[int, int]],
+            block_size: int) -> tuple[list[Request], int]:
+    reqs = []
+    for computed, scheduled in shape:
+        nb = _blocks_needed(computed + scheduled, block_size)
+        reqs.append(Request(computed, scheduled, [int(b) for b in perm[start:start + nb]]))
+        start += nb
+    return reqs, start
+
+
+def build(name: str, dtype: str, hq: int, hkv: int, d: int,
+          shape: list[tuple[int, int]], seed: int = 0, pool_blocks: int | None = None,
+          replicas: int = 1, scale: float | None = None, causal: bool = True,
+          lengths_drawn: bool = False, rng: np.random.Generator | None = None) -> Workload:
+    """Lay out a workload from a list of (computed, scheduled) pairs.
+
+    The pool holds ``replicas`` disjoint copies of the schedule's blocks (or
+    ``pool_blocks`` blocks if larger); the block IDs come from one random
+    permutation of the pool.
+    """
+    rng = rng if rng is not None else np.random.Generator(np.random.PCG64(seed))
+    need = sum(_blocks_needed(c + s, BLOCK_SIZE) for c, s in shape)
+    num_blocks = max(need * replicas, pool_blocks or 0)
+    perm = rng.permutation(num_blocks)
+    reps, start = [], 0
+    for _ in range(replicas):
+        reqs, start = _assign(perm, start, shape, BLOCK_SIZE)
+        reps.append(reqs)
+    n = sum(s for _, s in shape)
+    k_pool = _values(rng, (num_blocks, BLOCK_SIZE, hkv, d), dtype)
+    v_pool = _values(rng, (num_blocks, BLOCK_SIZE, hkv, d), dtype)
+    q = _values(rng, (n, hq, d), dtype)
+    k_new = _values(rng, (n, hkv, d), dtype)
+    v_new = _values(rng, (n, hkv, d), dtype)
+    return Workload(name=name, dtype=dtype, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                    num_blocks=num_blocks, requests=reps[0], q=q, k_new=k_new, v_new=v_new,
+                    k_pool=k_pool, v_pool=v_pool,
+                    softmax_scale=float(scale if scale is not None else 1.0 / np.sqrt(d)),
+                    causal=causal, replicas=reps)
+
+
+# ---------------------------------------------------------------------------
+# The five named workloads.
+# ---------------------------------------------------------------------------
+
+def tiny_mixed_f32(seed: int = 0) -> Workload:
+    """fp32, 2 q heads / 1 kv head, D = 64, 32-block pool: a 32-token prefill,
+    a decode at context 40 and a 3-token cache-hit tail on a 45-token prefix."""
+    return build("tiny_mixed_f32", "f32", 2, 1, 64, [(0, 32), (39, 1), (45, 3)],
+                 seed=seed, pool_blocks=32)
+
+
+def decode_8k(seed: int = 0, replicas: int = 1) -> Workload:
+    """bf16 batch-1 decode at context 8192, GQA 32/8, D = 128; the block table is
+    512 blocks of a randomly permuted 4096-block pool (8 disjoint replicas fit)."""
+    assert 1 <= replicas <= 8
+    return build("decode_8k", "bf16", 32, 8, 128, [(8191, 1)], seed=seed,
+                 pool_blocks=4096, replicas=replicas)
+
+
+def batched_decode_64(seed: int = 0, replicas: int = 1) -> Workload:
+    """bf16, 64 decodes with context ~ U[512, 4096], GQA 32/8, D = 128."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = rng.integers(512, 4096 + 1, size=64)
+    return build("batched_decode_64", "bf16", 32, 8, 128, [(int(c) - 1, 1) for c in ctx],
+                 replicas=replicas, rng=rng)
+
+
+def mixed_chunked(seed: int = 0, replicas: int = 1) -> Workload:
+    """bf16 flat batch: a 2048-token prefill chunk on an empty prefix, a 3-token
+    tail on a 1000-token prefix, then 62 decodes with context ~ U[256, 2048]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = rng.integers(256, 2048 + 1, size=62)
+    shape = [(0, 2048), (1000, 3)] + [(int(c) - 1, 1) for c in ctx]
+    return build("mixed_chunked", "bf16", 32, 8, 128, shape, replicas=replicas, rng=rng)
+
+
+def prefill_8k(seed: int = 0, replicas: int = 1) -> Workload:
+    """bf16 causal prefill of T = 8192 tokens, GQA 32/8, D = 128, written into
+    512 shuffled 16-token blocks."""
+    return build("prefill_8k", "bf16", 32, 8, 128, [(0, 8192)], seed=seed, replicas=replicas)
+
+
+NAMED = {
+    "tiny_mixed_f32": tiny_mixed_f32,
+    "decode_8k": decode_8k,
+    "batched_decode_64": batched_decode_64,
+    "mixed_chunked": mixed_chunked,
+    "prefill_8k": prefill_8k,
+}
+
+
+def random_small(seed: int, dtype: str = "bf16", hq: int = 4, hkv: int = 2, d: int = 128,
+                 num_seqs: int = 5, max_ctx: int = 200, max_new: int = 40,
+                 causal: bool = True, spare_blocks: int = 7) -> Workload:
+    """A random small flat batch with ragged lengths (decodes, tails, prefills,
+    empty requests) for parity sweeps."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shape = []
+    for _ in range(num_seqs):
+        kind = int(rng.integers(0, 4))
+        if kind == 0:                                  # decode
+            c = int(rng.integers(0, max_ctx))
+            shape.append((c, 1))
+        elif kind == 1:                                # short tail on a prefix
+            shape.append((int(rng.integers(0, max_ctx)), int(rng.integers(2, 5))))
+        elif kind == 2:                                # prefill chunk
+            shape.append((int(rng.integers(0, max_ctx // 2)), int(rng.integers(5, max_new + 1))))
+        else:                                          # idle request (padding row)
+            shape.append((int(rng.integers(0, max_ctx)), 0))
+    need = sum(_blocks_needed(c + s, BLOCK_SIZE) for c, s in shape)
+    return build(f"random_small_{seed}", dtype, hq, hkv, d, shape, rng=rng,
+                 pool_blocks=need + spare_blocks, causal=causal)
