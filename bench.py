@@ -1,0 +1,592 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV attention hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one flat batch: the slot-mapped
+write of the step's new K/V (``pkv_write``) followed by attention over the
+paged cache (``pkv_attention_varlen``: split-KV decode + log-sum-exp combine,
+or the tiled prefill).  The headline workload is batch-1 decode at context
+8192 (GQA 32/8, D = 128, bf16; 512 blocks of a shuffled 4096-block pool); the
+metric is KV bytes read per second.  Successive steps rotate over 8 disjoint
+block tables that tile the 268 MB pool, so every step reads its 33.5 MB of K/V
+from HBM, not from the 129 MB L2.  Steps are captured in a CUDA graph and
+replayed, the way a serving engine runs decode.
+
+Printed: one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead, on bounded samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% HBM peak); prefill attention TFLOP/s (% bf16 peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+HEADLINE = "decode_8k"
+WORKLOAD_TEXT = {
+    "decode_8k": "batch-1 decode, 1 query token at context 8192, GQA 32/8, head_dim 128, bf16, "
+                 "16-token blocks: 512-block table from a shuffled 4096-block pool",
+    "prefill_8k": "causal prefill of T=8192 tokens, GQA 32/8, head_dim 128, bf16, K/V written "
+                  "through slot_mapping into 512 shuffled 16-token blocks",
+    "batched_decode_64": "64 decodes, context U[512,4096], GQA 32/8, head_dim 128, bf16",
+    "mixed_chunked": "flat batch: 2048-token prefill chunk + 3-token tail on 1000 + 62 decodes "
+                     "U[256,2048], GQA 32/8, head_dim 128, bf16",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=8000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOAD_TEXT))
+    p.add_argument("--no-secondary", action="store_true", help="skip the prefill_8k line item")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU; replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a float over ranks (identity on one process)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Accounting (algorithmic work, counted as the method defines it)
+# ---------------------------------------------------------------------------
+
+def kv_bytes(requests, hkv, d, esize) -> int:
+    """K and V bytes the step must read: each kv head once, seq_len tokens."""
+    return sum((r.computed + r.scheduled) * hkv * d * 2 * esize for r in requests)
+
+
+def causal_flops(requests, hq, d) -> int:
+    """2 FLOPs per multiply-add of QK^T and of PV over visible (key <= query) pairs."""
+    total = 0
+    for r in requests:
+        L, n = r.computed + r.scheduled, r.scheduled
+        visible = sum(L - n + i + 1 for i in range(n))
+        total += visible * 4 * d * hq
+    return total
+
+
+def write_bytes(num_tokens, hkv, d, esize) -> int:
+    return num_tokens * hkv * d * esize * 2 * 2      # K and V, read + write
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured (MEASURED_PEAKS.json)"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = os.path.join(ROOT, "paged_kv_attention_17_gb300", "csrc", kernel_file)
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    for line in text.splitlines():
+        m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*(\d+)\s*\|\s*([0-9a-f]{16})\s*\|", line)
+        if m and m.group(1) == kernel_file and m.group(4) == digest:
+            return {"workload": m.group(2), "bytes": int(m.group(3))}
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.t0, self.t1 = index, None, None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        use = inside or rows[-3:]
+        mhz = sorted(r[1] for r in use)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "in_region": bool(inside)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def _device_replicas(w, device):
+    import numpy as np
+    import torch
+    from paged_kv_attention_17_gb300 import metadata
+
+    def tt(x):
+        if w.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+
+    common = {"q": tt(w.q), "k_new": tt(w.k_new), "v_new": tt(w.v_new),
+              "k_cache": tt(w.k_pool), "v_cache": tt(w.v_pool)}
+    reps = []
+    for reqs in w.replicas:
+        m = metadata.build(reqs, w.block_size)
+        reps.append({"meta": m, "requests": reqs,
+                     "qsl": torch.from_numpy(m["query_start_loc"]).to(device),
+                     "seq_lens": torch.from_numpy(m["seq_lens"]).to(device),
+                     "block_table": torch.from_numpy(m["block_table"]).to(device),
+                     "slot_mapping": torch.from_numpy(m["slot_mapping"]).to(device)})
+    return common, reps
+
+
+def _launches_per_step(splits, meta):
+    n = 2                                             # write + decode
+    if splits > 1:
+        n += 1                                        # combine
+    if meta["max_query_len"] > 4:
+        n += 1                                        # prefill tiles
+    return n
+
+
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import paged_kv_attention_17_gb300 as pkv
+    import workloads
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    peaks, peak_src = load_peaks()
+    name = args.workload
+    reps_wanted = 8 if name == "decode_8k" else 1
+    w = workloads.NAMED[name](replicas=reps_wanted) if name != "tiny_mixed_f32" else workloads.NAMED[name]()
+    common, reps = _device_replicas(w, device)
+    esize = 2 if w.dtype == "bf16" else 4
+    m0 = reps[0]["meta"]
+    hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
+    splits = pkv.pkv_num_splits(w.num_seqs, m0["max_query_len"], m0["max_seq_len"], hq, hkv, d,
+                                local_rank)
+    ws_bytes = pkv.pkv_workspace_bytes(w.num_seqs, hq, d, splits)
+    workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    out = torch.empty_like(common["q"])
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def write(rep):
+        pkv.pkv_write(common["k_new"], common["v_new"], rep["slot_mapping"], common["k_cache"],
+                      common["v_cache"], error_flag=flag)
+
+    def attend(rep):
+        m = rep["meta"]
+        pkv.pkv_attention_varlen(common["q"], common["k_cache"], common["v_cache"], out, rep["qsl"],
+                                 rep["seq_lens"], rep["block_table"], m["max_query_len"],
+                                 m["max_seq_len"], w.softmax_scale, causal=w.causal,
+                                 num_splits=splits, workspace=workspace, error_flag=flag)
+
+    def step(i):
+        rep = reps[i % len(reps)]
+        write(rep)
+        attend(rep)
+
+    # eager warm-up (sets kernel attributes, resolves the TMA encoder) before capture
+    for i in range(len(reps)):
+        step(i)
+    torch.cuda.synchronize()
+
+    G = len(reps)
+    use_graph = m0["max_query_len"] <= 4               # decode steps: graph, as a server runs them
+    graphs = {}
+
+    def graph_of(nsteps, body):
+        if nsteps in graphs:
+            return graphs[nsteps]
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(nsteps):
+                    body(i)
+        torch.cuda.current_stream().wait_stream(s)
+        graphs[nsteps] = g
+        return g
+
+    def run_steps(k):
+        if not use_graph:
+            for i in range(k):
+                step(i)
+            return
+        full, rest = divmod(k, G)
+        if full:
+            g = graph_of(G, step)
+            for _ in range(full):
+                g.replay()
+        if rest:
+            graph_of(rest, step).replay()
+
+    # ---- warm-up, then exactly K timed steps ----
+    run_steps(args.warmup)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    start.record()
+    run_steps(args.steps)
+    end.record()
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    barrier(world)
+    ms_total = reduce_max(start.elapsed_time(end), world, device)
+    clk = clocks.stop() if rank == 0 else None
+    if int(flag.item()) != 0:
+        raise RuntimeError(f"device error flag {int(flag.item())}")
+    ms_step = ms_total / args.steps
+    bytes_step = kv_bytes(w.requests, hkv, d, esize)
+    flops_step = causal_flops(w.requests, hq, d)
+    decode_like = m0["max_query_len"] <= 4
+    per_rank_value = (bytes_step / 1e9) / (ms_step / 1e3) if decode_like else (flops_step / 1e12) / (ms_step / 1e3)
+    value = per_rank_value * world
+
+    # ---- the dominant kernel alone: attention calls back to back, events around ----
+    nat = 400 if decode_like else 3
+    att_body = lambda i: attend(reps[i % len(reps)])  # noqa: E731
+    if use_graph:
+        ga = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(ga, stream=s):
+                for i in range(G):
+                    att_body(i)
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(20):
+            ga.replay()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    if use_graph:
+        for _ in range(nat):
+            ga.replay()
+        calls = nat * G
+    else:
+        for i in range(nat):
+            att_body(i)
+        calls = nat
+    a1.record()
+    torch.cuda.synchronize()
+    att_ms = a0.elapsed_time(a1) / calls
+    if decode_like:
+        achieved = (bytes_step / 1e9) / (att_ms / 1e3)
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4)}
+        kernel_file = "decode.cu"
+    else:
+        achieved = (flops_step / 1e12) / (att_ms / 1e3)
+        peak = float(peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4)}
+        kernel_file = "prefill.cu"
+    tr = traffic_record(kernel_file)
+    roof["traffic"] = tr["bytes"] if tr and tr["workload"] == name else None
+    roof["kernel"] = ("pkv_attention_varlen call (split-KV decode kernel + LSE combine), "
+                      f"{splits} splits" if decode_like else "pkv_attention_varlen call (prefill)")
+    roof["peak_source"] = peak_src
+    roof["ms_per_launch"] = round(att_ms, 6)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, flops_step,
+                  decode_like)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2),
+        "unit": "GB/s" if decode_like else "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1) PCG64(0), cast to bf16 (RNE)",
+        "config": {"workload": f"{name}: {WORKLOAD_TEXT[name]}", "num_splits": splits,
+                   "kv_bytes_per_step": bytes_step, "flops_per_step": flops_step,
+                   "l2": ("cold: steps rotate over 8 disjoint 512-block tables of a 268 MB pool"
+                          if name == "decode_8k" else "inputs larger than L2"),
+                   "cuda_graph": use_graph, "parallelism": f"replicas x{world}"},
+        "roofline": roof, "e2e": e2e,
+        "gpu_launches": _launches_per_step(splits, m0) * args.steps,
+    }
+    if clk is not None:
+        result["clocks"] = clk
+    return result, w
+
+
+def run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, flops_step,
+            decode_like):
+    """Per step: pinned host -> device copies of the step's inputs (Q, new K/V,
+    metadata), the two API calls, device -> host copy of the output."""
+    import torch
+
+    import paged_kv_attention_17_gb300 as pkv
+    host = {k: common[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+    hreps = [{k: r[k].cpu().pin_memory() for k in ("qsl", "seq_lens", "block_table", "slot_mapping")}
+             for r in reps]
+    dq = torch.empty_like(common["q"])
+    dk, dv = torch.empty_like(common["k_new"]), torch.empty_like(common["v_new"])
+    dmeta = {k: torch.empty_like(reps[0][k]) for k in ("qsl", "seq_lens", "block_table", "slot_mapping")}
+    out = torch.empty_like(common["q"])
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def one(i):
+        hr, m = hreps[i % len(hreps)], reps[i % len(reps)]["meta"]
+        dq.copy_(host["q"], non_blocking=True)
+        dk.copy_(host["k_new"], non_blocking=True)
+        dv.copy_(host["v_new"], non_blocking=True)
+        for k in dmeta:
+            dmeta[k].copy_(hr[k], non_blocking=True)
+        pkv.pkv_write(dk, dv, dmeta["slot_mapping"], common["k_cache"], common["v_cache"],
+                      error_flag=flag)
+        pkv.pkv_attention_varlen(dq, common["k_cache"], common["v_cache"], out, dmeta["qsl"],
+                                 dmeta["seq_lens"], dmeta["block_table"], m["max_query_len"],
+                                 m["max_seq_len"], w.softmax_scale, causal=w.causal,
+                                 num_splits=splits, workspace=workspace, error_flag=flag)
+        hout.copy_(out, non_blocking=True)
+
+    k = min(args.steps, 2000) if decode_like else max(1, min(args.steps, 5))
+    for i in range(min(20, k)):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(k):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / k
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        sum(t.numel() * t.element_size() for t in hreps[0].values())
+    d2h = hout.numel() * hout.element_size()
+    val = (bytes_step / 1e9) / (ms / 1e3) if decode_like else (flops_step / 1e12) / (ms / 1e3)
+    return {"value": round(val, 2), "unit": "GB/s" if decode_like else "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
+            "ms_per_step": round(ms, 6), "mode": "eager API calls, pinned host buffers"}
+
+
+def run_secondary_prefill(local_rank):
+    """prefill_8k: TFLOP/s of the causal prefill step (write + attention)."""
+    import torch
+    args = parse_args(["--workload", "prefill_8k", "--steps", "5", "--warmup", "2"])
+    res, _ = run_gpu(args, 0, 1, local_rank)
+    torch.cuda.synchronize()
+    return {"workload": res["config"]["workload"], "value": res["value"], "unit": res["unit"],
+            "ms_per_step": res["ms_per_step"], "roofline": res["roofline"], "e2e": res["e2e"]}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: the reference arm and the cpu_baseline
+# ---------------------------------------------------------------------------
+
+def oracle_sampler(name):
+    """Return (w, cache, run(sample_keys) -> bytes) for timing the oracle on
+    a bounded sample: its two-pass attention of the workload's decode rows over
+    the first `sample_keys` keys of each context (cache already written by the
+    oracle's scatter, which is not timed)."""
+    import workloads
+    from oracle import flatten as ofl
+    from oracle import ref
+    w = workloads.NAMED[name]()
+    meta = ofl.flatten(w.requests)
+    kc = ofl.write(w.k_pool, w.k_new, meta["slot_mapping"])
+    vc = ofl.write(w.v_pool, w.v_new, meta["slot_mapping"])
+    esize = 2 if w.dtype == "bf16" else 4
+
+    def run(sample_keys):
+        import numpy as np
+        from types import SimpleNamespace
+        reqs = []
+        for r in w.requests:
+            L = min(r.computed + r.scheduled, max(sample_keys, r.scheduled))
+            reqs.append(SimpleNamespace(computed=L - r.scheduled, scheduled=r.scheduled,
+                                        blocks=r.blocks))
+        m = ofl.flatten(reqs)
+        ref.attention(w.q, kc, vc, m["query_start_loc"], m["seq_lens"], m["block_table"],
+                      num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                      softmax_scale=w.softmax_scale, causal=w.causal, dtype=w.dtype)
+        return kv_bytes(reqs, w.num_kv_heads, w.head_dim, esize), causal_flops(
+            reqs, w.num_q_heads, w.head_dim)
+    full_keys = max(r.computed + r.scheduled for r in w.requests)
+    return w, run, full_keys
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(name, seconds):
+    w, run, full = oracle_sampler(name)
+    t = time.perf_counter()
+    run(full)
+    t_full = time.perf_counter() - t
+    reps = max(1, int(seconds / max(t_full, 1e-3)))
+    t = time.perf_counter()
+    tot_b = tot_f = 0
+    for _ in range(reps):
+        b, f = run(full)
+        tot_b, tot_f = tot_b + b, tot_f + f
+    dt = time.perf_counter() - t
+    decode_like = max(r.scheduled for r in w.requests) <= 4
+    val = (tot_b / 1e9) / dt if decode_like else (tot_f / 1e12) / dt
+    return {"value": round(val, 4), "unit": "GB/s" if decode_like else "TFLOP/s",
+            "cores": cores_used(), "kind": "oracle",
+            "sample": f"{reps} x full {name} step of oracle.ref.attention (float64 numpy, default "
+                      f"BLAS threads) over the cache the oracle scatter wrote; scatter untimed"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    name = args.workload
+    w, run, full = oracle_sampler(name)
+    t = time.perf_counter()
+    run(full)
+    t_full = time.perf_counter() - t
+    budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
+    keys = full if t_full <= budget else max(16, int(full * budget / t_full) // 16 * 16)
+    for _ in range(args.warmup):
+        run(keys)
+    t = time.perf_counter()
+    tot_b = tot_f = 0
+    for _ in range(args.steps):
+        b, f = run(keys)
+        tot_b, tot_f = tot_b + b, tot_f + f
+    dt = time.perf_counter() - t
+    decode_like = max(r.scheduled for r in w.requests) <= 4
+    val = (tot_b / 1e9) / dt if decode_like else (tot_f / 1e12) / dt
+    unit = "GB/s" if decode_like else "TFLOP/s"
+    sample = (f"each step: oracle.ref.attention of {name}'s rows over the first {keys} of "
+              f"{full} context keys (float64 numpy), cache written once by the oracle scatter")
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{name}: {WORKLOAD_TEXT[name]}"},
+            "cpu_baseline": {"value": round(val, 4), "unit": unit, "cores": cores_used(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 4), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" and torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, rank, world)
+            if res is not None:
+                print(json.dumps(res), flush=True)
+            return 0
+        result, w = run_gpu(args, rank, world, local_rank)
+        if rank == 0 and world == 1 and not args.no_secondary and args.workload == HEADLINE:
+            result["prefill"] = run_secondary_prefill(local_rank)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+        return 0
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

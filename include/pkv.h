@@ -1,0 +1,170 @@
+/*
+ * pkv.h - C ABI of the paged KV attention library for GB300 (sm_103a).
+ *
+ * What it computes.  Exact softmax attention of every new token of a flat,
+ * variable-length serving batch over its request's context, where the context
+ * K/V live in a paged cache of 16-token blocks named by per-request block
+ * tables, plus the slot-mapped write of the new tokens' K/V into that cache.
+ * The batch description follows "Model execution" (vLLM internals notes),
+ * section "Flattening a step": query_start_loc, seq_lens, block_table and
+ * slot_mapping; the method follows "Inside the engine: kernels, CUDA graphs
+ * and the life of a request", sections "Never materialise the TxT matrix"
+ * (online softmax), "Prefill has a full grid; decode at batch 1 has almost
+ * none" (split-KV partials merged by a second reduction kernel) and
+ * "Attention over a block table, not a contiguous tensor" (16-token blocks
+ * gathered through a block table).
+ *
+ * Conventions for every entry point.
+ *   - Device pointers are CUDA device addresses on the current device; the
+ *     caller allocates and owns every buffer.  The library never allocates,
+ *     frees or synchronises: each call validates its host arguments, enqueues
+ *     kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     returns.  All pointers to tensors must be 16-byte aligned.
+ *   - Host-checkable errors return a status and enqueue nothing.
+ *   - Data-dependent errors (a block ID or slot outside the cache, a request
+ *     with more new tokens than context, a query_start_loc that is not a
+ *     valid prefix sum) cannot be seen on the host without a sync.  Kernels
+ *     skip the offending access, never trap, and OR a PKV_FLAG_* bit into
+ *     *error_flag (a device int32 the caller zeroes and reads later) when
+ *     error_flag is non-NULL.  Outputs of the affected rows are unspecified.
+ *   - Tensors are dense and row-major in the shapes given; the KV cache is
+ *     two tensors (K and V), each [num_blocks, block_size, num_kv_heads,
+ *     head_dim], i.e. [num_slots, num_kv_heads, head_dim] with
+ *     slot = block_id * block_size + offset.
+ *   - Supported: block_size 16; head_dim 64 or 128; num_q_heads a multiple of
+ *     num_kv_heads; dtype PKV_F32 or PKV_BF16 (same dtype for Q, K, V and
+ *     the output).  Arithmetic is fp32 with fp32 accumulation.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size or count */
+    PKV_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+    PKV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+    PKV_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+    PKV_ERR_DEVICE_CHECK = 5,   /* reserved for callers mapping *error_flag */
+    PKV_ERR_DEVICE_TIMEOUT = 6  /* reserved for callers mapping *error_flag */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits a kernel ORs into *error_flag. */
+#define PKV_FLAG_BAD_BLOCK   1  /* block_table entry outside [0, num_blocks) */
+#define PKV_FLAG_BAD_SLOT    2  /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_FLAG_BAD_LENGTHS 4  /* q_len > seq_len, q_len > max_query_len,
+                                   seq_len > max_blocks_per_seq * block_size, or
+                                   query_start_loc not a prefix sum ending at
+                                   num_tokens */
+#define PKV_FLAG_TIMEOUT     8  /* a pipeline wait gave up (about 2 s bound) */
+
+/* Requests with at most this many new tokens take the split-KV decode path;
+ * longer ones take the tiled prefill path. */
+#define PKV_DECODE_MAX_QLEN 4
+
+/*
+ * pkv_write - store each new token's K and V at its slot.
+ *
+ * "Model execution", section "Flattening a step": slot_mapping gives, per new
+ * token, the physical slot block_id * block_size + offset its K and V go to;
+ * "Inside the engine ...", section "Attention over a block table ...": the
+ * KV-write kernel scatters into non-contiguous blocks.
+ *
+ *   k_new, v_new   device, [num_tokens, num_kv_heads, head_dim], dtype.
+ *   slot_mapping   device int64 [num_tokens]; a negative slot (a padding
+ *                  token) is skipped; a slot >= num_blocks * block_size is
+ *                  skipped and flagged PKV_FLAG_BAD_SLOT.
+ *   k_cache, v_cache  device, [num_blocks, block_size, num_kv_heads, head_dim].
+ *   error_flag     device int32 or NULL.
+ * Slots not named by slot_mapping keep their contents.  Two tokens naming
+ * the same slot leave either one's row there (unspecified which).
+ * num_tokens == 0 is a no-op returning PKV_OK.
+ */
+pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                     int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                     int block_size, int num_kv_heads, int head_dim, pkv_dtype dtype,
+                     int32_t* error_flag, void* stream);
+
+/*
+ * pkv_num_splits - how many KV splits the decode path should use.
+ *
+ * "Inside the engine ...", section "Prefill has a full grid; decode at batch 1
+ * has almost none": split the KV axis when there are too few query rows to
+ * fill the GPU; at high batch the grid is already full and the split is
+ * turned off.  Returns 1 once the decode grid (num_seqs x num_kv_heads work
+ * units) fills the device `device` (SM count from its properties), otherwise
+ * enough splits to fill it, with at least 8 blocks (128 keys) per split and at
+ * most 64 splits.  Returns 0 for invalid arguments or device.
+ */
+int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_heads,
+                   int num_kv_heads, int head_dim, int device);
+
+/*
+ * pkv_workspace_bytes - device workspace pkv_attention_varlen needs.
+ *
+ * Holds the split-KV partials of the decode path: for every split, request,
+ * decode row (< PKV_DECODE_MAX_QLEN) and query head, an fp32 partial output
+ * [head_dim] and its log-sum-exp.  0 when num_splits <= 1.
+ */
+size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_splits);
+
+/*
+ * pkv_attention_varlen - attention of a flat varlen batch over the paged cache.
+ *
+ * For request r (0 <= r < num_seqs), n = query_start_loc[r+1] -
+ * query_start_loc[r] new tokens occupy rows query_start_loc[r]..+n-1 of q and
+ * out, and L = seq_lens[r] is its context after this step (its new tokens
+ * already written, e.g. by pkv_write).  New token i is at position
+ * p = L - n + i; with causal != 0 it attends keys 0..p, otherwise all L keys.
+ * Key j of request r is cache row block_table[r * max_blocks_per_seq + j/16]
+ * * 16 + j % 16, kv head h / (num_q_heads / num_kv_heads) for query head h.
+ *   out[t, h, :] = sum_j softmax_j(softmax_scale * q[t,h,:] . k_j) v_j
+ * computed as an online softmax over key tiles ("Never materialise the TxT
+ * matrix"); requests with n <= PKV_DECODE_MAX_QLEN take the split-KV decode
+ * kernel (partials merged by a log-sum-exp combine kernel when num_splits >
+ * 1), longer ones the tiled prefill kernel.
+ *
+ *   q, out            device [num_tokens, num_q_heads, head_dim], dtype.
+ *   lse_out           device fp32 [num_tokens, num_q_heads] or NULL: natural-log
+ *                     log-sum-exp of each row's scaled scores (-inf if the row
+ *                     sees no key).
+ *   k_cache, v_cache  device [num_blocks, 16, num_kv_heads, head_dim], dtype.
+ *   query_start_loc   device int32 [num_seqs + 1], nondecreasing, [0] = 0,
+ *                     [num_seqs] = num_tokens.
+ *   seq_lens          device int32 [num_seqs].
+ *   block_table       device int32 [num_seqs, max_blocks_per_seq].
+ *   max_query_len     host: >= every n (bounds the prefill grid).
+ *   max_seq_len       host: >= every L (used by the split heuristic only).
+ *   num_splits        0 = pkv_num_splits(...); else 1..64.
+ *   workspace         device, >= pkv_workspace_bytes(num_seqs, num_q_heads,
+ *                     head_dim, splits) bytes, 256-byte aligned; may be NULL
+ *                     when that is 0.  Contents need no initialisation.
+ * Rows of requests with n == 0 are absent; a request with L == 0 and n == 0
+ * is a no-op.  Returns PKV_OK once the kernels are enqueued.
+ */
+pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                void* out, float* lse_out, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, const int32_t* block_table,
+                                int max_blocks_per_seq, int num_seqs, int64_t num_tokens,
+                                int max_query_len, int max_seq_len, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size,
+                                float softmax_scale, int causal, int num_splits,
+                                void* workspace, size_t workspace_bytes, int32_t* error_flag,
+                                int64_t num_blocks, pkv_dtype dtype, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* pkv_status_string(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

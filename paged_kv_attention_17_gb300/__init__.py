@@ -1,0 +1,15 @@
+"""Paged KV attention for GB300 (sm_103a).
+
+Exact softmax attention over a paged KV cache of 16-token blocks for a
+flattened, variable-length serving batch, plus the slot-mapped KV write.  The
+compute runs in hand-written CUDA kernels behind the C ABI of
+``include/pkv.h`` (``_lib/libpkv.so``); this package is its Python binding
+(``pkv_write``, ``pkv_attention_varlen``, ``pkv_num_splits``,
+``pkv_workspace_bytes``, ``pkv_status_string``) and the runner-side metadata
+builder (``metadata.build``).  PyTorch supplies device memory and streams.
+"""
+
+from . import metadata  # noqa: F401
+from ._binding import (EXPORTS, FLAG_BAD_BLOCK, FLAG_BAD_LENGTHS, FLAG_BAD_SLOT,  # noqa: F401
+                       FLAG_TIMEOUT, PKV_DECODE_MAX_QLEN, PkvError, lib, pkv_attention_varlen,
+                       pkv_num_splits, pkv_status_string, pkv_workspace_bytes, pkv_write)

@@ -1,0 +1,138 @@
+"""ctypes binding of ``libpkv.so`` (the C ABI declared in ``include/pkv.h``).
+
+Argument marshalling only: each wrapper reads pointers, shapes and the current
+CUDA stream from torch tensors and calls the C entry point of the same name;
+every step of the computation runs in the library's CUDA kernels.  There is no
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpkv.so")
+_lib = None
+
+PKV_OK = 0
+PKV_F32, PKV_BF16 = 0, 1
+PKV_DECODE_MAX_QLEN = 4
+FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
+
+# Every symbol include/pkv.h declares.
+EXPORTS = ("pkv_write", "pkv_num_splits", "pkv_workspace_bytes", "pkv_attention_varlen",
+           "pkv_status_string")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, func, code):
+        super().__init__(f"{func} returned {code} ({status_string(code)})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"CUDA library not built: {_LIB_PATH} is missing "
+                              "(run paged_kv_attention_17_gb300.build.build())")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        L.pkv_write.argtypes = [vp, vp, vp, i64, vp, vp, i64, i32, i32, i32, i32, vp, vp]
+        L.pkv_write.restype = i32
+        L.pkv_num_splits.argtypes = [i32] * 7
+        L.pkv_num_splits.restype = i32
+        L.pkv_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.pkv_workspace_bytes.restype = sz
+        L.pkv_attention_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32, i32,
+                                           i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, sz,
+                                           vp, i64, i32, vp]
+        L.pkv_attention_varlen.restype = i32
+        L.pkv_status_string.argtypes = [i32]
+        L.pkv_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().pkv_status_string(int(code)).decode()
+
+
+pkv_status_string = status_string
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return PKV_F32
+    if t == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(func, code):
+    if code != PKV_OK:
+        raise PkvError(func, code)
+
+
+def pkv_write(k_new, v_new, slot_mapping, k_cache, v_cache, error_flag=None, stream=None):
+    """Store k_new[t] / v_new[t] ([N, Hkv, D]) at cache slot slot_mapping[t] (int64)."""
+    nb, bs, hkv, d = k_cache.shape
+    code = lib().pkv_write(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping), int(slot_mapping.numel()),
+                           _ptr(k_cache), _ptr(v_cache), int(nb), int(bs), int(hkv), int(d),
+                           _dtype_code(k_cache.dtype), _ptr(error_flag), _stream(stream))
+    _check("pkv_write", code)
+
+
+def pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                   device=None) -> int:
+    dev = torch.cuda.current_device() if device is None else int(device)
+    return int(lib().pkv_num_splits(int(num_seqs), int(max_query_len), int(max_seq_len),
+                                    int(num_q_heads), int(num_kv_heads), int(head_dim), dev))
+
+
+def pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, num_splits) -> int:
+    return int(lib().pkv_workspace_bytes(int(num_seqs), int(num_q_heads), int(head_dim),
+                                         int(num_splits)))
+
+
+def pkv_attention_varlen(q, k_cache, v_cache, out, query_start_loc, seq_lens, block_table,
+                         max_query_len, max_seq_len, softmax_scale, causal=True, num_splits=0,
+                         workspace=None, lse_out=None, error_flag=None, stream=None):
+    """Attention of the flat batch q [N, Hq, D] over the paged cache into out.
+
+    Metadata tensors are int32 on the device.  ``workspace`` is a uint8 device
+    tensor of at least ``pkv_workspace_bytes(...)`` bytes; if None and one is
+    needed it is allocated with torch here (allocate it yourself to capture the
+    call in a CUDA graph).
+    """
+    n_tok, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    num_seqs = int(seq_lens.numel())
+    splits = int(num_splits)
+    if splits == 0 and num_seqs > 0:
+        splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, hq, hkv, d, q.device.index)
+    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().pkv_attention_varlen(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
+        _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]), num_seqs, int(n_tok),
+        int(max_query_len), int(max_seq_len), int(hq), int(hkv), int(d), int(bs),
+        float(softmax_scale), 1 if causal else 0, splits, _ptr(workspace), int(ws_bytes),
+        _ptr(error_flag), int(nb), _dtype_code(q.dtype), _stream(stream))
+    _check("pkv_attention_varlen", code)
+    return out

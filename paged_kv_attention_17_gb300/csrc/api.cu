@@ -1,0 +1,253 @@
+// C ABI of the paged KV attention library: host-side validation, the split
+// heuristic, workspace sizing, TMA descriptor encoding and kernel launches.
+// Every entry point only enqueues work on the caller's stream: no allocation,
+// no synchronisation, no host read of device data.
+#include <cmath>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace pkv {
+cudaError_t launch_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
+                            int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_slots,
+                            uint32_t row_bytes, int32_t* flag, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          bool bf16, int head_dim, bool pdl, cudaStream_t stream);
+cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStream_t stream);
+int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
+bool prefill_supported(int head_dim, bool bf16);
+cudaError_t launch_prefill(const AttnArgs& a, const void* k_cache, const void* v_cache,
+                           int head_dim, cudaStream_t stream);
+}  // namespace pkv
+
+using namespace pkv;
+
+namespace {
+
+constexpr int kDecodeCtasPerSm = 2;      // resident decode CTAs per SM (shared-memory bound)
+constexpr int kMinBlocksPerSplit = 8;    // 128 keys
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int device_sms(int device) {
+  static int cache[64] = {0};
+  if (device < 0 || device >= 64) return 0;
+  if (cache[device] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[device] = v;
+  }
+  return cache[device];
+}
+
+int current_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return device_sms(dev);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// 3-D map over one cache tensor viewed as [num_slots, num_kv_heads, head_dim]
+// (innermost first for TMA): a box is 16 slots x 1 head x head_dim, i.e. one
+// block of one kv head.
+bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_slots, int hkv, int d,
+                      bool bf16) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t es = bf16 ? 2 : 4;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                        static_cast<cuuint64_t>(num_slots)};
+  cuuint64_t strides[2] = {d * es, static_cast<cuuint64_t>(hkv) * d * es};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1, static_cast<cuuint32_t>(kBlock)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool valid_dtype(pkv_dtype dt) { return dt == PKV_F32 || dt == PKV_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK";
+    case PKV_ERR_DEVICE_TIMEOUT: return "PKV_ERR_DEVICE_TIMEOUT";
+  }
+  return "PKV_UNKNOWN_STATUS";
+}
+
+pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                     int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                     int block_size, int num_kv_heads, int head_dim, pkv_dtype dtype,
+                     int32_t* error_flag, void* stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1 || !valid_dtype(dtype))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlock) return PKV_ERR_UNSUPPORTED;
+  const int64_t row_bytes = static_cast<int64_t>(num_kv_heads) * head_dim * (dtype == PKV_BF16 ? 2 : 4);
+  if (row_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8) || (error_flag && !aligned(error_flag, 4)))
+    return PKV_ERR_INVALID_ARG;
+  const int sms = current_sms();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  cudaError_t e = launch_kv_write(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache,
+                                  num_blocks * kBlock, static_cast<uint32_t>(row_bytes), error_flag,
+                                  sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_heads,
+                   int num_kv_heads, int head_dim, int device) {
+  (void)head_dim;
+  if (num_seqs < 1 || max_seq_len < 0 || max_query_len < 0 || num_q_heads < 1 ||
+      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return 0;
+  const int sms = device_sms(device);
+  if (sms <= 0) return 0;
+  const int group = num_q_heads / num_kv_heads;
+  const int qd = max_query_len < kDecodeMaxQ ? (max_query_len < 1 ? 1 : max_query_len) : kDecodeMaxQ;
+  const int R = decode_rows_per_tile(group, qd, false);
+  const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((group * qd + R - 1) / R);
+  const int64_t capacity = static_cast<int64_t>(sms) * kDecodeCtasPerSm;
+  if (units >= capacity) return 1;                     // grid already full: no split
+  int64_t s = (capacity + units - 1) / units;
+  const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kBlock - 1) / kBlock;
+  int64_t by_len = nblk / kMinBlocksPerSplit;
+  if (by_len < 1) by_len = 1;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
+size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_splits) {
+  if (num_splits <= 1 || num_seqs < 1 || num_q_heads < 1 || head_dim < 1) return 0;
+  const size_t rows = static_cast<size_t>(num_splits) * num_seqs * kDecodeMaxQ * num_q_heads;
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* v_cache, void* out,
+                                float* lse_out, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, const int32_t* block_table,
+                                int max_blocks_per_seq, int num_seqs, int64_t num_tokens,
+                                int max_query_len, int max_seq_len, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size,
+                                float softmax_scale, int causal, int num_splits, void* workspace,
+                                size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+                                pkv_dtype dtype, void* stream) {
+  // ---- host-checkable arguments ----
+  if (!valid_dtype(dtype) || num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
+      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_splits < 0 ||
+      num_splits > kMaxSplits || num_blocks < 1 || max_seq_len < 0 || max_query_len < 0 ||
+      !std::isfinite(softmax_scale))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlock || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
+  if (max_query_len < 1 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !out || !query_start_loc || !seq_lens || !block_table)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(query_start_loc, 4) || !aligned(seq_lens, 4) || !aligned(block_table, 4) ||
+      (lse_out && !aligned(lse_out, 4)) || (error_flag && !aligned(error_flag, 4)))
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  const int64_t num_slots = num_blocks * kBlock;
+  if (num_slots > 0xFFFFFFFFll) return PKV_ERR_UNSUPPORTED;
+
+  int splits = num_splits;
+  if (splits == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
+                            head_dim, dev);
+  }
+  if (splits < 1) return PKV_ERR_CUDA;
+  const size_t need = pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return PKV_ERR_WORKSPACE;
+
+  const bool bf16 = dtype == PKV_BF16;
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.out = out;
+  a.lse_out = lse_out;
+  a.qsl = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_query_len = max_query_len;
+  a.hq = num_q_heads;
+  a.hkv = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.causal = causal ? 1 : 0;
+  a.num_splits = splits;
+  const bool tc_prefill = prefill_supported(head_dim, bf16);
+  a.long_rows = tc_prefill ? 0 : 1;
+  if (need > 0) {
+    const size_t rows = static_cast<size_t>(splits) * num_seqs * kDecodeMaxQ * num_q_heads;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        align256(rows * head_dim * sizeof(float)));
+  }
+  a.flag = error_flag;
+  a.num_blocks = num_blocks;
+
+  CUtensorMap kmap, vmap;
+  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, bf16) ||
+      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, bf16))
+    return PKV_ERR_CUDA;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(a, kmap, vmap, bf16, head_dim, /*pdl=*/true, st);
+  if (e == cudaSuccess && splits > 1) e = launch_combine(a, bf16, head_dim, st);
+  if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ)
+    e = launch_prefill(a, k_cache, v_cache, head_dim, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

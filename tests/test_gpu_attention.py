@@ -1,0 +1,213 @@
+"""pkv_attention_varlen on the GPU against the float64 oracle.
+
+Acceptance: max |err| <= 1e-2 and mean |err| <= 1e-3 for bf16 inputs with
+fp32 accumulation (output rounded to bf16); fp32 inputs are held to 1e-4 /
+1e-5.  Small workloads are compared element by element; the full-size
+workloads run in the configuration the benchmark times (automatic split count)
+and are compared on every row the oracle can afford (all decode rows, sampled
+prefill rows including block and tile boundaries).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import ref
+from tests.harness import device_inputs, errors, run_step
+
+import paged_kv_attention_17_gb300 as pkv
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": (1e-2, 1e-3), "f32": (1e-4, 1e-5)}
+
+
+def _check(out, o_ref, dtype, tokens=None):
+    mx, mean = errors(out, o_ref, tokens)
+    tmax, tmean = TOL[dtype]
+    assert mx <= tmax and mean <= tmean, (mx, mean)
+    return mx, mean
+
+
+def _check_lse(lse, lse_ref, tokens=None):
+    got = lse.cpu().double().numpy()
+    if tokens is not None:
+        got, lse_ref = got[tokens], lse_ref[tokens]
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    assert np.abs(got[fin] - lse_ref[fin]).max() <= 1e-3
+
+
+# --------------------------------------------------------------------------
+# Small ragged batches: every element
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("dtype,hq,hkv,d", [
+    ("bf16", 8, 2, 128), ("bf16", 4, 4, 64), ("bf16", 32, 8, 128), ("f32", 2, 1, 64),
+    ("f32", 4, 1, 128), ("bf16", 16, 1, 128)])
+def test_random_small_batches(seed, dtype, hq, hkv, d):
+    w = workloads.random_small(seed, dtype=dtype, hq=hq, hkv=hkv, d=d, num_seqs=6)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    _check(out, o_ref, dtype)
+    _check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_non_causal(seed):
+    w = workloads.random_small(seed + 40, dtype="bf16", hq=8, hkv=2, d=128, causal=False)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    _check_lse(lse, lse_ref)
+
+
+def test_tiny_mixed_f32_every_element():
+    w = workloads.tiny_mixed_f32()
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "f32")
+    _check_lse(lse, lse_ref)
+
+
+# --------------------------------------------------------------------------
+# Full-size workloads in the benchmark's launch configuration
+# --------------------------------------------------------------------------
+
+def _sample_prefill_tokens(start, n, rng, k=40):
+    fixed = [0, 1, 15, 16, 17, 127, 128, 129, n // 2, n - 2, n - 1]
+    extra = rng.integers(0, n, size=k).tolist()
+    return sorted({start + t for t in fixed + extra if 0 <= t < n})
+
+
+@pytest.mark.parametrize("name", ["decode_8k", "batched_decode_64"])
+def test_full_size_decode_all_rows(name):
+    w = workloads.NAMED[name]()
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    _check_lse(lse, lse_ref)
+
+
+def test_full_size_mixed_chunked_sampled():
+    w = workloads.mixed_chunked()
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    rng = np.random.default_rng(0)
+    toks = _sample_prefill_tokens(0, 2048, rng) + list(range(2048, w.num_tokens))
+    o_ref, lse_ref, *_ = ref.paged_step(w, tokens=toks)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16", toks)
+    _check_lse(lse, lse_ref, toks)
+
+
+def test_full_size_prefill_8k_sampled():
+    w = workloads.prefill_8k()
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    rng = np.random.default_rng(1)
+    toks = _sample_prefill_tokens(0, 8192, rng, k=24) + [4095, 4096, 8064, 8065]
+    toks = sorted(set(toks))
+    o_ref, lse_ref, *_ = ref.paged_step(w, tokens=toks)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16", toks)
+    _check_lse(lse, lse_ref, toks)
+
+
+# --------------------------------------------------------------------------
+# Invariances the pages state
+# --------------------------------------------------------------------------
+
+def test_split_count_changes_nothing():
+    # "split-KV ... changes nothing about the result"
+    w = workloads.decode_8k()
+    dev = device_inputs(w)
+    o_ref, *_ = ref.paged_step(w)
+    outs = []
+    for s in (1, 2, 3, 7, 0, 64):
+        out, lse, flag = run_step(dev, num_splits=s, write=(s == 1))
+        assert int(flag.item()) == 0
+        _check(out, o_ref, "bf16")
+        outs.append(out.float().cpu().numpy())
+    for a in outs:
+        for b in outs:
+            assert np.abs(a - b).max() <= 1e-3 + 2 ** -7 * np.abs(a).max()
+
+
+def test_block_permutation_is_bit_identical():
+    # "paging changes only the access pattern": relocate every physical block
+    # and rewrite the tables; with a fixed split count the result is identical
+    w = workloads.random_small(21, dtype="bf16", hq=8, hkv=2, d=128, num_seqs=8, max_ctx=400)
+    dev = device_inputs(w)
+    out1, lse1, _ = run_step(dev, num_splits=3)
+    perm = torch.from_numpy(np.random.default_rng(2).permutation(w.num_blocks)).cuda()
+    kc2, vc2 = torch.empty_like(dev["k_cache"]), torch.empty_like(dev["v_cache"])
+    kc2[perm] = dev["k_cache"]
+    vc2[perm] = dev["v_cache"]
+    dev2 = dict(dev, k_cache=kc2, v_cache=vc2, block_table=perm[dev["block_table"].long()].int())
+    out2, lse2, _ = run_step(dev2, num_splits=3, write=False)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
+def test_single_key_returns_v_exactly():
+    # a request whose first token is its whole context sees one key: out == v
+    w = workloads.build("single", "bf16", 8, 2, 128, [(0, 1), (0, 1), (5, 1)], seed=3)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    v = dev["v_new"]
+    for t in (0, 1):
+        for h in range(8):
+            assert torch.equal(out[t, h].view(torch.int16), v[t, h // 4].view(torch.int16))
+
+
+def test_empty_and_idle_requests():
+    w = workloads.build("idle", "bf16", 8, 2, 128, [(30, 0), (0, 0), (17, 2), (40, 0)], seed=4)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    # an empty batch enqueues nothing and succeeds
+    e = torch.empty(0, 8, 128, dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.pkv_attention_varlen(e, dev["k_cache"], dev["v_cache"], e, z, torch.zeros(0, dtype=torch.int32, device="cuda"),
+                             dev["block_table"][:0], 0, 0, 0.1)
+
+
+# --------------------------------------------------------------------------
+# Data-dependent errors: flagged on the device, never a fault
+# --------------------------------------------------------------------------
+
+def test_bad_block_id_is_flagged():
+    w = workloads.random_small(5, dtype="bf16", hq=8, hkv=2, d=128, num_seqs=4)
+    dev = device_inputs(w)
+    run_step(dev)
+    bt = dev["block_table"].clone()
+    bt[:, 0] = w.num_blocks + 1000
+    dev2 = dict(dev, block_table=bt)
+    out, lse, flag = run_step(dev2, write=False)
+    torch.cuda.synchronize()
+    assert int(flag.item()) & pkv.FLAG_BAD_BLOCK
+
+
+def test_query_longer_than_context_is_flagged():
+    w = workloads.build("bad", "bf16", 8, 2, 128, [(10, 3), (20, 1)], seed=6)
+    dev = device_inputs(w)
+    run_step(dev)
+    sl = dev["seq_lens"].clone()
+    sl[0] = 2                                        # q_len 3 > seq_len 2
+    out, lse, flag = run_step(dict(dev, seq_lens=sl), write=False)
+    torch.cuda.synchronize()
+    assert int(flag.item()) & pkv.FLAG_BAD_LENGTHS

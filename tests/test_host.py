@@ -1,0 +1,141 @@
+"""Host-side checks that need no GPU: the library builds, loads and exports
+every symbol of include/pkv.h; the runner-side metadata builder reproduces the
+page's printed flatten example and agrees with the oracle's builder; workspace
+sizing and host validation return the documented statuses without enqueuing
+anything."""
+
+import ctypes
+import json
+import os
+import re
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+
+import workloads
+from oracle import flatten as oracle_flatten
+from paged_kv_attention_17_gb300 import build as pkv_build
+from paged_kv_attention_17_gb300 import metadata
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    pkv_build.build()
+    import paged_kv_attention_17_gb300 as p
+    p.lib()
+    return p
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_header_symbol(pkv):
+    names = _header_functions()
+    assert names == sorted(pkv.EXPORTS)
+    for n in names:
+        assert hasattr(pkv.lib(), n), n
+
+
+def test_status_strings(pkv):
+    assert pkv.pkv_status_string(0) == "PKV_OK"
+    assert pkv.pkv_status_string(3) == "PKV_ERR_WORKSPACE"
+    assert pkv.pkv_status_string(99) == "PKV_UNKNOWN_STATUS"
+
+
+def _req(c, s, b):
+    return SimpleNamespace(computed=c, scheduled=s, blocks=list(b))
+
+
+def test_metadata_matches_printed_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "flatten_example.json")))
+    reqs = [_req(r["computed"], r["scheduled"], r["blocks"]) for r in g["schedule"]]
+    m = metadata.build(reqs, g["block_size"])
+    p = g["printed"]
+    assert m["slot_mapping"].tolist() == p["slot_mapping"]
+    assert m["query_start_loc"].tolist() == p["query_start_loc"]
+    assert m["seq_lens"].tolist() == p["seq_lens"]
+    assert m["positions"].tolist() == p["positions"]
+    assert m["query_start_loc"].dtype == np.int32 and m["slot_mapping"].dtype == np.int64
+
+
+def test_metadata_exercise(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "flatten_exercise.json")))
+    r = g["request"]
+    m = metadata.build([_req(r["computed"], r["scheduled"], r["blocks"])], g["block_size"])
+    assert m["slot_mapping"].tolist() == g["expected"]["slot_mapping"]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_metadata_agrees_with_oracle_builder(seed):
+    w = workloads.random_small(seed, num_seqs=9)
+    m = metadata.build(w.requests)
+    o = oracle_flatten.flatten(w.requests)
+    for k in ("slot_mapping", "query_start_loc", "seq_lens", "positions"):
+        assert m[k].tolist() == o[k].tolist(), k
+    ctx = metadata.context_slot_mapping(w.requests)
+    want = np.concatenate([oracle_flatten.context_slots(r) for r in w.requests])
+    assert ctx.tolist() == want.tolist()
+
+
+def test_workspace_bytes(pkv):
+    assert pkv.pkv_workspace_bytes(1, 32, 128, 1) == 0
+    rows = 7 * 3 * 4 * 32
+    want = -(-(rows * 128 * 4) // 256) * 256 + -(-(rows * 4) // 256) * 256
+    assert pkv.pkv_workspace_bytes(3, 32, 128, 7) == want
+
+
+def _attn_call(pkv, **over):
+    L = pkv.lib()
+    args = dict(q=16, k=16, v=16, out=16, lse=0, qsl=16, sl=16, bt=16, mbps=4, num_seqs=2,
+                num_tokens=5, max_q=4, max_s=40, hq=8, hkv=2, d=128, bs=16, scale=0.1, causal=1,
+                splits=1, ws=0, ws_bytes=0, flag=0, num_blocks=10, dtype=1, stream=0)
+    args.update(over)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.pkv_attention_varlen(vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["out"]),
+                                  vp(args["lse"]), vp(args["qsl"]), vp(args["sl"]), vp(args["bt"]),
+                                  args["mbps"], args["num_seqs"], args["num_tokens"], args["max_q"],
+                                  args["max_s"], args["hq"], args["hkv"], args["d"], args["bs"],
+                                  args["scale"], args["causal"], args["splits"], vp(args["ws"]),
+                                  args["ws_bytes"], vp(args["flag"]), args["num_blocks"],
+                                  args["dtype"], vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(hq=6, hkv=4), 1),            # Hq not a multiple of Hkv
+    (dict(d=96), 2),                   # unsupported head_dim
+    (dict(bs=32), 2),                  # unsupported block size
+    (dict(dtype=7), 1),                # unknown dtype
+    (dict(q=0), 1),                    # null q
+    (dict(q=24), 1),                   # misaligned q
+    (dict(splits=65), 1),              # too many splits
+    (dict(splits=4), 3),               # split partials need a workspace
+    (dict(splits=4, ws=4096, ws_bytes=16), 3),
+    (dict(max_q=0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(num_tokens=0), 0),           # empty batch: no-op
+    (dict(num_seqs=0), 0),
+])
+def test_attention_host_validation(pkv, over, code):
+    assert _attn_call(pkv, **over) == code
+
+
+def test_write_host_validation(pkv):
+    L = pkv.lib()
+    vp = ctypes.c_void_p
+    # empty batch is a no-op; bad sizes and null pointers are rejected
+    assert L.pkv_write(None, None, None, 0, None, None, 4, 16, 8, 128, 1, None, None) == 0
+    assert L.pkv_write(vp(16), vp(16), vp(16), 3, vp(16), vp(16), 4, 8, 8, 128, 1, None, None) == 2
+    assert L.pkv_write(None, vp(16), vp(16), 3, vp(16), vp(16), 4, 16, 8, 128, 1, None, None) == 1
+    assert L.pkv_write(vp(16), vp(16), vp(16), -1, vp(16), vp(16), 4, 16, 8, 128, 1, None, None) == 1
+    assert L.pkv_write(vp(18), vp(16), vp(16), 3, vp(16), vp(16), 4, 16, 8, 128, 1, None, None) == 1
+
+
+def test_num_splits_rejects_bad_args(pkv):
+    assert pkv.lib().pkv_num_splits(0, 1, 100, 32, 8, 128, 0) == 0
+    assert pkv.lib().pkv_num_splits(1, 1, 100, 30, 8, 128, 0) == 0
