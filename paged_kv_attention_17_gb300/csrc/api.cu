@@ -16,6 +16,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
                           bool bf16, int head_dim, bool pdl, cudaStream_t stream);
 cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStream_t stream);
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
+int decode_ctas_per_sm(int head_dim);
 bool prefill_supported(int head_dim, bool bf16);
 cudaError_t launch_prefill(const AttnArgs& a, const void* k_cache, const void* v_cache,
                            int head_dim, cudaStream_t stream);
@@ -25,7 +26,6 @@ using namespace pkv;
 
 namespace {
 
-constexpr int kDecodeCtasPerSm = 2;      // resident decode CTAs per SM (shared-memory bound)
 constexpr int kMinBlocksPerSplit = 8;    // 128 keys
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -133,7 +133,6 @@ pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_m
 
 int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_heads,
                    int num_kv_heads, int head_dim, int device) {
-  (void)head_dim;
   if (num_seqs < 1 || max_seq_len < 0 || max_query_len < 0 || num_q_heads < 1 ||
       num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
     return 0;
@@ -143,7 +142,7 @@ int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_h
   const int qd = max_query_len < kDecodeMaxQ ? (max_query_len < 1 ? 1 : max_query_len) : kDecodeMaxQ;
   const int R = decode_rows_per_tile(group, qd, false);
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((group * qd + R - 1) / R);
-  const int64_t capacity = static_cast<int64_t>(sms) * kDecodeCtasPerSm;
+  const int64_t capacity = static_cast<int64_t>(sms) * decode_ctas_per_sm(head_dim);
   if (units >= capacity) return 1;                     // grid already full: no split
   int64_t s = (capacity + units - 1) / units;
   const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kBlock - 1) / kBlock;

@@ -51,21 +51,40 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Packed fp32 pairs (fma.rn.f32x2 / mul.rn.f32x2 on sm_100+): two lanes of
+// fp32 arithmetic per instruction.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ void fma2(f32x2& acc, f32x2 a, f32x2 b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ void mul2(f32x2& acc, f32x2 a) {
+  asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(a));
+}
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pack2(bf16_lo(w), bf16_hi(w)); }
+
 template <typename T, int D>
 struct DecodeCfg {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
-  static constexpr int kChunks = kRowBytes / 16;          // 16-byte chunks per key row
-  static constexpr int kVec = 16 / static_cast<int>(sizeof(T));
-  static constexpr int kTileBlocks = 2;                   // blocks per stage
-  static constexpr int kTileKeys = kTileBlocks * kBlock;  // 32: one key per lane
-  static constexpr int kStageBytes = 2 * kTileKeys * kRowBytes;   // K + V
-  static constexpr int kWarps = 4;                        // consumer warps per CTA
-  static constexpr int kStagesRaw = 131072 / (kWarps * kStageBytes);
+  static constexpr int kHalfChunks = kRowBytes / 32;      // 16-byte chunks per half key row
+  static constexpr int kStageBytes = 2 * kBlock * kRowBytes;   // one block of K and of V
+  static constexpr int kWarps = 4;                        // warps per CTA
+  static constexpr int kStagesRaw = 65536 / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 4 ? 4 : kStagesRaw);
   static constexpr int kStages = kWarps * kStagesPerWarp;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kDPL = D / 32;                     // output columns per lane
-  static_assert((kChunks & (kChunks - 1)) == 0, "chunks per row must be a power of two");
+  static constexpr int kPairs = kDPL / 2;
+  static_assert((kHalfChunks & (kHalfChunks - 1)) == 0, "chunks per half row: power of two");
 };
 
 template <typename T, int D, int R>
@@ -76,7 +95,7 @@ struct DecodeSmem {
   static constexpr int kRingBytes = kStageArea > kMergeBytes ? kStageArea : kMergeBytes;
   static constexpr int kQOff = kRingBytes;
   static constexpr int kPOff = kQOff + R * D * 4;
-  static constexpr int kBarOff = kPOff + C::kWarps * C::kTileKeys * R * 4;
+  static constexpr int kBarOff = kPOff + C::kWarps * kBlock * R * 8;
   static constexpr int kBytes = kBarOff + C::kStages * 8;
   static constexpr int kAlloc = kBytes + 1024;            // slack to align the base to 1 KB
 };
@@ -122,6 +141,30 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// V columns lane*kDPL .. +kDPL-1 of one cached row, as fp32 pairs.
+template <typename T, int D>
+__device__ __forceinline__ void load_v_pairs(const uint8_t* vrow, int lane,
+                                             f32x2 (&v)[DecodeCfg<T, D>::kPairs]) {
+  using C = DecodeCfg<T, D>;
+  if constexpr (sizeof(T) == 4) {
+    if constexpr (C::kPairs == 1) {
+      v[0] = *reinterpret_cast<const f32x2*>(vrow + lane * 8);
+    } else {
+      const ulonglong2 t = *reinterpret_cast<const ulonglong2*>(vrow + lane * 16);
+      v[0] = t.x;
+      v[1] = t.y;
+    }
+  } else {
+    if constexpr (C::kPairs == 1) {
+      v[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(vrow + lane * 4));
+    } else {
+      const uint2 t = *reinterpret_cast<const uint2*>(vrow + lane * 8);
+      v[0] = bf16x2_to_f32x2(t.x);
+      v[1] = bf16x2_to_f32x2(t.y);
+    }
+  }
+}
+
 template <typename T, int D, int R>
 __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -133,7 +176,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* q_s = reinterpret_cast<float*>(smem + Sm::kQOff);
-  float* p_s = reinterpret_cast<float*>(smem + Sm::kPOff);
+  float* p_s = reinterpret_cast<float*>(smem + Sm::kPOff);   // [warp][key][row] (p, p)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -142,8 +185,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   const int z = blockIdx.y;
   const int r = blockIdx.z;
 
-  // ---- request geometry (uniform over the CTA) ----
+  // ---- request geometry (uniform over the CTA); inputs only after the wait ----
   pdl_wait_primary();
+  pdl_launch_dependents();
   const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
   const int n = q1 - q0;
   const int L = __ldg(a.seq_lens + r);
@@ -156,11 +200,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   if (!decode_class && !a.long_rows) return;          // the prefill kernel owns it
   const bool split_mode = decode_class && a.num_splits > 1;
   if (!split_mode && s != 0) return;
-  const int rows_total = a.group * n;
+  const int group = a.group;
+  const int rows_total = group * n;
   const int rho0 = z * R;
   if (rho0 >= rows_total) return;
   const int nrows = min(R, rows_total - rho0);
-  const int i_last = (rho0 + nrows - 1) / a.group;
+  const int i_last = (rho0 + nrows - 1) / group;
   const int kv_len = a.causal ? (L - n + i_last + 1) : L;
   const int nblk = (kv_len + kBlock - 1) / kBlock;
   if (nblk > a.max_blocks_per_seq) {
@@ -177,18 +222,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
     // empty split: partial (o = 0, lse = -inf) so the combine weighs it 0
     for (int rho = warp; rho < nrows; rho += C::kWarps) {
       const int rr = rho0 + rho;
-      const int64_t w = ws_row(a, s, r, rr / a.group, g * a.group + rr % a.group);
+      const int64_t w = ws_row(a, s, r, rr / group, g * group + rr % group);
 #pragma unroll
       for (int e = 0; e < C::kDPL; ++e) a.ws_o[w * D + lane * C::kDPL + e] = 0.f;
       if (lane == 0) a.ws_lse[w] = -INFINITY;
     }
     return;
   }
-  const int ntiles = (b1 - b0 + C::kTileBlocks - 1) / C::kTileBlocks;
-  // this warp's tiles: k = warp + kWarps * j, j < my_tiles
-  const int my_tiles = ntiles > warp ? (ntiles - warp + C::kWarps - 1) / C::kWarps : 0;
+  const int key_end = min(kv_len, b1 * kBlock);       // keys of this split: [b0*16, key_end)
+  const int nt = b1 - b0;                              // one block per stage
+  const int my_tiles = nt > warp ? (nt - warp + C::kWarps - 1) / C::kWarps : 0;
 
-  // ---- barriers first, so the loads can start while q is staged ----
+  // ---- barriers first, so the loads start while q is staged ----
   if (lane == 0) {
     if (warp == 0) {
       tma_prefetch_desc(&kmap);
@@ -201,43 +246,30 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
 
   const uint64_t pol = l2_policy_evict_first();
   const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
-  // Block-table entries of this warp's tiles, 16 tiles (32 blocks) per refill:
-  // lane l holds block b0 + 2 * (warp + kWarps * (base + l / 2)) + l % 2.
+  // Block-table entries of this warp's blocks, 32 per refill: lane l holds the
+  // entry of the warp's tile (base + l), block b0 + warp + kWarps * (base + l).
   int32_t entry = 0;
   int entry_base = -1;
-  auto issue = [&](int j) {           // warp-uniform call
+  auto issue = [&](int j) {            // warp-uniform call
     if (j >= my_tiles) return;
-    if ((j & ~15) != entry_base) {
-      entry_base = j & ~15;
-      const int kk = warp + C::kWarps * (entry_base + (lane >> 1));
-      const int bb = b0 + kk * C::kTileBlocks + (lane & 1);
+    if ((j & ~31) != entry_base) {
+      entry_base = j & ~31;
+      const int bb = b0 + warp + C::kWarps * (entry_base + lane);
       entry = (bb < b1) ? __ldg(table + bb) : 0;
     }
-    const int k = warp + C::kWarps * j;
-    const int first = b0 + k * C::kTileBlocks;
-    const int nb = min(C::kTileBlocks, b1 - first);
-    int ids[C::kTileBlocks];
-#pragma unroll
-    for (int u = 0; u < C::kTileBlocks; ++u)
-      ids[u] = __shfl_sync(0xffffffffu, entry, ((j & 15) * 2 + u) & 31);
+    int id = __shfl_sync(0xffffffffu, entry, j & 31);
     if (lane == 0) {
       const int st = warp * P + (j % P);
       uint8_t* ks = smem + st * C::kStageBytes;
-      uint8_t* vs = ks + C::kTileKeys * C::kRowBytes;
-      fence_proxy_async_smem();       // earlier generic reads of this stage before the refill
-      mbar_arrive_expect_tx(&full[st], nb * 2 * kBlock * C::kRowBytes);
-#pragma unroll
-      for (int u = 0; u < C::kTileBlocks; ++u) {
-        if (u < nb) {
-          int id = ids[u];
-          if (id < 0 || id >= a.num_blocks) {
-            raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
-            id = 0;
-          }
-          tma_load_3d(ks + u * kBlock * C::kRowBytes, &kmap, &full[st], 0, g, id * kBlock, pol);
-          tma_load_3d(vs + u * kBlock * C::kRowBytes, &vmap, &full[st], 0, g, id * kBlock, pol);
-        }
+      uint8_t* vs = ks + kBlock * C::kRowBytes;
+      if (id < 0 || id >= a.num_blocks) {
+        raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
+        id = 0;
       }
+      fence_proxy_async_smem();        // earlier generic reads of this stage before the refill
+      mbar_arrive_expect_tx(&full[st], 2 * kBlock * C::kRowBytes);
+      tma_load_3d(ks, &kmap, &full[st], 0, g, id * kBlock, pol);
+      tma_load_3d(vs, &vmap, &full[st], 0, g, id * kBlock, pol);
     }
     __syncwarp();
   };
@@ -245,33 +277,39 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   for (int j = 0; j < P; ++j) issue(j);
 
   // ---- stage q rows (pre-scaled into the log2 domain) ----
-  for (int e = threadIdx.x; e < R * D; e += blockDim.x) {
+  for (int e = threadIdx.x; e < R * D; e += C::kThreads) {
     const int rho = e / D, d = e % D;
     float v = 0.f;
     if (rho < nrows) {
       const int rr = rho0 + rho;
-      const int64_t t = q0 + rr / a.group;
-      const int h = g * a.group + rr % a.group;
+      const int64_t t = q0 + rr / group;
+      const int h = g * group + rr % group;
       v = load_elem<T>(a.q, (t * a.hq + h) * D + d) * a.scale_log2;
     }
     q_s[q_index<T, D>(rho, d)] = v;
   }
+  // causal limit of each row: keys < lim[rho] are visible
+  int lim[R];
+#pragma unroll
+  for (int rho = 0; rho < R; ++rho)
+    lim[rho] = min(key_end, a.causal ? (L - n + (rho0 + rho) / group + 1) : L);
   __syncthreads();
-  pdl_launch_dependents();
 
-  float m[R], l[R], acc[R][C::kDPL];
+  float m[R], l[R];
+  f32x2 acc[R][C::kPairs];
 #pragma unroll
   for (int rho = 0; rho < R; ++rho) {
     m[rho] = -INFINITY;
     l[rho] = 0.f;
 #pragma unroll
-    for (int e = 0; e < C::kDPL; ++e) acc[rho][e] = 0.f;
+    for (int e = 0; e < C::kPairs; ++e) acc[rho][e] = 0ull;
   }
 
-  const int pos0 = L - n;                             // position of new token 0
+  const int kl = lane & (kBlock - 1);                  // key of this lane within a block
+  const int half = lane >> 4;                          // which half of the key row it dots
   int j = 0;
   for (; j < my_tiles; ++j) {
-    const int k = warp + C::kWarps * j;
+    const int blk = b0 + warp + C::kWarps * j;
     const int st = warp * P + (j % P);
     const bool got = mbar_wait(&full[st], (j / P) & 1);
     if (!__all_sync(0xffffffffu, got)) {
@@ -279,128 +317,99 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
       break;
     }
     const uint8_t* ks = smem + st * C::kStageBytes;
-    const uint8_t* vs = ks + C::kTileKeys * C::kRowBytes;
-    const int key0 = (b0 + k * C::kTileBlocks) * kBlock;
-    const int nvalid = min(C::kTileKeys, kv_len - key0);
+    const uint8_t* vs = ks + kBlock * C::kRowBytes;
+    const int key0 = blk * kBlock;
+    const int nvalid = min(kBlock, key_end - key0);
 
-    // ---- scores: lane owns key key0 + lane ----
-    float sc[R];
+    // ---- scores: lane owns key key0 + kl, half of its row; halves summed by shuffle ----
+    f32x2 sc2[R];
 #pragma unroll
-    for (int rho = 0; rho < R; ++rho) sc[rho] = 0.f;
-    const uint8_t* krow = ks + lane * C::kRowBytes;
+    for (int rho = 0; rho < R; ++rho) sc2[rho] = 0ull;
+    const uint8_t* krow = ks + kl * C::kRowBytes + half * (C::kRowBytes / 2);
 #pragma unroll
-    for (int c = 0; c < C::kChunks; ++c) {
-      const int idx = (c + lane) & (C::kChunks - 1);
+    for (int c = 0; c < C::kHalfChunks; ++c) {
+      const int idx = (c + lane) & (C::kHalfChunks - 1);
+      const int chunk = half * C::kHalfChunks + idx;   // 16-byte chunk of the full row
       const uint4 kc = *reinterpret_cast<const uint4*>(krow + idx * 16);
       if constexpr (sizeof(T) == 4) {
-        const float k0 = __uint_as_float(kc.x), k1 = __uint_as_float(kc.y);
-        const float k2 = __uint_as_float(kc.z), k3 = __uint_as_float(kc.w);
+        const f32x2 k01 = pack2(__uint_as_float(kc.x), __uint_as_float(kc.y));
+        const f32x2 k23 = pack2(__uint_as_float(kc.z), __uint_as_float(kc.w));
 #pragma unroll
         for (int rho = 0; rho < R; ++rho) {
           if (rho < nrows) {
-            const float4 qa = *reinterpret_cast<const float4*>(q_s + rho * D + idx * 4);
-            sc[rho] = fmaf(qa.x, k0, sc[rho]);
-            sc[rho] = fmaf(qa.y, k1, sc[rho]);
-            sc[rho] = fmaf(qa.z, k2, sc[rho]);
-            sc[rho] = fmaf(qa.w, k3, sc[rho]);
+            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
+            fma2(sc2[rho], qa.x, k01);
+            fma2(sc2[rho], qa.y, k23);
           }
         }
       } else {
-        const float k0 = bf16_lo(kc.x), k1 = bf16_hi(kc.x), k2 = bf16_lo(kc.y),
-                    k3 = bf16_hi(kc.y);
-        const float k4 = bf16_lo(kc.z), k5 = bf16_hi(kc.z), k6 = bf16_lo(kc.w),
-                    k7 = bf16_hi(kc.w);
+        const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
+        const f32x2 k45 = bf16x2_to_f32x2(kc.z), k67 = bf16x2_to_f32x2(kc.w);
 #pragma unroll
         for (int rho = 0; rho < R; ++rho) {
           if (rho < nrows) {
-            const float4 qa = *reinterpret_cast<const float4*>(q_s + rho * D + idx * 4);
-            const float4 qb = *reinterpret_cast<const float4*>(q_s + rho * D + D / 2 + idx * 4);
-            float t0 = sc[rho];
-            t0 = fmaf(qa.x, k0, t0);
-            t0 = fmaf(qa.y, k1, t0);
-            t0 = fmaf(qa.z, k2, t0);
-            t0 = fmaf(qa.w, k3, t0);
-            t0 = fmaf(qb.x, k4, t0);
-            t0 = fmaf(qb.y, k5, t0);
-            t0 = fmaf(qb.z, k6, t0);
-            t0 = fmaf(qb.w, k7, t0);
-            sc[rho] = t0;
+            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
+            const ulonglong2 qb =
+                *reinterpret_cast<const ulonglong2*>(q_s + rho * D + D / 2 + chunk * 4);
+            fma2(sc2[rho], qa.x, k01);
+            fma2(sc2[rho], qa.y, k23);
+            fma2(sc2[rho], qb.x, k45);
+            fma2(sc2[rho], qb.y, k67);
           }
         }
       }
     }
 
     // ---- online softmax update (per row; m uniform over the warp) ----
-    const int key = key0 + lane;
-    float* pw = p_s + (warp * C::kTileKeys + lane) * R;
+    const int key = key0 + kl;
+    float* pw = p_s + ((warp * kBlock + kl) * R) * 2;
 #pragma unroll
     for (int rho = 0; rho < R; ++rho) {
       if (rho < nrows) {
-        const int lim = a.causal ? (pos0 + (rho0 + rho) / a.group + 1) : L;
-        const float sv = key < lim ? sc[rho] : -INFINITY;
-        const float mnew = fmaxf(m[rho], warp_max(sv));
+        const float2 t2 = unpack2(sc2[rho]);
+        float sv = t2.x + t2.y;
+        sv += __shfl_xor_sync(0xffffffffu, sv, 16);
+        sv = key < lim[rho] ? sv : -INFINITY;
+        float mx = sv;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float mnew = fmaxf(m[rho], mx);
         const float msafe = mnew == -INFINITY ? 0.f : mnew;
         const float alpha = ex2(m[rho] - msafe);
         const float p = ex2(sv - msafe);
-        l[rho] = l[rho] * alpha + p;
+        l[rho] = l[rho] * alpha + (half == 0 ? p : 0.f);
         m[rho] = mnew;
+        const f32x2 a2 = pack2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < C::kDPL; ++e) acc[rho][e] *= alpha;
-        pw[rho] = p;
+        for (int e = 0; e < C::kPairs; ++e) mul2(acc[rho][e], a2);
+        if (half == 0) *reinterpret_cast<float2*>(pw + rho * 2) = make_float2(p, p);
       }
     }
     __syncwarp();
 
     // ---- P.V: lane owns output columns lane*kDPL .. +kDPL-1 ----
-#pragma unroll 2
+#pragma unroll 4
     for (int jj = 0; jj < nvalid; ++jj) {
-      const float* pr = p_s + (warp * C::kTileKeys + jj) * R;
-      float pv[R];
+      const float* pr = p_s + ((warp * kBlock + jj) * R) * 2;
+      f32x2 pp[R];
 #pragma unroll
-      for (int r4 = 0; r4 < R; r4 += 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(pr + r4);
-        pv[r4] = t4.x;
-        pv[r4 + 1] = t4.y;
-        pv[r4 + 2] = t4.z;
-        pv[r4 + 3] = t4.w;
+      for (int r2 = 0; r2 < R; r2 += 2) {
+        const ulonglong2 t = *reinterpret_cast<const ulonglong2*>(pr + r2 * 2);
+        pp[r2] = t.x;
+        pp[r2 + 1] = t.y;
       }
-      float vf[C::kDPL];
-      const uint8_t* vrow = vs + jj * C::kRowBytes;
-      if constexpr (sizeof(T) == 4) {
-        if constexpr (C::kDPL == 2) {
-          const float2 v2 = *reinterpret_cast<const float2*>(vrow + lane * 8);
-          vf[0] = v2.x;
-          vf[1] = v2.y;
-        } else {
-          const float4 v4 = *reinterpret_cast<const float4*>(vrow + lane * 16);
-          vf[0] = v4.x;
-          vf[1] = v4.y;
-          vf[2] = v4.z;
-          vf[3] = v4.w;
-        }
-      } else {
-        if constexpr (C::kDPL == 2) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow + lane * 4);
-          vf[0] = bf16_lo(w);
-          vf[1] = bf16_hi(w);
-        } else {
-          const uint2 w = *reinterpret_cast<const uint2*>(vrow + lane * 8);
-          vf[0] = bf16_lo(w.x);
-          vf[1] = bf16_hi(w.x);
-          vf[2] = bf16_lo(w.y);
-          vf[3] = bf16_hi(w.y);
-        }
-      }
+      f32x2 v[C::kPairs];
+      load_v_pairs<T, D>(vs + jj * C::kRowBytes, lane, v);
 #pragma unroll
       for (int rho = 0; rho < R; ++rho) {
         if (rho < nrows) {
 #pragma unroll
-          for (int e = 0; e < C::kDPL; ++e) acc[rho][e] = fmaf(pv[rho], vf[e], acc[rho][e]);
+          for (int e = 0; e < C::kPairs; ++e) fma2(acc[rho][e], pp[rho], v[e]);
         }
       }
     }
     __syncwarp();
-    issue(j + P);                     // refill the stage just consumed
+    issue(j + P);                      // refill the stage just consumed
   }
   if (j < my_tiles && lane == 0) {
     // gave up early: let this warp's loads still in flight land before the
@@ -423,8 +432,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
         lw[warp * R + rho] = lt;
       }
 #pragma unroll
-      for (int e = 0; e < C::kDPL; ++e)
-        aw[(warp * R + rho) * D + lane * C::kDPL + e] = acc[rho][e];
+      for (int e = 0; e < C::kPairs; ++e)
+        *reinterpret_cast<float2*>(aw + (warp * R + rho) * D + lane * C::kDPL + 2 * e) =
+            unpack2(acc[rho][e]);
     }
   }
   __syncthreads();
@@ -449,8 +459,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     const float lse2 = lsum > 0.f ? M + lg2(lsum) : -INFINITY;
     const int rr = rho0 + rho;
-    const int i = rr / a.group;
-    const int h = g * a.group + rr % a.group;
+    const int i = rr / group;
+    const int h = g * group + rr % group;
     if (split_mode) {
       const int64_t w = ws_row(a, s, r, i, h);
 #pragma unroll
@@ -466,15 +476,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   }
 }
 
-// One warp per (request, decode row, q head): merge the split partials by
-// their log-sum-exp weights, M = max_s lse_s, w_s = 2^(lse_s - M),
-// o = sum_s w_s o_s / sum_s w_s.
+// Log-sum-exp merge of the split partials: for each (request, decode row,
+// q head), M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s.
+// One CTA of 4 warps per row: warp w takes splits s = w, w + 4, ...; all of a
+// warp's partial loads are issued before any is used.
 template <typename T, int D>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   constexpr int kDPL = D / 32;
+  __shared__ float red[4][D + 1];
   pdl_wait_primary();
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  const int64_t item = blockIdx.x;
   const int h = static_cast<int>(item % a.hq);
   const int64_t ri = item / a.hq;
   const int i = static_cast<int>(ri % kDecodeMaxQ);
@@ -484,35 +497,49 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   const int n = q1 - q0;
   if (n <= 0 || n > kDecodeMaxQ || i >= n || q0 < 0 || q1 > a.num_tokens) return;
   if (n > __ldg(a.seq_lens + r)) return;
-  const int S = a.num_splits;
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, a.ws_lse[ws_row(a, s, r, i, h)]);
-  M = warp_max(M);
+  const int S = a.num_splits;                          // <= kMaxSplits = 64
+  // every lane reads up to two lse values; the max and weights are warp-wide
+  const float l0 = lane < S ? a.ws_lse[ws_row(a, lane, r, i, h)] : -INFINITY;
+  const float l1 = lane + 32 < S ? a.ws_lse[ws_row(a, lane + 32, r, i, h)] : -INFINITY;
+  float M = warp_max(fmaxf(l0, l1));
+  const float w0 = M == -INFINITY ? 0.f : ex2(l0 - M);
+  const float w1 = M == -INFINITY ? 0.f : ex2(l1 - M);
+  const float wsum = warp_sum(w0 + w1);
   float o[kDPL];
 #pragma unroll
   for (int e = 0; e < kDPL; ++e) o[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const int64_t w = ws_row(a, s, r, i, h);
-      const float f = ex2(a.ws_lse[w] - M);
-      wsum += f;
-      if (kDPL == 4) {
-        const float4 p = *reinterpret_cast<const float4*>(a.ws_o + w * D + lane * 4);
-        o[0] = fmaf(f, p.x, o[0]);
-        o[1] = fmaf(f, p.y, o[1]);
-        o[2 % kDPL] = fmaf(f, p.z, o[2 % kDPL]);
-        o[3 % kDPL] = fmaf(f, p.w, o[3 % kDPL]);
-      } else {
+  constexpr int kMaxPer = kMaxSplits / 4;
+  float part[kMaxPer][kDPL];
 #pragma unroll
-        for (int e = 0; e < kDPL; ++e) o[e] = fmaf(f, a.ws_o[w * D + lane * kDPL + e], o[e]);
-      }
+  for (int u = 0; u < kMaxPer; ++u) {
+    const int sp = warp + 4 * u;
+    if (sp < S) {
+      const float* src = a.ws_o + ws_row(a, sp, r, i, h) * D + lane * kDPL;
+#pragma unroll
+      for (int e = 0; e < kDPL; ++e) part[u][e] = src[e];
     }
   }
+#pragma unroll
+  for (int u = 0; u < kMaxPer; ++u) {
+    const int sp = warp + 4 * u;
+    if (sp < S) {
+      const float f = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+#pragma unroll
+      for (int e = 0; e < kDPL; ++e) o[e] = fmaf(f, part[u][e], o[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) red[warp][lane * kDPL + e] = o[e];
+  __syncthreads();
+  if (warp != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const int64_t t = q0 + i;
 #pragma unroll
-  for (int e = 0; e < kDPL; ++e) store_elem<T>(a.out, (t * a.hq + h) * D + lane * kDPL + e, o[e] * inv);
+  for (int e = 0; e < kDPL; ++e) {
+    const int col = lane * kDPL + e;
+    const float v = red[0][col] + red[1][col] + red[2][col] + red[3][col];
+    store_elem<T>(a.out, (t * a.hq + h) * D + col, v * inv);
+  }
   if (a.lse_out != nullptr && lane == 0)
     a.lse_out[t * a.hq + h] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
 }
@@ -521,18 +548,27 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
 // Host launchers
 // ---------------------------------------------------------------------------
 template <typename T, int D, int R>
+static cudaError_t ensure_smem_attr() {
+  using Sm = DecodeSmem<T, D, R>;
+  static unsigned done = 0;                 // one bit per device already configured
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 32 && ((done >> dev) & 1u)) return cudaSuccess;
+  e = cudaFuncSetAttribute(decode_kernel<T, D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Sm::kAlloc);
+  if (e == cudaSuccess && dev < 32) done |= 1u << dev;
+  return e;
+}
+
+template <typename T, int D, int R>
 static cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int row_tiles, bool pdl,
                                    cudaStream_t stream) {
   using C = DecodeCfg<T, D>;
   using Sm = DecodeSmem<T, D, R>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, R>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_attr<T, D, R>();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.hkv * a.num_splits), static_cast<unsigned>(row_tiles),
                      static_cast<unsigned>(a.num_seqs));
@@ -560,6 +596,36 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
 
 // Rows per CTA tile for a launch: the smallest of 4/8/16 holding one request's
 // decode rows (group x q_len), 16 when longer requests also run here.
+// Resident decode CTAs per SM for the bf16 single-token configuration (the
+// one the split heuristic sizes), from the occupancy calculator.
+int decode_ctas_per_sm(int head_dim) {
+  static int cache[2] = {0, 0};
+  const int k = head_dim == 128 ? 1 : 0;
+  if (cache[k] == 0) {
+    int n = 0;
+    cudaError_t e;
+    if (k) {
+      e = ensure_smem_attr<__nv_bfloat16, 128, 4>();
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, decode_kernel<__nv_bfloat16, 128, 4>, DecodeCfg<__nv_bfloat16, 128>::kThreads,
+            DecodeSmem<__nv_bfloat16, 128, 4>::kAlloc);
+    } else {
+      e = ensure_smem_attr<__nv_bfloat16, 64, 4>();
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, decode_kernel<__nv_bfloat16, 64, 4>, DecodeCfg<__nv_bfloat16, 64>::kThreads,
+            DecodeSmem<__nv_bfloat16, 64, 4>::kAlloc);
+    }
+    if (e != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      return 1;
+    }
+    cache[k] = n;
+  }
+  return cache[k];
+}
+
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows) {
   const int q = long_rows ? max_query_len : (max_query_len < kDecodeMaxQ ? max_query_len : kDecodeMaxQ);
   const int need = group * (q < 1 ? 1 : q);
@@ -583,7 +649,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(a.num_seqs) * kDecodeMaxQ * a.hq;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((items + 3) / 4));
+  cfg.gridDim = dim3(static_cast<unsigned>(items));
   cfg.blockDim = dim3(128);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(
     const int64_t* __restrict__ slots, int64_t num_tokens, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, int64_t num_slots, uint32_t chunks_per_row,
     int32_t* flag) {
+  pdl_wait_primary();        // inputs and cache are safe to touch only after the predecessor
+  pdl_launch_dependents();   // let the attention kernel launch and set up meanwhile
   const int64_t total = num_tokens * chunks_per_row;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -49,10 +51,19 @@ cudaError_t launch_kv_write(const void* k_new, const void* v_new, const int64_t*
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  kv_write_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, num_tokens,
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_slots, chunks, flag);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_write_kernel, static_cast<const uint4*>(k_new),
+                            static_cast<const uint4*>(v_new), slots, num_tokens,
+                            static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_slots,
+                            chunks, flag);
 }
 
 }  // namespace pkv
