@@ -160,6 +160,34 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
                                 void* workspace, size_t workspace_bytes, int32_t* error_flag,
                                 int64_t num_blocks, pkv_dtype dtype, void* stream);
 
+/*
+ * pkv_attention_varlen_noalloc - pkv_attention_varlen without a caller
+ * workspace.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory (for example a plain C host program
+ * whose device memory is owned by another runtime's caching allocator, or a
+ * path that must never block in cudaMalloc/cudaFree).  The split-KV partials
+ * live in a fixed 8 MiB array compiled into the library (held on every GPU
+ * that loads it until the process exits); the call allocates nothing.
+ *   Arguments are those of pkv_attention_varlen minus the workspace.
+ *   Returns PKV_ERR_WORKSPACE when the partials of the chosen split count
+ *   (pkv_workspace_bytes) exceed 8 MiB; nothing is enqueued then.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current): make it before any
+ *   stream capture.  All calls on a device share the array, so calls whose
+ *   kernels overlap on the GPU race; serialise them.
+ */
+pkv_status pkv_attention_varlen_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        void* out, float* lse_out,
+                                        const int32_t* query_start_loc, const int32_t* seq_lens,
+                                        const int32_t* block_table, int max_blocks_per_seq,
+                                        int num_seqs, int64_t num_tokens, int max_query_len,
+                                        int max_seq_len, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, float softmax_scale,
+                                        int causal, int num_splits, int32_t* error_flag,
+                                        int64_t num_blocks, pkv_dtype dtype, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* pkv_status_string(pkv_status status);
 

@@ -12,4 +12,5 @@ builder (``metadata.build``).  PyTorch supplies device memory and streams.
 from . import metadata  # noqa: F401
 from ._binding import (EXPORTS, FLAG_BAD_BLOCK, FLAG_BAD_LENGTHS, FLAG_BAD_SLOT,  # noqa: F401
                        FLAG_TIMEOUT, PKV_DECODE_MAX_QLEN, PkvError, lib, pkv_attention_varlen,
+                       pkv_attention_varlen_noalloc,
                        pkv_num_splits, pkv_status_string, pkv_workspace_bytes, pkv_write)

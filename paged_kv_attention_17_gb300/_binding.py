@@ -23,7 +23,7 @@ FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_write", "pkv_num_splits", "pkv_workspace_bytes", "pkv_attention_varlen",
-           "pkv_status_string")
+           "pkv_attention_varlen_noalloc", "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -51,6 +51,10 @@ def lib() -> ctypes.CDLL:
                                            i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, sz,
                                            vp, i64, i32, vp]
         L.pkv_attention_varlen.restype = i32
+        L.pkv_attention_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
+                                                   i32, i32, i32, i32, i32, i32, ctypes.c_float,
+                                                   i32, i32, vp, i64, i32, vp]
+        L.pkv_attention_varlen_noalloc.restype = i32
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -135,4 +139,23 @@ def pkv_attention_varlen(q, k_cache, v_cache, out, query_start_loc, seq_lens, bl
         float(softmax_scale), 1 if causal else 0, splits, _ptr(workspace), int(ws_bytes),
         _ptr(error_flag), int(nb), _dtype_code(q.dtype), _stream(stream))
     _check("pkv_attention_varlen", code)
+    return out
+
+
+def pkv_attention_varlen_noalloc(q, k_cache, v_cache, out, query_start_loc, seq_lens, block_table,
+                                 max_query_len, max_seq_len, softmax_scale, causal=True,
+                                 num_splits=0, lse_out=None, error_flag=None, stream=None):
+    """pkv_attention_varlen for callers that cannot allocate: the split-KV
+    partials use the library's fixed 8 MiB device array instead of a
+    workspace.  Calls whose kernels overlap on the GPU share that array and
+    race; the first call on a device should come before any stream capture."""
+    n_tok, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    code = lib().pkv_attention_varlen_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
+        _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]), int(seq_lens.numel()),
+        int(n_tok), int(max_query_len), int(max_seq_len), int(hq), int(hkv), int(d), int(bs),
+        float(softmax_scale), 1 if causal else 0, int(num_splits), _ptr(error_flag), int(nb),
+        _dtype_code(q.dtype), _stream(stream))
+    _check("pkv_attention_varlen_noalloc", code)
     return out
