@@ -99,10 +99,11 @@ pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_m
  * "Inside the engine ...", section "Prefill has a full grid; decode at batch 1
  * has almost none": split the KV axis when there are too few query rows to
  * fill the GPU; at high batch the grid is already full and the split is
- * turned off.  Returns 1 once the decode grid (num_seqs x num_kv_heads work
- * units) fills the device `device` (SM count from its properties), otherwise
- * enough splits to fill it, with at least 8 blocks (128 keys) per split and at
- * most 64 splits.  Returns 0 for invalid arguments or device.
+ * turned off.  With U = num_seqs x num_kv_heads decode work units and C the
+ * decode CTAs device `device` holds at once (SM count x resident CTAs per SM):
+ * 1 when U >= C (the grid is already full), else ceil(C / U) to fill the
+ * device once; never fewer than 8 blocks (128 keys) per split nor more than
+ * 64 splits.  Returns 0 for invalid arguments or device.
  */
 int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_heads,
                    int num_kv_heads, int head_dim, int device);
@@ -170,9 +171,10 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
  * path that must never block in cudaMalloc/cudaFree).  The split-KV partials
  * live in a fixed 8 MiB array compiled into the library (held on every GPU
  * that loads it until the process exits); the call allocates nothing.
- *   Arguments are those of pkv_attention_varlen minus the workspace.
- *   Returns PKV_ERR_WORKSPACE when the partials of the chosen split count
- *   (pkv_workspace_bytes) exceed 8 MiB; nothing is enqueued then.
+ *   Arguments are those of pkv_attention_varlen minus the workspace.  With
+ *   num_splits == 0 the automatic split count is lowered until its partials
+ *   (pkv_workspace_bytes) fit in 8 MiB; an explicit num_splits whose partials
+ *   exceed 8 MiB returns PKV_ERR_WORKSPACE and enqueues nothing.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current): make it before any
  *   stream capture.  All calls on a device share the array, so calls whose

@@ -147,8 +147,10 @@ def pkv_attention_varlen_noalloc(q, k_cache, v_cache, out, query_start_loc, seq_
                                  num_splits=0, lse_out=None, error_flag=None, stream=None):
     """pkv_attention_varlen for callers that cannot allocate: the split-KV
     partials use the library's fixed 8 MiB device array instead of a
-    workspace.  Calls whose kernels overlap on the GPU share that array and
-    race; the first call on a device should come before any stream capture."""
+    workspace (automatic split counts are lowered to fit it; an explicit one
+    that does not fit raises PkvError with PKV_ERR_WORKSPACE).  Calls whose
+    kernels overlap on the GPU share that array and race; the first call on a
+    device should come before any stream capture."""
     n_tok, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     code = lib().pkv_attention_varlen_noalloc(

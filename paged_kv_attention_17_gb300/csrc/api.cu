@@ -143,7 +143,9 @@ int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_h
   const int R = decode_rows_per_tile(group, qd, false);
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((group * qd + R - 1) / R);
   const int64_t capacity = static_cast<int64_t>(sms) * decode_ctas_per_sm(head_dim);
-  if (units >= capacity) return 1;                     // grid already full: no split
+  // Grid already full: no split.  Otherwise enough splits to fill the
+  // device once (one wave: every CTA's blocks in flight together).
+  if (units >= capacity) return 1;
   int64_t s = (capacity + units - 1) / units;
   const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kBlock - 1) / kBlock;
   int64_t by_len = nblk / kMinBlocksPerSplit;

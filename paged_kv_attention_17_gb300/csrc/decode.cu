@@ -77,9 +77,12 @@ struct DecodeCfg {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
   static constexpr int kHalfChunks = kRowBytes / 32;      // 16-byte chunks per half key row
   static constexpr int kStageBytes = 2 * kBlock * kRowBytes;   // one block of K and of V
-  static constexpr int kWarps = 4;                        // warps per CTA
-  static constexpr int kStagesRaw = 65536 / (kWarps * kStageBytes);
-  static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 4 ? 4 : kStagesRaw);
+  static constexpr int kWarps = 8;                        // warps per CTA
+  // A 192 KB ring per CTA (one CTA per SM): 3 blocks in flight per warp for
+  // 256-byte rows, so a 19-way split of an 8K context has every block in
+  // flight at once and longer contexts keep two prefetched per warp.
+  static constexpr int kStagesRaw = 196608 / (kWarps * kStageBytes);
+  static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 6 ? 6 : kStagesRaw);
   static constexpr int kStages = kWarps * kStagesPerWarp;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kDPL = D / 32;                     // output columns per lane
@@ -233,6 +236,22 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   const int nt = b1 - b0;                              // one block per stage
   const int my_tiles = nt > warp ? (nt - warp + C::kWarps - 1) / C::kWarps : 0;
 
+  // q elements this thread stages: loads issued now, before the table lookup
+  constexpr int kQPer = (R * D + C::kThreads - 1) / C::kThreads;
+  float qv[kQPer];
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int e = threadIdx.x + u * C::kThreads;
+    const int rho = e / D, d = e % D;
+    qv[u] = 0.f;
+    if (e < R * D && rho < nrows) {
+      const int rr = rho0 + rho;
+      const int64_t t = q0 + rr / group;
+      const int h = g * group + rr % group;
+      qv[u] = load_elem<T>(a.q, (t * a.hq + h) * D + d) * a.scale_log2;
+    }
+  }
+
   // ---- barriers first, so the loads start while q is staged ----
   if (lane == 0) {
     if (warp == 0) {
@@ -276,17 +295,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
 #pragma unroll
   for (int j = 0; j < P; ++j) issue(j);
 
-  // ---- stage q rows (pre-scaled into the log2 domain) ----
-  for (int e = threadIdx.x; e < R * D; e += C::kThreads) {
-    const int rho = e / D, d = e % D;
-    float v = 0.f;
-    if (rho < nrows) {
-      const int rr = rho0 + rho;
-      const int64_t t = q0 + rr / group;
-      const int h = g * group + rr % group;
-      v = load_elem<T>(a.q, (t * a.hq + h) * D + d) * a.scale_log2;
-    }
-    q_s[q_index<T, D>(rho, d)] = v;
+  // ---- stage q rows (pre-scaled into the log2 domain); loaded before the
+  //      table round trip above, stored now ----
+#pragma unroll
+  for (int u = 0; u < kQPer; ++u) {
+    const int e = threadIdx.x + u * C::kThreads;
+    if (e < R * D) q_s[q_index<T, D>(e / D, e % D)] = qv[u];
   }
   // causal limit of each row: keys < lim[rho] are visible
   int lim[R];
@@ -336,54 +350,62 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
         const f32x2 k23 = pack2(__uint_as_float(kc.z), __uint_as_float(kc.w));
 #pragma unroll
         for (int rho = 0; rho < R; ++rho) {
-          if (rho < nrows) {
-            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
-            fma2(sc2[rho], qa.x, k01);
-            fma2(sc2[rho], qa.y, k23);
-          }
+          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
+          fma2(sc2[rho], qa.x, k01);
+          fma2(sc2[rho], qa.y, k23);
         }
       } else {
         const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
         const f32x2 k45 = bf16x2_to_f32x2(kc.z), k67 = bf16x2_to_f32x2(kc.w);
 #pragma unroll
         for (int rho = 0; rho < R; ++rho) {
-          if (rho < nrows) {
-            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
-            const ulonglong2 qb =
-                *reinterpret_cast<const ulonglong2*>(q_s + rho * D + D / 2 + chunk * 4);
-            fma2(sc2[rho], qa.x, k01);
-            fma2(sc2[rho], qa.y, k23);
-            fma2(sc2[rho], qb.x, k45);
-            fma2(sc2[rho], qb.y, k67);
-          }
+          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
+          const ulonglong2 qb =
+              *reinterpret_cast<const ulonglong2*>(q_s + rho * D + D / 2 + chunk * 4);
+          fma2(sc2[rho], qa.x, k01);
+          fma2(sc2[rho], qa.y, k23);
+          fma2(sc2[rho], qb.x, k45);
+          fma2(sc2[rho], qb.y, k67);
         }
       }
     }
 
-    // ---- online softmax update (per row; m uniform over the warp) ----
+    // ---- online softmax update (per row; m uniform over the warp).  Every
+    //      row of the tile is computed (rows past nrows have q = 0 and are
+    //      never stored), so the rows' shuffle and exp chains interleave ----
     const int key = key0 + kl;
     float* pw = p_s + ((warp * kBlock + kl) * R) * 2;
+    float sv[R], mx[R];
 #pragma unroll
     for (int rho = 0; rho < R; ++rho) {
-      if (rho < nrows) {
-        const float2 t2 = unpack2(sc2[rho]);
-        float sv = t2.x + t2.y;
-        sv += __shfl_xor_sync(0xffffffffu, sv, 16);
-        sv = key < lim[rho] ? sv : -INFINITY;
-        float mx = sv;
+      const float2 t2 = unpack2(sc2[rho]);
+      sv[rho] = t2.x + t2.y;
+    }
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float mnew = fmaxf(m[rho], mx);
-        const float msafe = mnew == -INFINITY ? 0.f : mnew;
-        const float alpha = ex2(m[rho] - msafe);
-        const float p = ex2(sv - msafe);
-        l[rho] = l[rho] * alpha + (half == 0 ? p : 0.f);
-        m[rho] = mnew;
-        const f32x2 a2 = pack2(alpha, alpha);
+    for (int rho = 0; rho < R; ++rho) sv[rho] += __shfl_xor_sync(0xffffffffu, sv[rho], 16);
 #pragma unroll
-        for (int e = 0; e < C::kPairs; ++e) mul2(acc[rho][e], a2);
-        if (half == 0) *reinterpret_cast<float2*>(pw + rho * 2) = make_float2(p, p);
-      }
+    for (int rho = 0; rho < R; ++rho) {
+      sv[rho] = key < lim[rho] ? sv[rho] : -INFINITY;
+      mx[rho] = sv[rho];
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+      for (int rho = 0; rho < R; ++rho)
+        mx[rho] = fmaxf(mx[rho], __shfl_xor_sync(0xffffffffu, mx[rho], o));
+    }
+#pragma unroll
+    for (int rho = 0; rho < R; ++rho) {
+      const float mnew = fmaxf(m[rho], mx[rho]);
+      const float msafe = mnew == -INFINITY ? 0.f : mnew;
+      const float alpha = ex2(m[rho] - msafe);
+      const float p = ex2(sv[rho] - msafe);
+      l[rho] = l[rho] * alpha + (half == 0 ? p : 0.f);
+      m[rho] = mnew;
+      const f32x2 a2 = pack2(alpha, alpha);
+#pragma unroll
+      for (int e = 0; e < C::kPairs; ++e) mul2(acc[rho][e], a2);
+      if (half == 0) *reinterpret_cast<float2*>(pw + rho * 2) = make_float2(p, p);
     }
     __syncwarp();
 
@@ -402,10 +424,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
       load_v_pairs<T, D>(vs + jj * C::kRowBytes, lane, v);
 #pragma unroll
       for (int rho = 0; rho < R; ++rho) {
-        if (rho < nrows) {
 #pragma unroll
-          for (int e = 0; e < C::kPairs; ++e) fma2(acc[rho][e], pp[rho], v[e]);
-        }
+        for (int e = 0; e < C::kPairs; ++e) fma2(acc[rho][e], pp[rho], v[e]);
       }
     }
     __syncwarp();
@@ -493,21 +513,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   const int i = static_cast<int>(ri % kDecodeMaxQ);
   const int r = static_cast<int>(ri / kDecodeMaxQ);
   if (r >= a.num_seqs) return;
-  const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
-  const int n = q1 - q0;
-  if (n <= 0 || n > kDecodeMaxQ || i >= n || q0 < 0 || q1 > a.num_tokens) return;
-  if (n > __ldg(a.seq_lens + r)) return;
   const int S = a.num_splits;                          // <= kMaxSplits = 64
-  // every lane reads up to two lse values; the max and weights are warp-wide
+  // Partials are loaded before the row is known to exist (rows of requests
+  // that are not decode-class hold stale data and are simply not stored), so
+  // the metadata and workspace loads are in flight together.
+  const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
+  const int L = __ldg(a.seq_lens + r);
   const float l0 = lane < S ? a.ws_lse[ws_row(a, lane, r, i, h)] : -INFINITY;
   const float l1 = lane + 32 < S ? a.ws_lse[ws_row(a, lane + 32, r, i, h)] : -INFINITY;
-  float M = warp_max(fmaxf(l0, l1));
-  const float w0 = M == -INFINITY ? 0.f : ex2(l0 - M);
-  const float w1 = M == -INFINITY ? 0.f : ex2(l1 - M);
-  const float wsum = warp_sum(w0 + w1);
-  float o[kDPL];
-#pragma unroll
-  for (int e = 0; e < kDPL; ++e) o[e] = 0.f;
   constexpr int kMaxPer = kMaxSplits / 4;
   float part[kMaxPer][kDPL];
 #pragma unroll
@@ -519,6 +532,15 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
       for (int e = 0; e < kDPL; ++e) part[u][e] = src[e];
     }
   }
+  const int n = q1 - q0;
+  if (n <= 0 || n > kDecodeMaxQ || i >= n || q0 < 0 || q1 > a.num_tokens || n > L) return;
+  float M = warp_max(fmaxf(l0, l1));
+  const float w0 = M == -INFINITY ? 0.f : ex2(l0 - M);
+  const float w1 = M == -INFINITY ? 0.f : ex2(l1 - M);
+  const float wsum = warp_sum(w0 + w1);
+  float o[kDPL];
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) o[e] = 0.f;
 #pragma unroll
   for (int u = 0; u < kMaxPer; ++u) {
     const int sp = warp + 4 * u;

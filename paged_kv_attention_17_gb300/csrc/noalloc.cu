@@ -51,11 +51,16 @@ extern "C" pkv_status pkv_attention_varlen_noalloc(
   }
   int splits = num_splits;
   if (splits == 0) {
+    // automatic: the heuristic's count, lowered until the partials fit the
+    // array (the split count never changes the result; one split needs none)
     splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
                             head_dim, dev);
     if (splits < 1) return PKV_ERR_INVALID_ARG;
+    while (splits > 1 &&
+           pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits) > kStaticWorkspaceBytes)
+      --splits;
   }
-  // the fixed array bounds the split partials this entry point can hold
+  // an explicit split count whose partials do not fit is rejected
   if (pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits) > kStaticWorkspaceBytes)
     return PKV_ERR_WORKSPACE;
   if (g_workspace_ptr[dev] == nullptr) {
