@@ -71,22 +71,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over one cache tensor viewed as [num_slots, num_kv_heads, head_dim]
-// (innermost first for TMA): a box is 16 slots x 1 head x head_dim, i.e. one
-// block of one kv head.
+// (innermost first for TMA); a box covers 16 slots (one block) of one kv
+// head: the whole row unswizzled (V), or a 128-byte slice of it with the 128B
+// swizzle (K).
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_slots, int hkv, int d,
-                      bool bf16) {
+                      bool bf16, bool swizzle128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t es = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
                         static_cast<cuuint64_t>(num_slots)};
   cuuint64_t strides[2] = {d * es, static_cast<cuuint64_t>(hkv) * d * es};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1, static_cast<cuuint32_t>(kBlock)};
+  const cuuint32_t inner = swizzle128 ? static_cast<cuuint32_t>(128 / es) : static_cast<cuuint32_t>(d);
+  cuuint32_t box[3] = {inner, 1, static_cast<cuuint32_t>(kBlock)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -235,8 +237,8 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
   a.num_blocks = num_blocks;
 
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, bf16) ||
-      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, bf16))
+  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, bf16, true) ||
+      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, bf16, false))
     return PKV_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -76,6 +76,13 @@ template <typename T, int D>
 struct DecodeCfg {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
   static constexpr int kHalfChunks = kRowBytes / 32;      // 16-byte chunks per half key row
+  // K arrives as 128-byte-wide TMA boxes with the 128B swizzle (16-byte chunk
+  // c of row j stored at chunk c ^ (j % 8) of its 128-byte line), so lanes on
+  // 16 different keys can all read one logical chunk without bank conflicts
+  // while every lane of a half-warp reads the same q chunk (a broadcast).
+  static constexpr int kKBoxElems = 128 / static_cast<int>(sizeof(T));
+  static constexpr int kKBoxes = kRowBytes / 128;
+  static constexpr int kKBoxBytes = kBlock * 128;
   static constexpr int kStageBytes = 2 * kBlock * kRowBytes;   // one block of K and of V
   static constexpr int kWarps = 8;                        // warps per CTA
   // A 192 KB ring per CTA (one CTA per SM): 3 blocks in flight per warp for
@@ -169,12 +176,17 @@ __device__ __forceinline__ void load_v_pairs(const uint8_t* vrow, int lane,
 }
 
 template <typename T, int D, int R>
-__global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
+__global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   using C = DecodeCfg<T, D>;
   using Sm = DecodeSmem<T, D, R>;
   constexpr int P = C::kStagesPerWarp;
+  // Register-q path for one token of a 4-query-head GQA group in bf16 (the
+  // decode hot case); every other shape takes the generic path below.
+  constexpr bool kFast = sizeof(T) == 2 && R == 4;
+  constexpr int kFastChunks = D / 64;                 // 16-byte chunks of q/K per lane
+  constexpr int kPWarpFloats = kBlock * R * 2;        // p_s floats per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -236,19 +248,22 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   const int nt = b1 - b0;                              // one block per stage
   const int my_tiles = nt > warp ? (nt - warp + C::kWarps - 1) / C::kWarps : 0;
 
-  // q elements this thread stages: loads issued now, before the table lookup
+  // q elements this thread stages: raw loads issued before the table lookup
+  // and the K/V loads (so they do not queue behind them); first used, and
+  // converted, only after the first K/V loads are in flight
   constexpr int kQPer = (R * D + C::kThreads - 1) / C::kThreads;
-  float qv[kQPer];
+  T qraw[kQPer];
 #pragma unroll
   for (int u = 0; u < kQPer; ++u) {
     const int e = threadIdx.x + u * C::kThreads;
     const int rho = e / D, d = e % D;
-    qv[u] = 0.f;
     if (e < R * D && rho < nrows) {
       const int rr = rho0 + rho;
       const int64_t t = q0 + rr / group;
       const int h = g * group + rr % group;
-      qv[u] = load_elem<T>(a.q, (t * a.hq + h) * D + d) * a.scale_log2;
+      qraw[u] = static_cast<const T*>(a.q)[(t * a.hq + h) * D + d];
+    } else {
+      qraw[u] = T(0.f);
     }
   }
 
@@ -287,7 +302,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
       }
       fence_proxy_async_smem();        // earlier generic reads of this stage before the refill
       mbar_arrive_expect_tx(&full[st], 2 * kBlock * C::kRowBytes);
-      tma_load_3d(ks, &kmap, &full[st], 0, g, id * kBlock, pol);
+#pragma unroll
+      for (int b = 0; b < C::kKBoxes; ++b)
+        tma_load_3d(ks + b * C::kKBoxBytes, &kmap, &full[st], b * C::kKBoxElems, g, id * kBlock,
+                    pol);
       tma_load_3d(vs, &vmap, &full[st], 0, g, id * kBlock, pol);
     }
     __syncwarp();
@@ -295,12 +313,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
 #pragma unroll
   for (int j = 0; j < P; ++j) issue(j);
 
-  // ---- stage q rows (pre-scaled into the log2 domain); loaded before the
-  //      table round trip above, stored now ----
+  // ---- stage q rows (pre-scaled into the log2 domain) ----
 #pragma unroll
   for (int u = 0; u < kQPer; ++u) {
     const int e = threadIdx.x + u * C::kThreads;
-    if (e < R * D) q_s[q_index<T, D>(e / D, e % D)] = qv[u];
+    if (e < R * D) q_s[q_index<T, D>(e / D, e % D)] = static_cast<float>(qraw[u]) * a.scale_log2;
   }
   // causal limit of each row: keys < lim[rho] are visible
   int lim[R];
@@ -321,6 +338,32 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
 
   const int kl = lane & (kBlock - 1);                  // key of this lane within a block
   const int half = lane >> 4;                          // which half of the key row it dots
+
+  // ---- register-q path state: lane = (key group kg of 4 keys, D slice dc).
+  //      The slice is chunks dc and dc + 8 of each row (16 dims for D = 128),
+  //      so the 8 lanes of a group read 8 distinct bank groups of one row. ----
+  const int kg = lane >> 3, dc = lane & 7;
+  const int fb2 = (dc >> 2) & 1, fb1 = (dc >> 1) & 1, fb0 = dc & 1;
+  const int my_r = 2 * fb2 + fb1;                      // row this lane owns after reduction
+  const int kk0 = kg * 4 + 2 * fb0;                    // first of its two keys in a block
+  f32x2 qr[kFast ? 4 : 1][kFast ? 4 * kFastChunks : 1];
+  f32x2 acc2[kFast ? C::kDPL : 1][2];                  // [column][row pair (0,1) | (2,3)]
+  float m_mine = -INFINITY, l_mine = 0.f;
+  int lim_mine = 0;
+  if constexpr (kFast) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int cc = 0; cc < kFastChunks; ++cc)
+#pragma unroll
+        for (int p2 = 0; p2 < 4; ++p2) {
+          const int d = 8 * (dc + 8 * cc) + 2 * p2;
+          qr[r][cc * 4 + p2] = pack2(q_s[q_index<T, D>(r, d)], q_s[q_index<T, D>(r, d + 1)]);
+        }
+#pragma unroll
+    for (int c = 0; c < C::kDPL; ++c) acc2[c][0] = acc2[c][1] = 0ull;
+    lim_mine = min(key_end, a.causal ? (L - n + (rho0 + my_r) / group + 1) : L);
+  }
   int j = 0;
   for (; j < my_tiles; ++j) {
     const int blk = b0 + warp + C::kWarps * j;
@@ -335,16 +378,119 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
     const int key0 = blk * kBlock;
     const int nvalid = min(kBlock, key_end - key0);
 
+    if constexpr (kFast) {
+      // ---- scores: partial dots of 4 keys x 4 rows over this lane's slice ----
+      f32x2 part[4][4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) part[t][r] = 0ull;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int key = kg * 4 + t;
+        const uint8_t* kline = ks + key * 128;
+        const int kswz = key & 7;
+#pragma unroll
+        for (int cc = 0; cc < kFastChunks; ++cc) {
+          const int chunk = dc + 8 * cc;
+          const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
+                                                            (((chunk & 7) ^ kswz) << 4));
+          const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
+          const f32x2 k45 = bf16x2_to_f32x2(kc.z), k67 = bf16x2_to_f32x2(kc.w);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            fma2(part[t][r], qr[r][cc * 4 + 0], k01);
+            fma2(part[t][r], qr[r][cc * 4 + 1], k23);
+            fma2(part[t][r], qr[r][cc * 4 + 2], k45);
+            fma2(part[t][r], qr[r][cc * 4 + 3], k67);
+          }
+        }
+      }
+      // ---- transpose-reduce over the 8 slice lanes (xor 4, 2, 1): values
+      //      v = row * 4 + key end up summed, two per lane (row my_r, keys
+      //      kk0 and kk0 + 1) ----
+      float sv[16];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 x = unpack2(part[t][r]);
+          sv[r * 4 + t] = x.x + x.y;
+        }
+      float s8[8], s4[4], s2[2];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float send = fb2 ? sv[i] : sv[i + 8], keep = fb2 ? sv[i + 8] : sv[i];
+        s8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float send = fb1 ? s8[i] : s8[i + 4], keep = fb1 ? s8[i + 4] : s8[i];
+        s4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float send = fb0 ? s4[i] : s4[i + 2], keep = fb0 ? s4[i + 2] : s4[i];
+        s2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+      }
+      // ---- online softmax of row my_r (the 8 lanes holding it share m) ----
+      const float x0 = key0 + kk0 < lim_mine ? s2[0] : -INFINITY;
+      const float x1 = key0 + kk0 + 1 < lim_mine ? s2[1] : -INFINITY;
+      float mx = fmaxf(x0, x1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mnew = fmaxf(m_mine, mx);
+      const float msafe = mnew == -INFINITY ? 0.f : mnew;
+      const float alpha = ex2(m_mine - msafe);
+      const float p0 = ex2(x0 - msafe), p1 = ex2(x1 - msafe);
+      l_mine = l_mine * alpha + (p0 + p1);
+      m_mine = mnew;
+      float* pw = p_s + warp * kPWarpFloats;           // [16 keys][4 rows], then alpha[4]
+      pw[kk0 * 4 + my_r] = p0;
+      pw[(kk0 + 1) * 4 + my_r] = p1;
+      if (kg == 0 && fb0 == 0) pw[kBlock * 4 + my_r] = alpha;
+      __syncwarp();
+      const ulonglong2 al = *reinterpret_cast<const ulonglong2*>(pw + kBlock * 4);
+#pragma unroll
+      for (int c = 0; c < C::kDPL; ++c) {
+        mul2(acc2[c][0], al.x);
+        mul2(acc2[c][1], al.y);
+      }
+      // ---- P.V: lane owns columns lane*kDPL.., rows paired in each FMA ----
+      auto pv_fast = [&](int jj) {
+        const ulonglong2 pp = *reinterpret_cast<const ulonglong2*>(pw + jj * 4);
+        f32x2 v[C::kPairs];
+        load_v_pairs<T, D>(vs + jj * C::kRowBytes, lane, v);
+#pragma unroll
+        for (int e = 0; e < C::kPairs; ++e) {
+          const float2 vf = unpack2(v[e]);
+          const f32x2 va = pack2(vf.x, vf.x), vb = pack2(vf.y, vf.y);
+          fma2(acc2[2 * e][0], pp.x, va);
+          fma2(acc2[2 * e][1], pp.y, va);
+          fma2(acc2[2 * e + 1][0], pp.x, vb);
+          fma2(acc2[2 * e + 1][1], pp.y, vb);
+        }
+      };
+      if (nvalid == kBlock) {
+#pragma unroll
+        for (int jj = 0; jj < kBlock; ++jj) pv_fast(jj);
+      } else {
+#pragma unroll 4
+        for (int jj = 0; jj < nvalid; ++jj) pv_fast(jj);
+      }
+    } else {
     // ---- scores: lane owns key key0 + kl, half of its row; halves summed by shuffle ----
     f32x2 sc2[R];
 #pragma unroll
     for (int rho = 0; rho < R; ++rho) sc2[rho] = 0ull;
-    const uint8_t* krow = ks + kl * C::kRowBytes + half * (C::kRowBytes / 2);
+    const uint8_t* kline = ks + kl * 128;              // this key's line in each K box
+    const int kswz = kl & 7;                           // its swizzle phase
 #pragma unroll
     for (int c = 0; c < C::kHalfChunks; ++c) {
-      const int idx = (c + lane) & (C::kHalfChunks - 1);
-      const int chunk = half * C::kHalfChunks + idx;   // 16-byte chunk of the full row
-      const uint4 kc = *reinterpret_cast<const uint4*>(krow + idx * 16);
+      const int chunk = half * C::kHalfChunks + c;     // 16-byte chunk of the full row
+      const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
+                                                        (((chunk & 7) ^ kswz) << 4));
       if constexpr (sizeof(T) == 4) {
         const f32x2 k01 = pack2(__uint_as_float(kc.x), __uint_as_float(kc.y));
         const f32x2 k23 = pack2(__uint_as_float(kc.z), __uint_as_float(kc.w));
@@ -410,8 +556,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
     __syncwarp();
 
     // ---- P.V: lane owns output columns lane*kDPL .. +kDPL-1 ----
-#pragma unroll 4
-    for (int jj = 0; jj < nvalid; ++jj) {
+    auto pv_key = [&](int jj) {
       const float* pr = p_s + ((warp * kBlock + jj) * R) * 2;
       f32x2 pp[R];
 #pragma unroll
@@ -427,7 +572,16 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
 #pragma unroll
         for (int e = 0; e < C::kPairs; ++e) fma2(acc[rho][e], pp[rho], v[e]);
       }
+    };
+    if (nvalid == kBlock) {
+      // a full block: fully unrolled, so its loads are issued ahead of the FMAs
+#pragma unroll
+      for (int jj = 0; jj < kBlock; ++jj) pv_key(jj);
+    } else {
+#pragma unroll 4
+      for (int jj = 0; jj < nvalid; ++jj) pv_key(jj);
     }
+    }  // generic path
     __syncwarp();
     issue(j + P);                      // refill the stage just consumed
   }
@@ -443,9 +597,26 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads)
   float* mw = reinterpret_cast<float*>(smem);
   float* lw = mw + C::kWarps * R;
   float* aw = lw + C::kWarps * R;
+  if constexpr (kFast) {
+    float lt = l_mine + __shfl_xor_sync(0xffffffffu, l_mine, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+    if (kg == 0 && fb0 == 0) {
+      mw[warp * R + my_r] = m_mine;
+      lw[warp * R + my_r] = lt;
+    }
+#pragma unroll
+    for (int c = 0; c < C::kDPL; ++c) {
+      const float2 a01 = unpack2(acc2[c][0]), a23 = unpack2(acc2[c][1]);
+      aw[(warp * R + 0) * D + lane * C::kDPL + c] = a01.x;
+      aw[(warp * R + 1) * D + lane * C::kDPL + c] = a01.y;
+      aw[(warp * R + 2) * D + lane * C::kDPL + c] = a23.x;
+      aw[(warp * R + 3) * D + lane * C::kDPL + c] = a23.y;
+    }
+  }
 #pragma unroll
   for (int rho = 0; rho < R; ++rho) {
-    if (rho < nrows) {
+    if (!kFast && rho < nrows) {
       const float lt = warp_sum(l[rho]);
       if (lane == 0) {
         mw[warp * R + rho] = m[rho];
