@@ -18,8 +18,8 @@ cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStrea
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
 int decode_ctas_per_sm(int head_dim);
 bool prefill_supported(int head_dim, bool bf16);
-cudaError_t launch_prefill(const AttnArgs& a, const void* k_cache, const void* v_cache,
-                           int head_dim, cudaStream_t stream);
+cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, cudaStream_t stream);
 }  // namespace pkv
 
 using namespace pkv;
@@ -88,6 +88,22 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_slots, int
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D map over q viewed as [num_tokens, num_q_heads, head_dim]: a box is 128
+// tokens of one head, 64 columns wide (128 bytes, 128B swizzle).
+bool encode_q_map(CUtensorMap* map, const void* q, int64_t num_tokens, int hq, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hq),
+                        static_cast<cuuint64_t>(num_tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hq) * d * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -244,8 +260,13 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode(a, kmap, vmap, bf16, head_dim, /*pdl=*/true, st);
   if (e == cudaSuccess && splits > 1) e = launch_combine(a, bf16, head_dim, st);
-  if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ)
-    e = launch_prefill(a, k_cache, v_cache, head_dim, st);
+  if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ) {
+    CUtensorMap qmap, vmap_sw;
+    if (num_tokens > 0x7FFFFFFFll || !encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim) ||
+        !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, bf16, true))
+      return PKV_ERR_CUDA;
+    e = launch_prefill(a, qmap, kmap, vmap_sw, st);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
     return PKV_ERR_CUDA;

@@ -1,18 +1,507 @@
 // Tiled causal prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// "Inside the engine: kernels, CUDA graphs and the life of a request":
+//   * "Never materialise the TxT matrix" - a block of queries stays on chip
+//     while K/V tiles stream past it; a running max m and denominator l are
+//     kept per row and the accumulator is rescaled by e^(m_old - m_new)
+//     whenever the max moves;
+//   * "Prefill has a full grid ..." - prefill has a tile per 128 queries, so it
+//     parallelises without splitting the key axis;
+//   * "Attention over a block table, not a contiguous tensor" - every K/V tile
+//     is gathered block by block through the request's block table.
+//
+// One CTA = (tile of 128 query rows of one request, one query head).
+//   warps 0-3 (128 threads): one query row per thread - softmax on the S row
+//     read from TMEM, O-row rescale in TMEM, P row written to shared memory,
+//     epilogue;
+//   warp 4: TMA producer - Q once (two 64-column boxes, 128B swizzle), then per
+//     128-key tile 8 blocks x 2 column halves of K and of V through the block
+//     table into a 2-stage ring;
+//   warp 5: allocates TMEM (S: columns 0-127, O: columns 128-255) and one lane
+//     issues the tcgen05.mma instructions: S = Q K^T (A, B K-major), then
+//     O += P V (P K-major, V MN-major), committing to mbarriers.
+// Blocks past the context are fetched at an out-of-range coordinate (TMA fills
+// zeros) and V rows past the last valid key are zeroed before P.V, so no stale
+// cache contents can reach the output.  Every wait is bounded (about 2 s); on
+// expiry PKV_FLAG_TIMEOUT is set and the CTA winds down without hanging.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace pkv {
 
-bool prefill_supported(int head_dim, bool bf16) {
-  (void)head_dim;
-  (void)bf16;
-  return false;
+namespace {
+
+constexpr int kQRows = 128;          // query rows per tile
+constexpr int kKeys = 128;           // keys per K/V tile (8 blocks)
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr int kHalf = 16384;         // one 64-column half of a 128-row bf16 tile (128 B rows)
+
+// shared-memory layout (bytes from a 1024-aligned base)
+constexpr int kOffQ = 0;                                  // 2 halves
+constexpr int kOffKV = 2 * kHalf;                         // stages x (K 2 halves, V 2 halves)
+constexpr int kStageBytes = 4 * kHalf;
+constexpr int kOffP = kOffKV + kStages * kStageBytes;     // 2 halves
+constexpr int kOffBar = kOffP + 2 * kHalf;
+constexpr int kNumBars = 1 + 2 * kStages + 3;             // q, kv_full[], kv_empty[], s, p, o
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 32;
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+
+// shared-memory matrix descriptor, 128B swizzle (sm_100 format, version 1)
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
 }
 
-cudaError_t launch_prefill(const AttnArgs& a, const void* k_cache, const void* v_cache,
-                           int head_dim, cudaStream_t stream) {
-  (void)a; (void)k_cache; (void)v_cache; (void)head_dim; (void)stream;
-  return cudaErrorNotSupported;
+// instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n, int b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2f_(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2f_(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                   const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bar_q = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = bars + 1 + kStages;
+  uint64_t* bar_s = bars + 1 + 2 * kStages;
+  uint64_t* bar_p = bar_s + 1;
+  uint64_t* bar_o = bar_s + 2;
+  int* misc = reinterpret_cast<int*>(smem + kOffMisc);   // [0] request, [1] tile, [2] tmem
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int tglob = blockIdx.x;
+
+  pdl_wait_primary();
+  pdl_launch_dependents();
+
+  // ---- which (request, query tile) this CTA owns: warp 0 scans the long
+  //      requests' tile counts (ceil(n / 128) for n > the decode bound) ----
+  if (warp == 0) {
+    int base = 0, found_r = -1, found_t = 0;
+    for (int r0 = 0; r0 < a.num_seqs && found_r < 0; r0 += 32) {
+      const int r = r0 + lane;
+      int nt = 0;
+      if (r < a.num_seqs) {
+        const int n = __ldg(a.qsl + r + 1) - __ldg(a.qsl + r);
+        nt = n > kDecodeMaxQ ? (n + kQRows - 1) / kQRows : 0;
+      }
+      int inc = nt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const int total = __shfl_sync(0xffffffffu, inc, 31);
+      if (tglob < base + total) {
+        const unsigned hit = __ballot_sync(0xffffffffu, base + inc > tglob);
+        const int src = __ffs(hit) - 1;
+        const int excl = __shfl_sync(0xffffffffu, inc - nt, src);
+        const int ntr = __shfl_sync(0xffffffffu, nt, src);
+        found_r = r0 + src;
+        found_t = ntr - 1 - (tglob - base - excl);        // last (heaviest) tiles first
+      }
+      base += total;
+    }
+    if (lane == 0) {
+      misc[0] = found_r;
+      misc[1] = found_t;
+    }
+  }
+  __syncthreads();
+  const int r = misc[0];
+  if (r < 0) return;                                     // past the last tile
+  const int tile = misc[1];
+  const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
+  const int n = q1 - q0;
+  const int L = __ldg(a.seq_lens + r);
+  if (q0 < 0 || q1 > a.num_tokens || n > L || n > a.max_query_len) {
+    if (threadIdx.x == 0 && h == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
+    return;
+  }
+  const int g = h / a.group;
+  const int i0 = tile * kQRows;
+  const int i_hi = min(i0 + kQRows, n) - 1;              // last real row of the tile
+  const int kv_len = a.causal ? (L - n + i_hi + 1) : L;
+  const int nblk_ctx = (kv_len + kBlock - 1) / kBlock;
+  if ((L + kBlock - 1) / kBlock > a.max_blocks_per_seq) {
+    if (threadIdx.x == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
+    return;
+  }
+  const int ntk = (kv_len + kKeys - 1) / kKeys;
+
+  // ---- barriers and TMEM ----
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_p, kQRows);
+    mbar_init(bar_o, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&misc[2])),
+                 "r"(256));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = static_cast<uint32_t>(misc[2]);
+  bool ok = true;
+
+  if (warp == 4) {
+    // ================= TMA producer =================
+    const uint64_t pol_kv = l2_policy_evict_last();      // K/V tiles are re-read by other CTAs
+    const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
+    const int oob = static_cast<int>(a.num_blocks * kBlock);   // a slot past the cache
+    if (lane == 0) {
+      tma_prefetch_desc(&qmap);
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
+      mbar_arrive_expect_tx(bar_q, 2 * kHalf);
+      for (int hh = 0; hh < 2; ++hh)
+        tma_load_3d(smem + kOffQ + hh * kHalf, &qmap, bar_q, hh * 64, h, q0 + i0,
+                    l2_policy_evict_first());
+    }
+    int kt = 0;
+    for (; kt < ntk; ++kt) {
+      const int st = kt % kStages;
+      if (kt >= kStages) {
+        uint32_t w = 1;
+        if (lane == 0) w = mbar_wait(&kv_empty[st], ((kt / kStages) - 1) & 1) ? 1u : 0u;
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      const int blk = kt * (kKeys / kBlock) + (lane & 7);
+      int32_t ent = -1;
+      if (lane < kKeys / kBlock && blk < nblk_ctx) {
+        ent = __ldg(table + blk);
+        if (ent < 0 || ent >= a.num_blocks) {
+          raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
+          ent = -1;
+        }
+      }
+      const int slot = ent >= 0 ? ent * kBlock : oob;   // past the context: zero fill
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 4 * kHalf);
+      __syncwarp();
+      if (lane < kKeys / kBlock) {
+        uint8_t* kst = smem + kOffKV + st * kStageBytes;
+        uint8_t* vst = kst + 2 * kHalf;
+        for (int hh = 0; hh < 2; ++hh) {
+          tma_load_3d(kst + hh * kHalf + lane * (kBlock * 128), &kmap, &kv_full[st], hh * 64, g,
+                      slot, pol_kv);
+          tma_load_3d(vst + hh * kHalf + lane * (kBlock * 128), &vmap, &kv_full[st], hh * 64, g,
+                      slot, pol_kv);
+        }
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+    // let every issued load land before the CTA can exit
+    if (lane == 0) {
+      for (int kk = max(0, kt - kStages); kk < kt; ++kk)
+        if (!mbar_wait(&kv_full[kk % kStages], (kk / kStages) & 1)) break;
+      mbar_wait(bar_q, 0);
+    }
+  } else if (warp == 5) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16(kQRows, kKeys, 0);
+      const uint32_t id_o = idesc_bf16(kQRows, 128, 1);
+      const uint32_t t_s = tbase, t_o = tbase + 128;
+      const uint32_t q_addr = smem_u32(smem + kOffQ);
+      const uint32_t p_addr = smem_u32(smem + kOffP);
+      if (!mbar_wait(bar_q, 0)) ok = false;
+      for (int kt = 0; ok && kt < ntk; ++kt) {
+        const int st = kt % kStages;
+        if (!mbar_wait(&kv_full[st], (kt / kStages) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + kOffKV + st * kStageBytes);
+        const uint32_t v_addr = k_addr + 2 * kHalf;
+        // S = Q K^T over D = 128 in 8 steps of 16
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+          umma(t_s, sdesc(q_addr + off, 16, 1024), sdesc(k_addr + off, 16, 1024), id_s, k > 0);
+        }
+        umma_commit(bar_s);
+        if (!mbar_wait(bar_p, kt & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // O += P V over the tile's 128 keys in 8 steps of 16
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t poff = (k >> 2) * kHalf + (k & 3) * 32;
+          umma(t_o, sdesc(p_addr + poff, 16, 1024), sdesc(v_addr + k * 2048, kHalf, 1024), id_o,
+               (kt > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(bar_o);
+        umma_commit(&kv_empty[st]);
+      }
+      if (!ok) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax / epilogue: thread = query row =================
+    const int row = threadIdx.x;                         // 0..127 == TMEM lane
+    const int i_r = i0 + row;
+    const int i_eff = min(i_r, n - 1);                   // padding rows mirror the last row
+    const int lim = a.causal ? (L - n + i_eff + 1) : L;  // keys < lim are visible
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t t_s = lane_base, t_o = lane_base + 128;
+    uint8_t* prow = smem + kOffP + row * 128;
+    const int pswz = row & 7;
+    float m = -INFINITY, l = 0.f;
+    for (int kt = 0; kt < ntk; ++kt) {
+      const bool got = mbar_wait(bar_s, kt & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kKeys];
+#pragma unroll
+      for (int c = 0; c < kKeys / 32; ++c) {
+        float v[32];
+        tmem_ld32(t_s + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+      }
+      const int key0 = kt * kKeys;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kKeys; ++i) {
+        s[i] = (key0 + i < lim) ? s[i] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
+      const float mnew = fmaxf(m, mx);
+      const float msafe = mnew == -INFINITY ? 0.f : mnew;
+      const float alpha = ex2f_(m - msafe);
+      float psum = 0.f;
+#pragma unroll
+      for (int i = 0; i < kKeys; ++i) {
+        s[i] = ex2f_(s[i] - msafe);
+        psum += s[i];
+      }
+      l = l * alpha + psum;
+      m = mnew;
+      if (kt > 0) {
+        // the previous P.V must be done before O is rescaled and P rewritten
+        const bool got_o = mbar_wait(bar_o, (kt - 1) & 1);
+        if (!__all_sync(0xffffffffu, got_o)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(t_o + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(t_o + c * 32, v);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+      }
+      // P row (bf16) into the K-major, 128B-swizzled A-operand tile
+#pragma unroll
+      for (int ch = 0; ch < kKeys / 8; ++ch) {
+        uint4 w;
+        w.x = pack_bf16(s[ch * 8 + 0], s[ch * 8 + 1]);
+        w.y = pack_bf16(s[ch * 8 + 2], s[ch * 8 + 3]);
+        w.z = pack_bf16(s[ch * 8 + 4], s[ch * 8 + 5]);
+        w.w = pack_bf16(s[ch * 8 + 6], s[ch * 8 + 7]);
+        *reinterpret_cast<uint4*>(prow + (ch >> 3) * kHalf + (((ch & 7) ^ pswz) << 4)) = w;
+      }
+      if (kt == ntk - 1 && key0 + row >= kv_len) {
+        // this key row of the last V tile lies past the context: zero it
+        uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kHalf + row * 128;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(vrow + hh * kHalf + c * 16) = make_uint4(0, 0, 0, 0);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    // ---- epilogue: O row / l -> output dtype, lse ----
+    bool got_o = ok && mbar_wait(bar_o, (ntk - 1) & 1);
+    got_o = __all_sync(0xffffffffu, got_o);
+    if (!got_o) {
+      ok = false;
+    } else {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = i_r < n;
+      __nv_bfloat16* orow =
+          static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(q0 + i_r) * a.hq + h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(t_o + c * 32, v);
+        if (store) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16(v[q * 8 + 0] * inv, v[q * 8 + 1] * inv);
+            w.y = pack_bf16(v[q * 8 + 2] * inv, v[q * 8 + 3] * inv);
+            w.z = pack_bf16(v[q * 8 + 4] * inv, v[q * 8 + 5] * inv);
+            w.w = pack_bf16(v[q * 8 + 6] * inv, v[q * 8 + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = w;
+          }
+        }
+      }
+      if (store && a.lse_out != nullptr)
+        a.lse_out[static_cast<int64_t>(q0 + i_r) * a.hq + h] =
+            l > 0.f ? (m + lg2f_(l)) * kLn2 : -INFINITY;
+    }
+    if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+  }
+
+  // ---- teardown: every TMEM access is done before the columns are freed ----
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(256));
+}
+
+bool prefill_supported(int head_dim, bool bf16) { return bf16 && head_dim == 128; }
+
+cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                           const CUtensorMap& vmap, cudaStream_t stream) {
+  static unsigned done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 32 || !((done >> dev) & 1u)) {
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    if (dev < 32) done |= 1u << dev;
+  }
+  // upper bound on the long requests' query tiles: sum ceil(n / 128) <=
+  // ceil(N / 128) + (number of long requests)
+  const int64_t long_reqs = std::min<int64_t>(a.num_seqs, a.num_tokens / (kDecodeMaxQ + 1));
+  const int64_t tiles = (a.num_tokens + kQRows - 1) / kQRows + long_reqs;
+  if (tiles <= 0) return cudaSuccess;
+  if (tiles > 0x7FFFFFFF || a.hq > 65535) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(a.hq));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel, qmap, kmap, vmap, a);
 }
 
 }  // namespace pkv
