@@ -17,7 +17,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStream_t stream);
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
 int decode_ctas_per_sm(int head_dim);
-bool prefill_supported(int head_dim, bool bf16);
+bool prefill_supported(int head_dim, bool bf16, int group);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t stream);
 }  // namespace pkv
@@ -241,7 +241,9 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
   a.scale_log2 = softmax_scale * kLog2e;
   a.causal = causal ? 1 : 0;
   a.num_splits = splits;
-  const bool tc_prefill = prefill_supported(head_dim, bf16);
+  // the tensor-core softmax takes the row max before scaling: positive scales only
+  const bool tc_prefill =
+      prefill_supported(head_dim, bf16, num_q_heads / num_kv_heads) && softmax_scale > 0.f;
   a.long_rows = tc_prefill ? 0 : 1;
   if (need > 0) {
     const size_t rows = static_cast<size_t>(splits) * num_seqs * kDecodeMaxQ * num_q_heads;

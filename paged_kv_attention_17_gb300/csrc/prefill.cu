@@ -33,21 +33,24 @@ namespace pkv {
 namespace {
 
 constexpr int kQRows = 128;          // query rows per tile
-constexpr int kKeys = 128;           // keys per K/V tile (8 blocks)
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
-constexpr int kHalf = 16384;         // one 64-column half of a 128-row bf16 tile (128 B rows)
+constexpr int kKeys = 64;            // keys per K/V tile (4 blocks)
+constexpr int kStages = 3;
+constexpr int kThreads = 320;        // 2 softmax warpgroups + producer warp + MMA warp
+constexpr int kQHalf = 16384;        // 64 columns of a 128-row bf16 tile (128-byte rows)
+constexpr int kKVHalf = 8192;        // 64 columns of a 64-row bf16 tile
 
 // shared-memory layout (bytes from a 1024-aligned base)
-constexpr int kOffQ = 0;                                  // 2 halves
-constexpr int kOffKV = 2 * kHalf;                         // stages x (K 2 halves, V 2 halves)
-constexpr int kStageBytes = 4 * kHalf;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;     // 2 halves
-constexpr int kOffBar = kOffP + 2 * kHalf;
-constexpr int kNumBars = 1 + 2 * kStages + 3;             // q, kv_full[], kv_empty[], s, p, o
+constexpr int kOffQ = 0;                                  // 2 tiles x 2 halves
+constexpr int kOffKV = 4 * kQHalf;                        // stages x (K 2 halves, V 2 halves)
+constexpr int kStageBytes = 4 * kKVHalf;
+constexpr int kOffP = kOffKV + kStages * kStageBytes;     // 2 tiles x [128 rows][64 keys]
+constexpr int kPBytes = kQRows * kKeys * 2;
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 1 + 2 * kStages + 6;             // q, kv_full[], kv_empty[], s[2], p[2], o[2]
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
+constexpr int kTmemCols = 512;       // S0 | S1 (64 each), O0 | O1 (128 each)
 
 // shared-memory matrix descriptor, 128B swizzle (sm_100 format, version 1)
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -152,13 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_q = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + kStages;
-  uint64_t* bar_s = bars + 1 + 2 * kStages;
-  uint64_t* bar_p = bar_s + 1;
-  uint64_t* bar_o = bar_s + 2;
+  uint64_t* bar_s = bars + 1 + 2 * kStages;              // [2]
+  uint64_t* bar_p = bar_s + 2;                           // [2]
+  uint64_t* bar_o = bar_s + 4;                           // [2]
   int* misc = reinterpret_cast<int*>(smem + kOffMisc);   // [0] request, [1] tile, [2] tmem
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  const int h0 = 2 * blockIdx.y;                         // query heads h0, h0 + 1 (same KV head)
   const int tglob = blockIdx.x;
 
   pdl_wait_primary();
@@ -205,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = q1 - q0;
   const int L = __ldg(a.seq_lens + r);
   if (q0 < 0 || q1 > a.num_tokens || n > L || n > a.max_query_len) {
-    if (threadIdx.x == 0 && h == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
+    if (threadIdx.x == 0 && h0 == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
     return;
   }
-  const int g = h / a.group;
+  const int g = h0 / a.group;
   const int i0 = tile * kQRows;
   const int i_hi = min(i0 + kQRows, n) - 1;              // last real row of the tile
   const int kv_len = a.causal ? (L - n + i_hi + 1) : L;
@@ -226,15 +229,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, kQRows);
-    mbar_init(bar_o, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_p[i], kQRows);
+      mbar_init(&bar_o[i], 1);
+    }
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&misc[2])),
-                 "r"(256));
+                 "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -243,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = static_cast<uint32_t>(misc[2]);
   bool ok = true;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ================= TMA producer =================
     const uint64_t pol_kv = l2_policy_evict_last();      // K/V tiles are re-read by other CTAs
     const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
@@ -252,10 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(bar_q, 2 * kHalf);
-      for (int hh = 0; hh < 2; ++hh)
-        tma_load_3d(smem + kOffQ + hh * kHalf, &qmap, bar_q, hh * 64, h, q0 + i0,
-                    l2_policy_evict_first());
+      mbar_arrive_expect_tx(bar_q, 4 * kQHalf);
+      const uint64_t pol_q = l2_policy_evict_first();
+      for (int t = 0; t < 2; ++t)
+        for (int hh = 0; hh < 2; ++hh)
+          tma_load_3d(smem + kOffQ + (2 * t + hh) * kQHalf, &qmap, bar_q, hh * 64, h0 + t,
+                      q0 + i0, pol_q);
     }
     int kt = 0;
     for (; kt < ntk; ++kt) {
@@ -268,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      const int blk = kt * (kKeys / kBlock) + (lane & 7);
+      const int blk = kt * (kKeys / kBlock) + (lane & 3);
       int32_t ent = -1;
       if (lane < kKeys / kBlock && blk < nblk_ctx) {
         ent = __ldg(table + blk);
@@ -278,16 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int slot = ent >= 0 ? ent * kBlock : oob;   // past the context: zero fill
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 4 * kHalf);
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
       __syncwarp();
       if (lane < kKeys / kBlock) {
         uint8_t* kst = smem + kOffKV + st * kStageBytes;
-        uint8_t* vst = kst + 2 * kHalf;
+        uint8_t* vst = kst + 2 * kKVHalf;
         for (int hh = 0; hh < 2; ++hh) {
-          tma_load_3d(kst + hh * kHalf + lane * (kBlock * 128), &kmap, &kv_full[st], hh * 64, g,
-                      slot, pol_kv);
-          tma_load_3d(vst + hh * kHalf + lane * (kBlock * 128), &vmap, &kv_full[st], hh * 64, g,
-                      slot, pol_kv);
+          tma_load_3d(kst + hh * kKVHalf + lane * (kBlock * 128), &kmap, &kv_full[st], hh * 64,
+                      g, slot, pol_kv);
+          tma_load_3d(vst + hh * kKVHalf + lane * (kBlock * 128), &vmap, &kv_full[st], hh * 64,
+                      g, slot, pol_kv);
         }
       }
       __syncwarp();
@@ -299,62 +306,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&kv_full[kk % kStages], (kk / kStages) & 1)) break;
       mbar_wait(bar_q, 0);
     }
-  } else if (warp == 5) {
-    // ================= MMA issuer =================
+  } else if (warp == 9) {
+    // ================= MMA issuer (one lane) =================
+    // Order per K/V tile k: PV0(k), S0(k+1), PV1(k), S1(k+1), so softmax group
+    // 0 works on S0(k+1) while group 1 still finishes tile k.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(kQRows, kKeys, 0);
       const uint32_t id_o = idesc_bf16(kQRows, 128, 1);
-      const uint32_t t_s = tbase, t_o = tbase + 128;
       const uint32_t q_addr = smem_u32(smem + kOffQ);
       const uint32_t p_addr = smem_u32(smem + kOffP);
-      if (!mbar_wait(bar_q, 0)) ok = false;
+      auto kv_addr = [&](int kt) { return smem_u32(smem + kOffKV + (kt % kStages) * kStageBytes); };
+      auto issue_s = [&](int t, int kt) {                // S_t = Q_t K^T, D = 128 in 8 steps
+        const uint32_t k_addr = kv_addr(kt);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          umma(tbase + t * kKeys,
+               sdesc(q_addr + t * 2 * kQHalf + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024),
+               sdesc(k_addr + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024), id_s, k > 0);
+        umma_commit(&bar_s[t]);
+      };
+      auto issue_pv = [&](int t, int kt) {               // O_t += P_t V, 64 keys in 4 steps
+        const uint32_t v_addr = kv_addr(kt) + 2 * kKVHalf;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          umma(tbase + 2 * kKeys + t * 128, sdesc(p_addr + t * kPBytes + k * 32, 16, 1024),
+               sdesc(v_addr + k * 2048, kKVHalf, 1024), id_o, (kt > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&bar_o[t]);
+      };
+      auto wait_kv = [&](int kt) {
+        if (!mbar_wait(&kv_full[kt % kStages], (kt / kStages) & 1)) return false;
+        tc_fence_after();
+        return true;
+      };
+      ok = mbar_wait(bar_q, 0) && wait_kv(0);
+      if (ok) {
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
       for (int kt = 0; ok && kt < ntk; ++kt) {
-        const int st = kt % kStages;
-        if (!mbar_wait(&kv_full[st], (kt / kStages) & 1)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&bar_p[0], kt & 1)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + kOffKV + st * kStageBytes);
-        const uint32_t v_addr = k_addr + 2 * kHalf;
-        // S = Q K^T over D = 128 in 8 steps of 16
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-          umma(t_s, sdesc(q_addr + off, 16, 1024), sdesc(k_addr + off, 16, 1024), id_s, k > 0);
+        issue_pv(0, kt);
+        const bool more = kt + 1 < ntk;
+        if (more) {
+          if (!wait_kv(kt + 1)) { ok = false; break; }
+          issue_s(0, kt + 1);
         }
-        umma_commit(bar_s);
-        if (!mbar_wait(bar_p, kt & 1)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&bar_p[1], kt & 1)) { ok = false; break; }
         tc_fence_after();
-        // O += P V over the tile's 128 keys in 8 steps of 16
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t poff = (k >> 2) * kHalf + (k & 3) * 32;
-          umma(t_o, sdesc(p_addr + poff, 16, 1024), sdesc(v_addr + k * 2048, kHalf, 1024), id_o,
-               (kt > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(bar_o);
-        umma_commit(&kv_empty[st]);
+        issue_pv(1, kt);
+        umma_commit(&kv_empty[kt % kStages]);
+        if (more) issue_s(1, kt + 1);
       }
       if (!ok) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     }
     __syncwarp();
   } else {
-    // ================= softmax / epilogue: thread = query row =================
-    const int row = threadIdx.x;                         // 0..127 == TMEM lane
+    // ================= softmax / epilogue: thread = query row of tile t =================
+    const int t = warp >> 2;                             // 0: warps 0-3, 1: warps 4-7
+    const int row = threadIdx.x - t * kQRows;            // 0..127 == TMEM lane
+    const int h = h0 + t;
     const int i_r = i0 + row;
     const int i_eff = min(i_r, n - 1);                   // padding rows mirror the last row
     const int lim = a.causal ? (L - n + i_eff + 1) : L;  // keys < lim are visible
-    const uint32_t lane_base = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t t_s = lane_base, t_o = lane_base + 128;
-    uint8_t* prow = smem + kOffP + row * 128;
+    const int lim_min = a.causal ? min(L - n + i0 + 1, L) : L;   // smallest lim of the tile
+    const uint32_t lane_base = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t t_s = lane_base + t * kKeys, t_o = lane_base + 2 * kKeys + t * 128;
+    uint8_t* prow = smem + kOffP + t * kPBytes + row * 128;
     const int pswz = row & 7;
+    const float sc = a.scale_log2;
     float m = -INFINITY, l = 0.f;
     for (int kt = 0; kt < ntk; ++kt) {
-      const bool got = mbar_wait(bar_s, kt & 1);
+      const bool got = mbar_wait(&bar_s[t], kt & 1);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -370,25 +393,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int key0 = kt * kKeys;
       float mx = -INFINITY;
+      if (key0 + kKeys <= lim_min) {                     // every key visible to every row
 #pragma unroll
-      for (int i = 0; i < kKeys; ++i) {
-        s[i] = (key0 + i < lim) ? s[i] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < kKeys; ++i) mx = fmaxf(mx, s[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) {
+          s[i] = (key0 + i < lim) ? s[i] : -INFINITY;
+          mx = fmaxf(mx, s[i]);
+        }
       }
-      const float mnew = fmaxf(m, mx);
+      // scores are unscaled here: m is kept in the scaled log2 domain
+      const float mnew = fmaxf(m, mx * sc);
       const float msafe = mnew == -INFINITY ? 0.f : mnew;
       const float alpha = ex2f_(m - msafe);
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < kKeys; ++i) {
-        s[i] = ex2f_(s[i] - msafe);
+        s[i] = ex2f_(fmaf(s[i], sc, -msafe));
         psum += s[i];
       }
       l = l * alpha + psum;
       m = mnew;
       if (kt > 0) {
-        // the previous P.V must be done before O is rescaled and P rewritten
-        const bool got_o = mbar_wait(bar_o, (kt - 1) & 1);
+        // the previous P.V of this tile must be done before O is rescaled and P rewritten
+        const bool got_o = mbar_wait(&bar_o[t], (kt - 1) & 1);
         if (!__all_sync(0xffffffffu, got_o)) {
           ok = false;
           break;
@@ -414,23 +443,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         w.y = pack_bf16(s[ch * 8 + 2], s[ch * 8 + 3]);
         w.z = pack_bf16(s[ch * 8 + 4], s[ch * 8 + 5]);
         w.w = pack_bf16(s[ch * 8 + 6], s[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(prow + (ch >> 3) * kHalf + (((ch & 7) ^ pswz) << 4)) = w;
+        *reinterpret_cast<uint4*>(prow + ((ch ^ pswz) << 4)) = w;
       }
-      if (kt == ntk - 1 && key0 + row >= kv_len) {
+      if (t == 0 && kt == ntk - 1 && row < kKeys && key0 + row >= kv_len) {
         // this key row of the last V tile lies past the context: zero it
-        uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kHalf + row * 128;
+        uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kKVHalf + row * 128;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(vrow + hh * kHalf + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + hh * kKVHalf + c * 16) = make_uint4(0, 0, 0, 0);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(&bar_p[t]);
     }
     // ---- epilogue: O row / l -> output dtype, lse ----
-    bool got_o = ok && mbar_wait(bar_o, (ntk - 1) & 1);
+    bool got_o = ok && mbar_wait(&bar_o[t], (ntk - 1) & 1);
     got_o = __all_sync(0xffffffffu, got_o);
     if (!got_o) {
       ok = false;
@@ -467,11 +496,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(256));
+  if (warp == 9)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
+                 "r"(kTmemCols));
 }
 
-bool prefill_supported(int head_dim, bool bf16) { return bf16 && head_dim == 128; }
+// The tensor-core path pairs two query heads of one KV head per CTA, so the
+// GQA group size must be even; other shapes run long rows on CUDA cores.
+bool prefill_supported(int head_dim, bool bf16, int group) {
+  return bf16 && head_dim == 128 && group % 2 == 0;
+}
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t stream) {
@@ -490,9 +524,9 @@ cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUt
   const int64_t long_reqs = std::min<int64_t>(a.num_seqs, a.num_tokens / (kDecodeMaxQ + 1));
   const int64_t tiles = (a.num_tokens + kQRows - 1) / kQRows + long_reqs;
   if (tiles <= 0) return cudaSuccess;
-  if (tiles > 0x7FFFFFFF || a.hq > 65535) return cudaErrorInvalidConfiguration;
+  if (tiles > 0x7FFFFFFF || a.hq / 2 > 65535) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(a.hq));
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(a.hq / 2));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;
