@@ -787,8 +787,6 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
   }
 }
 
-// Rows per CTA tile for a launch: the smallest of 4/8/16 holding one request's
-// decode rows (group x q_len), 16 when longer requests also run here.
 // Resident decode CTAs per SM for the bf16 single-token configuration (the
 // one the split heuristic sizes), from the occupancy calculator.
 int decode_ctas_per_sm(int head_dim) {
@@ -819,10 +817,14 @@ int decode_ctas_per_sm(int head_dim) {
   return cache[k];
 }
 
+// Rows per CTA tile: one token's GQA group rounded up to 4/8/16 rows, so a
+// single-token decode always takes the tile shape it needs (requests with a
+// few new tokens get one tile per token); 16 when the CUDA-core path also
+// runs long requests.
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows) {
-  const int q = long_rows ? max_query_len : (max_query_len < kDecodeMaxQ ? max_query_len : kDecodeMaxQ);
-  const int need = group * (q < 1 ? 1 : q);
-  return need <= 4 ? 4 : (need <= 8 ? 8 : 16);
+  (void)max_query_len;
+  if (long_rows) return 16;
+  return group <= 4 ? 4 : (group <= 8 ? 8 : 16);
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
