@@ -34,7 +34,7 @@ namespace {
 
 constexpr int kQRows = 128;          // query rows per tile
 constexpr int kKeys = 64;            // keys per K/V tile (4 blocks)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kThreads = 320;        // 2 softmax warpgroups + producer warp + MMA warp
 constexpr int kQHalf = 16384;        // 64 columns of a 128-row bf16 tile (128-byte rows)
 constexpr int kKVHalf = 8192;        // 64 columns of a 64-row bf16 tile
@@ -46,11 +46,12 @@ constexpr int kStageBytes = 4 * kKVHalf;
 constexpr int kOffP = kOffKV + kStages * kStageBytes;     // 2 tiles x [128 rows][64 keys]
 constexpr int kPBytes = kQRows * kKeys * 2;
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 1 + 2 * kStages + 6;             // q, kv_full[], kv_empty[], s[2], p[2], o[2]
+constexpr int kNumBars = 1 + 2 * kStages + 8;             // q, kv_full[], kv_empty[], s[2][2], p[2], o[2]
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kTmemCols = 512;       // S0 | S1 (64 each), O0 | O1 (128 each)
+constexpr int kTmemCols = 512;       // S[tile][buffer] (64 each), O0 | O1 (128 each)
+constexpr float kRescaleSlack = 8.f; // log2 units the reference max may lag the true max
 
 // shared-memory matrix descriptor, 128B swizzle (sm_100 format, version 1)
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -155,9 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_q = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + kStages;
-  uint64_t* bar_s = bars + 1 + 2 * kStages;              // [2]
-  uint64_t* bar_p = bar_s + 2;                           // [2]
-  uint64_t* bar_o = bar_s + 4;                           // [2]
+  uint64_t* bar_s = bars + 1 + 2 * kStages;              // [tile][buffer]
+  uint64_t* bar_p = bar_s + 4;                           // [tile]
+  uint64_t* bar_o = bar_s + 6;                           // [tile]
   int* misc = reinterpret_cast<int*>(smem + kOffMisc);   // [0] request, [1] tile, [2] tmem
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -229,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&bar_s[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar_s[i], 1);
       mbar_init(&bar_p[i], kQRows);
       mbar_init(&bar_o[i], 1);
     }
@@ -308,8 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ================= MMA issuer (one lane) =================
-    // Order per K/V tile k: PV0(k), S0(k+1), PV1(k), S1(k+1), so softmax group
-    // 0 works on S0(k+1) while group 1 still finishes tile k.
+    // S is double-buffered per query tile, so S_t(k+2) is issued as soon as
+    // softmax t has read S_t(k), and the exponentials of tile k+1 overlap
+    // P.V(k).  Per K/V tile k: PV0(k), S0(k+2), PV1(k), S1(k+2).
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(kQRows, kKeys, 0);
       const uint32_t id_o = idesc_bf16(kQRows, 128, 1);
@@ -318,18 +320,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kv_addr = [&](int kt) { return smem_u32(smem + kOffKV + (kt % kStages) * kStageBytes); };
       auto issue_s = [&](int t, int kt) {                // S_t = Q_t K^T, D = 128 in 8 steps
         const uint32_t k_addr = kv_addr(kt);
+        const int b = kt & 1;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          umma(tbase + t * kKeys,
+          umma(tbase + (2 * t + b) * kKeys,
                sdesc(q_addr + t * 2 * kQHalf + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024),
                sdesc(k_addr + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024), id_s, k > 0);
-        umma_commit(&bar_s[t]);
+        umma_commit(&bar_s[2 * t + b]);
       };
       auto issue_pv = [&](int t, int kt) {               // O_t += P_t V, 64 keys in 4 steps
         const uint32_t v_addr = kv_addr(kt) + 2 * kKVHalf;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          umma(tbase + 2 * kKeys + t * 128, sdesc(p_addr + t * kPBytes + k * 32, 16, 1024),
+          umma(tbase + 4 * kKeys + t * 128, sdesc(p_addr + t * kPBytes + k * 32, 16, 1024),
                sdesc(v_addr + k * 2048, kKVHalf, 1024), id_o, (kt > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bar_o[t]);
       };
@@ -338,25 +341,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         return true;
       };
-      ok = mbar_wait(bar_q, 0) && wait_kv(0);
-      if (ok) {
-        issue_s(0, 0);
-        issue_s(1, 0);
+      ok = mbar_wait(bar_q, 0);
+      for (int kt = 0; ok && kt < 2 && kt < ntk; ++kt) {
+        if (!wait_kv(kt)) { ok = false; break; }
+        issue_s(0, kt);
+        issue_s(1, kt);
       }
       for (int kt = 0; ok && kt < ntk; ++kt) {
+        const bool more = kt + 2 < ntk;
         if (!mbar_wait(&bar_p[0], kt & 1)) { ok = false; break; }
         tc_fence_after();
         issue_pv(0, kt);
-        const bool more = kt + 1 < ntk;
         if (more) {
-          if (!wait_kv(kt + 1)) { ok = false; break; }
-          issue_s(0, kt + 1);
+          if (!wait_kv(kt + 2)) { ok = false; break; }
+          issue_s(0, kt + 2);
         }
         if (!mbar_wait(&bar_p[1], kt & 1)) { ok = false; break; }
         tc_fence_after();
         issue_pv(1, kt);
         umma_commit(&kv_empty[kt % kStages]);
-        if (more) issue_s(1, kt + 1);
+        if (more) issue_s(1, kt + 2);
       }
       if (!ok) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     }
@@ -371,13 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = a.causal ? (L - n + i_eff + 1) : L;  // keys < lim are visible
     const int lim_min = a.causal ? min(L - n + i0 + 1, L) : L;   // smallest lim of the tile
     const uint32_t lane_base = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t t_s = lane_base + t * kKeys, t_o = lane_base + 2 * kKeys + t * 128;
+    const uint32_t t_o = lane_base + 4 * kKeys + t * 128;
     uint8_t* prow = smem + kOffP + t * kPBytes + row * 128;
     const int pswz = row & 7;
     const float sc = a.scale_log2;
     float m = -INFINITY, l = 0.f;
     for (int kt = 0; kt < ntk; ++kt) {
-      const bool got = mbar_wait(&bar_s[t], kt & 1);
+      const bool got = mbar_wait(&bar_s[2 * t + (kt & 1)], (kt >> 1) & 1);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {
         float v[32];
-        tmem_ld32(t_s + c * 32, v);
+        tmem_ld32(lane_base + (2 * t + (kt & 1)) * kKeys + c * 32, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
       }
@@ -403,8 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx = fmaxf(mx, s[i]);
         }
       }
-      // scores are unscaled here: m is kept in the scaled log2 domain
-      const float mnew = fmaxf(m, mx * sc);
+      // Scores are unscaled here; m (scaled log2 domain) is the reference max
+      // the accumulator and l are kept relative to.  It moves only when the
+      // row max exceeds it by more than kRescaleSlack, so p <= 2^kRescaleSlack
+      // and O is rescaled rarely; o = acc / l is unchanged by the choice.
+      const float mcand = fmaxf(m, mx * sc);
+      const float mnew = (mcand > m + kRescaleSlack) ? mcand : m;
       const float msafe = mnew == -INFINITY ? 0.f : mnew;
       const float alpha = ex2f_(m - msafe);
       float psum = 0.f;
