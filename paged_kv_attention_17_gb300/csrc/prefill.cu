@@ -92,9 +92,9 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// Issue a load of 32 consecutive fp32 columns of this thread's TMEM lane; the
+// registers are valid only after tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
       "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -104,7 +104,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Wait for this thread's outstanding TMEM loads.  The registers pass through
+// the wait as operands, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld32_issue(taddr, r);
+  tmem_wait_ld(r);
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -388,25 +408,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s[kKeys];
+      {
+        uint32_t ra[32], rb[32];                         // both halves in flight, one wait
+        const uint32_t sa = lane_base + (2 * t + (kt & 1)) * kKeys;
+        tmem_ld32_issue(sa, ra);
+        tmem_ld32_issue(sa + 32, rb);
+        tmem_wait_ld(ra);
+        tmem_wait_ld(rb);
 #pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) {
-        float v[32];
-        tmem_ld32(lane_base + (2 * t + (kt & 1)) * kKeys + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-      }
-      const int key0 = kt * kKeys;
-      float mx = -INFINITY;
-      if (key0 + kKeys <= lim_min) {                     // every key visible to every row
-#pragma unroll
-        for (int i = 0; i < kKeys; ++i) mx = fmaxf(mx, s[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < kKeys; ++i) {
-          s[i] = (key0 + i < lim) ? s[i] : -INFINITY;
-          mx = fmaxf(mx, s[i]);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(ra[i]);
+          s[32 + i] = __uint_as_float(rb[i]);
         }
       }
+      const int key0 = kt * kKeys;
+      if (key0 + kKeys > lim_min) {                      // a tile crossing the causal edge
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) s[i] = (key0 + i < lim) ? s[i] : -INFINITY;
+      }
+      float mx8[8];                                      // 8 independent max chains
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx8[j] = s[j];
+#pragma unroll
+      for (int i = 8; i < kKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       // Scores are unscaled here; m (scaled log2 domain) is the reference max
       // the accumulator and l are kept relative to.  It moves only when the
       // row max exceeds it by more than kRescaleSlack, so p <= 2^kRescaleSlack
@@ -415,12 +441,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mnew = (mcand > m + kRescaleSlack) ? mcand : m;
       const float msafe = mnew == -INFINITY ? 0.f : mnew;
       const float alpha = ex2f_(m - msafe);
-      float psum = 0.f;
+      float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 8 independent sums
 #pragma unroll
       for (int i = 0; i < kKeys; ++i) {
         s[i] = ex2f_(fmaf(s[i], sc, -msafe));
-        psum += s[i];
+        ps8[i & 7] += s[i];
       }
+      const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
+                         ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       l = l * alpha + psum;
       m = mnew;
       if (kt > 0) {
