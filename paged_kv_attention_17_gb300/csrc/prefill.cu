@@ -33,24 +33,23 @@ namespace pkv {
 namespace {
 
 constexpr int kQRows = 128;          // query rows per tile
-constexpr int kKeys = 64;            // keys per K/V tile (4 blocks)
-constexpr int kStages = 4;
+constexpr int kKeys = 128;           // keys per K/V tile (8 blocks)
+constexpr int kStages = 2;
 constexpr int kThreads = 320;        // 2 softmax warpgroups + producer warp + MMA warp
-constexpr int kQHalf = 16384;        // 64 columns of a 128-row bf16 tile (128-byte rows)
-constexpr int kKVHalf = 8192;        // 64 columns of a 64-row bf16 tile
+constexpr int kHalf = 16384;         // 64 columns of a 128-row bf16 tile (128-byte rows)
 
 // shared-memory layout (bytes from a 1024-aligned base)
-constexpr int kOffQ = 0;                                  // 2 tiles x 2 halves
-constexpr int kOffKV = 4 * kQHalf;                        // stages x (K 2 halves, V 2 halves)
-constexpr int kStageBytes = 4 * kKVHalf;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;     // 2 tiles x [128 rows][64 keys]
-constexpr int kPBytes = kQRows * kKeys * 2;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 1 + 2 * kStages + 8;             // q, kv_full[], kv_empty[], s[2][2], p[2], o[2]
+constexpr int kOffQ = 0;                                  // 2 query tiles x 2 halves
+constexpr int kOffKV = 4 * kHalf;                         // stages x (K 2 halves, V 2 halves)
+constexpr int kStageBytes = 4 * kHalf;
+constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+constexpr int kNumBars = 1 + 2 * kStages + 6;             // q, kv_full[], kv_empty[], s[2], p[2], o[2]
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kTmemCols = 512;       // S[tile][buffer] (64 each), O0 | O1 (128 each)
+// TMEM: S_t in columns [128 t, 128 t + 128) - its first 64 columns take P_t
+// (bf16 pairs) once the scores are read - and O_t in [256 + 128 t, ...).
+constexpr int kTmemCols = 512;
 constexpr float kRescaleSlack = 8.f; // log2 units the reference max may lag the true max
 
 // shared-memory matrix descriptor, 128B swizzle (sm_100 format, version 1)
@@ -76,6 +75,15 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(id), "r"(accumulate));
+}
+
+// O += A B with A (M x K, bf16 pairs per column) read from TMEM
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -129,6 +137,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -176,9 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_q = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = bars + 1 + kStages;
-  uint64_t* bar_s = bars + 1 + 2 * kStages;              // [tile][buffer]
-  uint64_t* bar_p = bar_s + 4;                           // [tile]
-  uint64_t* bar_o = bar_s + 6;                           // [tile]
+  uint64_t* bar_s = bars + 1 + 2 * kStages;              // [tile]
+  uint64_t* bar_p = bar_s + 2;                           // [tile]
+  uint64_t* bar_o = bar_s + 4;                           // [tile]
   int* misc = reinterpret_cast<int*>(smem + kOffMisc);   // [0] request, [1] tile, [2] tmem
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&bar_s[i], 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s[i], 1);
       mbar_init(&bar_p[i], kQRows);
       mbar_init(&bar_o[i], 1);
     }
@@ -278,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(bar_q, 4 * kQHalf);
+      mbar_arrive_expect_tx(bar_q, 4 * kHalf);
       const uint64_t pol_q = l2_policy_evict_first();
       for (int t = 0; t < 2; ++t)
         for (int hh = 0; hh < 2; ++hh)
-          tma_load_3d(smem + kOffQ + (2 * t + hh) * kQHalf, &qmap, bar_q, hh * 64, h0 + t,
+          tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64, h0 + t,
                       q0 + i0, pol_q);
     }
     int kt = 0;
@@ -296,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      const int blk = kt * (kKeys / kBlock) + (lane & 3);
+      const int blk = kt * (kKeys / kBlock) + (lane & 7);
       int32_t ent = -1;
       if (lane < kKeys / kBlock && blk < nblk_ctx) {
         ent = __ldg(table + blk);
@@ -310,12 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane < kKeys / kBlock) {
         uint8_t* kst = smem + kOffKV + st * kStageBytes;
-        uint8_t* vst = kst + 2 * kKVHalf;
+        uint8_t* vst = kst + 2 * kHalf;
         for (int hh = 0; hh < 2; ++hh) {
-          tma_load_3d(kst + hh * kKVHalf + lane * (kBlock * 128), &kmap, &kv_full[st], hh * 64,
-                      g, slot, pol_kv);
-          tma_load_3d(vst + hh * kKVHalf + lane * (kBlock * 128), &vmap, &kv_full[st], hh * 64,
-                      g, slot, pol_kv);
+          tma_load_3d(kst + hh * kHalf + lane * (kBlock * 128), &kmap, &kv_full[st], hh * 64, g,
+                      slot, pol_kv);
+          tma_load_3d(vst + hh * kHalf + lane * (kBlock * 128), &vmap, &kv_full[st], hh * 64, g,
+                      slot, pol_kv);
         }
       }
       __syncwarp();
@@ -329,31 +349,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ================= MMA issuer (one lane) =================
-    // S is double-buffered per query tile, so S_t(k+2) is issued as soon as
-    // softmax t has read S_t(k), and the exponentials of tile k+1 overlap
-    // P.V(k).  Per K/V tile k: PV0(k), S0(k+2), PV1(k), S1(k+2).
+    // Per K/V tile k: PV0(k), S0(k+1), PV1(k), S1(k+1).  The tensor pipe runs
+    // one issuer's MMAs in order, so S_t(k+1) overwrites the P_t columns only
+    // after PV_t(k) has read them; group 0's softmax of tile k+1 overlaps
+    // group 1's P.V of tile k and the reverse.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(kQRows, kKeys, 0);
       const uint32_t id_o = idesc_bf16(kQRows, 128, 1);
-      const uint32_t q_addr = smem_u32(smem + kOffQ);
-      const uint32_t p_addr = smem_u32(smem + kOffP);
-      auto kv_addr = [&](int kt) { return smem_u32(smem + kOffKV + (kt % kStages) * kStageBytes); };
+      // Descriptors are built once; a step only adds its byte offset >> 4 to
+      // the start-address field (every address stays below 256 KB, so the
+      // 14-bit field never carries).
+      const uint32_t kv_addr0 = smem_u32(smem + kOffKV);
+      const uint64_t dq = sdesc(smem_u32(smem + kOffQ), 16, 1024);
+      const uint64_t dk = sdesc(kv_addr0, 16, 1024);
+      const uint64_t dv = sdesc(kv_addr0 + 2 * kHalf, kHalf, 1024);
       auto issue_s = [&](int t, int kt) {                // S_t = Q_t K^T, D = 128 in 8 steps
-        const uint32_t k_addr = kv_addr(kt);
-        const int b = kt & 1;
+        const uint64_t a0 = dq + static_cast<uint64_t>((t * 2 * kHalf) >> 4);
+        const uint64_t b0 = dk + static_cast<uint64_t>(((kt % kStages) * kStageBytes) >> 4);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t off = static_cast<uint64_t>(((k >> 2) * kHalf + (k & 3) * 32) >> 4);
+          umma(tbase + t * kKeys, a0 + off, b0 + off, id_s, k > 0);
+        }
+        umma_commit(&bar_s[t]);
+      };
+      auto issue_pv = [&](int t, int kt) {               // O_t += P_t V, 128 keys in 8 steps
+        const uint64_t b0 = dv + static_cast<uint64_t>(((kt % kStages) * kStageBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          umma(tbase + (2 * t + b) * kKeys,
-               sdesc(q_addr + t * 2 * kQHalf + (k >> 2) * kQHalf + (k & 3) * 32, 16, 1024),
-               sdesc(k_addr + (k >> 2) * kKVHalf + (k & 3) * 32, 16, 1024), id_s, k > 0);
-        umma_commit(&bar_s[2 * t + b]);
-      };
-      auto issue_pv = [&](int t, int kt) {               // O_t += P_t V, 64 keys in 4 steps
-        const uint32_t v_addr = kv_addr(kt) + 2 * kKVHalf;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma(tbase + 4 * kKeys + t * 128, sdesc(p_addr + t * kPBytes + k * 32, 16, 1024),
-               sdesc(v_addr + k * 2048, kKVHalf, 1024), id_o, (kt > 0 || k > 0) ? 1u : 0u);
+          umma_ts(tbase + 2 * kKeys + t * 128, tbase + t * kKeys + k * 8,
+                  b0 + static_cast<uint64_t>((k * 2048) >> 4), id_o, (kt > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bar_o[t]);
       };
       auto wait_kv = [&](int kt) {
@@ -361,26 +386,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         return true;
       };
-      ok = mbar_wait(bar_q, 0);
-      for (int kt = 0; ok && kt < 2 && kt < ntk; ++kt) {
-        if (!wait_kv(kt)) { ok = false; break; }
-        issue_s(0, kt);
-        issue_s(1, kt);
+      ok = mbar_wait(bar_q, 0) && wait_kv(0);
+      if (ok) {
+        issue_s(0, 0);
+        issue_s(1, 0);
       }
       for (int kt = 0; ok && kt < ntk; ++kt) {
-        const bool more = kt + 2 < ntk;
+        const bool more = kt + 1 < ntk;
         if (!mbar_wait(&bar_p[0], kt & 1)) { ok = false; break; }
         tc_fence_after();
         issue_pv(0, kt);
         if (more) {
-          if (!wait_kv(kt + 2)) { ok = false; break; }
-          issue_s(0, kt + 2);
+          if (!wait_kv(kt + 1)) { ok = false; break; }
+          issue_s(0, kt + 1);
         }
         if (!mbar_wait(&bar_p[1], kt & 1)) { ok = false; break; }
         tc_fence_after();
         issue_pv(1, kt);
         umma_commit(&kv_empty[kt % kStages]);
-        if (more) issue_s(1, kt + 2);
+        if (more) issue_s(1, kt + 1);
       }
       if (!ok) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     }
@@ -395,13 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = a.causal ? (L - n + i_eff + 1) : L;  // keys < lim are visible
     const int lim_min = a.causal ? min(L - n + i0 + 1, L) : L;   // smallest lim of the tile
     const uint32_t lane_base = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t t_o = lane_base + 4 * kKeys + t * 128;
-    uint8_t* prow = smem + kOffP + t * kPBytes + row * 128;
-    const int pswz = row & 7;
+    const uint32_t t_s = lane_base + t * kKeys, t_o = lane_base + 2 * kKeys + t * 128;
     const float sc = a.scale_log2;
     float m = -INFINITY, l = 0.f;
     for (int kt = 0; kt < ntk; ++kt) {
-      const bool got = mbar_wait(&bar_s[2 * t + (kt & 1)], (kt >> 1) & 1);
+      const bool got = mbar_wait(&bar_s[t], kt & 1);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
         break;
@@ -409,16 +431,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[kKeys];
       {
-        uint32_t ra[32], rb[32];                         // both halves in flight, one wait
-        const uint32_t sa = lane_base + (2 * t + (kt & 1)) * kKeys;
-        tmem_ld32_issue(sa, ra);
-        tmem_ld32_issue(sa + 32, rb);
-        tmem_wait_ld(ra);
-        tmem_wait_ld(rb);
+        uint32_t r0[32], r1[32], r2[32], r3[32];         // all four loads in flight, one wait
+        tmem_ld32_issue(t_s, r0);
+        tmem_ld32_issue(t_s + 32, r1);
+        tmem_ld32_issue(t_s + 64, r2);
+        tmem_ld32_issue(t_s + 96, r3);
+        tmem_wait_ld(r0);
+        tmem_wait_ld(r1);
+        tmem_wait_ld(r2);
+        tmem_wait_ld(r3);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(ra[i]);
-          s[32 + i] = __uint_as_float(rb[i]);
+          s[i] = __uint_as_float(r0[i]);
+          s[32 + i] = __uint_as_float(r1[i]);
+          s[64 + i] = __uint_as_float(r2[i]);
+          s[96 + i] = __uint_as_float(r3[i]);
         }
       }
       const int key0 = kt * kKeys;
@@ -451,8 +478,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                          ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       l = l * alpha + psum;
       m = mnew;
+      // P row as bf16 pairs into the first 64 columns of this row's S (the
+      // scores are all read); the P.V MMA takes it from there as operand A
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) w[j] = pack_bf16(s[64 * c + 2 * j], s[64 * c + 2 * j + 1]);
+        tmem_st32u(t_s + 32 * c, w);
+      }
       if (kt > 0) {
-        // the previous P.V of this tile must be done before O is rescaled and P rewritten
+        // the previous P.V of this tile must be done before O is rescaled
         const bool got_o = mbar_wait(&bar_o[t], (kt - 1) & 1);
         if (!__all_sync(0xffffffffu, got_o)) {
           ok = false;
@@ -468,27 +504,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) v[i] *= alpha;
             tmem_st32(t_o + c * 32, v);
           }
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
       }
-      // P row (bf16) into the K-major, 128B-swizzled A-operand tile
-#pragma unroll
-      for (int ch = 0; ch < kKeys / 8; ++ch) {
-        uint4 w;
-        w.x = pack_bf16(s[ch * 8 + 0], s[ch * 8 + 1]);
-        w.y = pack_bf16(s[ch * 8 + 2], s[ch * 8 + 3]);
-        w.z = pack_bf16(s[ch * 8 + 4], s[ch * 8 + 5]);
-        w.w = pack_bf16(s[ch * 8 + 6], s[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ pswz) << 4)) = w;
-      }
-      if (t == 0 && kt == ntk - 1 && row < kKeys && key0 + row >= kv_len) {
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      if (t == 0 && kt == ntk - 1 && key0 + row >= kv_len) {
         // this key row of the last V tile lies past the context: zero it
-        uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kKVHalf + row * 128;
+        uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kHalf + row * 128;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(vrow + hh * kKVHalf + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + hh * kHalf + c * 16) = make_uint4(0, 0, 0, 0);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
