@@ -43,7 +43,7 @@ constexpr int kOffQ = 0;                                  // 2 query tiles x 2 h
 constexpr int kOffKV = 4 * kHalf;                         // stages x (K 2 halves, V 2 halves)
 constexpr int kStageBytes = 4 * kHalf;
 constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-constexpr int kNumBars = 1 + 2 * kStages + 6;             // q, kv_full[], kv_empty[], s[2], p[2], o[2]
+constexpr int kNumBars = 1 + 4 * kStages + 6;   // q, k_full[], v_full[], k_empty[], v_empty[], s[2], p[2], o[2]
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -194,9 +194,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* bar_q = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 1 + kStages;
-  uint64_t* bar_s = bars + 1 + 2 * kStages;              // [tile]
+  // K and V halves of a stage have their own barriers: K(k) is free once
+  // S1(k) has run, V(k) only after PV1(k), so K(k+2) can load earlier.
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + kStages;
+  uint64_t* k_empty = v_full + kStages;
+  uint64_t* v_empty = k_empty + kStages;
+  uint64_t* bar_s = bars + 1 + 4 * kStages;              // [tile]
   uint64_t* bar_p = bar_s + 2;                           // [tile]
   uint64_t* bar_o = bar_s + 4;                           // [tile]
   int* misc = reinterpret_cast<int*>(smem + kOffMisc);   // [0] request, [1] tile, [2] tmem
@@ -267,8 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_s[i], 1);
@@ -308,14 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kt = 0;
     for (; kt < ntk; ++kt) {
       const int st = kt % kStages;
-      if (kt >= kStages) {
-        uint32_t w = 1;
-        if (lane == 0) w = mbar_wait(&kv_empty[st], ((kt / kStages) - 1) & 1) ? 1u : 0u;
-        if (!__shfl_sync(0xffffffffu, w, 0)) {
-          ok = false;
-          break;
-        }
-      }
       const int blk = kt * (kKeys / kBlock) + (lane & 7);
       int32_t ent = -1;
       if (lane < kKeys / kBlock && blk < nblk_ctx) {
@@ -326,25 +324,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int slot = ent >= 0 ? ent * kBlock : oob;   // past the context: zero fill
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
-      __syncwarp();
-      if (lane < kKeys / kBlock) {
-        uint8_t* kst = smem + kOffKV + st * kStageBytes;
-        uint8_t* vst = kst + 2 * kHalf;
-        for (int hh = 0; hh < 2; ++hh) {
-          tma_load_3d(kst + hh * kHalf + lane * (kBlock * 128), &kmap, &kv_full[st], hh * 64, g,
-                      slot, pol_kv);
-          tma_load_3d(vst + hh * kHalf + lane * (kBlock * 128), &vmap, &kv_full[st], hh * 64, g,
-                      slot, pol_kv);
+      uint8_t* kst = smem + kOffKV + st * kStageBytes;
+      // K half of the stage, then its V half, each once its previous tile is done
+      for (int part = 0; part < 2; ++part) {
+        uint64_t* fullb = part == 0 ? &k_full[st] : &v_full[st];
+        uint64_t* emptyb = part == 0 ? &k_empty[st] : &v_empty[st];
+        if (kt >= kStages) {
+          uint32_t w = 1;
+          if (lane == 0) w = mbar_wait(emptyb, ((kt / kStages) - 1) & 1) ? 1u : 0u;
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
         }
+        if (lane == 0) mbar_arrive_expect_tx(fullb, 2 * kHalf);
+        __syncwarp();
+        if (lane < kKeys / kBlock) {
+          uint8_t* dst = kst + part * 2 * kHalf;
+          const CUtensorMap* map = part == 0 ? &kmap : &vmap;
+          for (int hh = 0; hh < 2; ++hh)
+            tma_load_3d(dst + hh * kHalf + lane * (kBlock * 128), map, fullb, hh * 64, g, slot,
+                        pol_kv);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      if (!ok) break;
     }
     if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     // let every issued load land before the CTA can exit
     if (lane == 0) {
-      for (int kk = max(0, kt - kStages); kk < kt; ++kk)
-        if (!mbar_wait(&kv_full[kk % kStages], (kk / kStages) & 1)) break;
+      for (int kk = max(0, kt - kStages); kk < min(kt + 1, ntk); ++kk) {
+        if (!mbar_wait(&k_full[kk % kStages], (kk / kStages) & 1)) break;
+        if (kk < kt && !mbar_wait(&v_full[kk % kStages], (kk / kStages) & 1)) break;
+      }
       mbar_wait(bar_q, 0);
     }
   } else if (warp == 9) {
@@ -381,30 +393,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                   b0 + static_cast<uint64_t>((k * 2048) >> 4), id_o, (kt > 0 || k > 0) ? 1u : 0u);
         umma_commit(&bar_o[t]);
       };
-      auto wait_kv = [&](int kt) {
-        if (!mbar_wait(&kv_full[kt % kStages], (kt / kStages) & 1)) return false;
+      auto wait_k = [&](int kt) {
+        if (!mbar_wait(&k_full[kt % kStages], (kt / kStages) & 1)) return false;
         tc_fence_after();
         return true;
       };
-      ok = mbar_wait(bar_q, 0) && wait_kv(0);
+      auto wait_v = [&](int kt) {
+        if (!mbar_wait(&v_full[kt % kStages], (kt / kStages) & 1)) return false;
+        tc_fence_after();
+        return true;
+      };
+      ok = mbar_wait(bar_q, 0) && wait_k(0);
       if (ok) {
         issue_s(0, 0);
         issue_s(1, 0);
+        umma_commit(&k_empty[0]);
       }
       for (int kt = 0; ok && kt < ntk; ++kt) {
         const bool more = kt + 1 < ntk;
-        if (!mbar_wait(&bar_p[0], kt & 1)) { ok = false; break; }
+        if (!mbar_wait(&bar_p[0], kt & 1) || !wait_v(kt)) { ok = false; break; }
         tc_fence_after();
         issue_pv(0, kt);
         if (more) {
-          if (!wait_kv(kt + 1)) { ok = false; break; }
+          if (!wait_k(kt + 1)) { ok = false; break; }
           issue_s(0, kt + 1);
         }
         if (!mbar_wait(&bar_p[1], kt & 1)) { ok = false; break; }
         tc_fence_after();
         issue_pv(1, kt);
-        umma_commit(&kv_empty[kt % kStages]);
-        if (more) issue_s(1, kt + 1);
+        umma_commit(&v_empty[kt % kStages]);
+        if (more) {
+          issue_s(1, kt + 1);
+          umma_commit(&k_empty[(kt + 1) % kStages]);
+        }
       }
       if (!ok) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     }
@@ -507,8 +528,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      if (t == 0 && kt == ntk - 1) {
+        // key rows of the last V tile past the context are zeroed, once the
+        // tile's V half has landed (its barrier is separate from K's)
+        const bool got_v = mbar_wait(&v_full[kt % kStages], (kt / kStages) & 1);
+        if (!__all_sync(0xffffffffu, got_v)) {
+          ok = false;
+          break;
+        }
+      }
       if (t == 0 && kt == ntk - 1 && key0 + row >= kv_len) {
-        // this key row of the last V tile lies past the context: zero it
         uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kHalf + row * 128;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh)
