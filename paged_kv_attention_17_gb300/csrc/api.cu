@@ -235,6 +235,7 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
   a.num_seqs = num_seqs;
   a.num_tokens = num_tokens;
   a.max_query_len = max_query_len;
+  a.max_seq_len = max_seq_len;
   a.hq = num_q_heads;
   a.hkv = num_kv_heads;
   a.group = num_q_heads / num_kv_heads;

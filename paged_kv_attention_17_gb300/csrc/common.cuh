@@ -33,6 +33,7 @@ struct AttnArgs {
   int num_seqs;
   int64_t num_tokens;
   int max_query_len;
+  int max_seq_len;        // host bound on seq_lens (speculative table prefetch)
   int hq, hkv, group;
   float scale_log2;       // softmax_scale * log2(e): scores live in the log2 domain
   int causal;

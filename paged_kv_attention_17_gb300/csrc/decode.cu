@@ -203,6 +203,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
   // ---- request geometry (uniform over the CTA); inputs only after the wait ----
   pdl_wait_primary();
   pdl_launch_dependents();
+  // This warp's first 32 block-table entries, fetched speculatively for the
+  // split range a context of max_seq_len keys would give, in flight together
+  // with the metadata; kept if the real range starts at the same block (so
+  // the K/V loads can be issued as soon as the metadata arrives).
+  const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
+  int spec_b0;
+  int32_t spec_entry = 0;
+  {
+    const int nb_spec = min((a.max_seq_len + kBlock - 1) / kBlock, a.max_blocks_per_seq);
+    const int per_spec = a.num_splits > 1 ? (nb_spec + a.num_splits - 1) / a.num_splits : nb_spec;
+    spec_b0 = min(s * per_spec, nb_spec);
+    const int bb = spec_b0 + warp + C::kWarps * lane;
+    if (bb < nb_spec) spec_entry = __ldg(table + bb);
+  }
   const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
   const int n = q1 - q0;
   const int L = __ldg(a.seq_lens + r);
@@ -279,11 +293,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
   __syncwarp();
 
   const uint64_t pol = l2_policy_evict_first();
-  const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
   // Block-table entries of this warp's blocks, 32 per refill: lane l holds the
   // entry of the warp's tile (base + l), block b0 + warp + kWarps * (base + l).
-  int32_t entry = 0;
-  int entry_base = -1;
+  int32_t entry = spec_entry;
+  int entry_base = (spec_b0 == b0) ? 0 : -1;
   auto issue = [&](int j) {            // warp-uniform call
     if (j >= my_tiles) return;
     if ((j & ~31) != entry_base) {
