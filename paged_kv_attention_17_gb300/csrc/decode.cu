@@ -14,17 +14,30 @@
 //   * One CTA = (split, kv head, row tile of one request).  The rows of a tile
 //     are the GQA group's query heads x the request's new tokens, so every K/V
 //     byte fetched from HBM feeds all query heads that share the kv head.
-//   * Each of the CTA's four warps owns a private ring of shared-memory stages
-//     (one mbarrier each, so every barrier has exactly one waiter and parity
-//     waits cannot alias); its lane 0 issues TMA tensor loads - one 16-row box
-//     per block, for K and for V - through the block table, whose entries the
-//     warp prefetches 32 at a time, one per lane.
-//   * A warp takes whole 32-key stages: lane j owns key j for
-//     the dot products (chunk order rotated per lane, conflict-free without
-//     swizzle), row max via warp shuffles, exp2 in the log2 domain, then lanes
-//     own D/32 output columns for P.V.  Each warp keeps its own (m, l, acc); the
-//     warps are merged through shared memory at the end (same algebra as the
-//     split merge).
+//   * Warp-specialised CTA: consumer warps (11 for 4-row tiles, 7 otherwise)
+//     each own a private ring of shared-memory stages, one 16-token block of
+//     K and of V per stage, with a "full" and an "empty" mbarrier per stage
+//     (one waiter each, so parity waits cannot alias).  One producer warp
+//     fetches the block table (32 entries per load, one per lane) and its
+//     lane 0 issues every TMA tensor load - one 16-row box per block for V,
+//     two swizzled boxes for K - in the order the consumers take the blocks
+//     (block b0 + i to warp i % warps), refilling a stage as soon as it is
+//     released.  Only the producer ever waits on the TMA unit's queue.
+//   * Barrier set-up and the tensor-map prefetch read no input, so they run
+//     before the programmatic-dependent-launch wait.
+//   * Generic path: a warp takes one 16-key block per stage; lanes j and
+//     j + 16 dot the two halves of key j's row against q in shared memory
+//     (K arrives in 128B-swizzled boxes, so the lanes' chunk reads do not
+//     conflict), one shuffle adds the halves, the row max is a shuffle tree,
+//     exp2 works in the log2 domain, then lanes own D/32 output columns for
+//     P.V.
+//   * Register-q path (bf16, 4-row tiles, the decode hot case): each lane
+//     holds a 16-dim slice of the four q rows in registers (loaded straight
+//     from global memory, no CTA-wide barrier), dots 4 keys with packed fp32
+//     FMAs and a transpose-reduce over the 8 slice lanes leaves it 2 scores
+//     of one row; P.V pairs rows in each packed FMA.
+//   * Each warp keeps its own (m, l, acc); the warps are merged through shared
+//     memory at the end (same algebra as the split merge).
 //   * Bounded mbarrier waits: a stuck pipeline sets PKV_FLAG_TIMEOUT and exits.
 #include "common.cuh"
 
@@ -72,7 +85,7 @@ __device__ __forceinline__ void mul2(f32x2& acc, f32x2 a) {
 }
 __device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pack2(bf16_lo(w), bf16_hi(w)); }
 
-template <typename T, int D>
+template <typename T, int D, int R = 4>
 struct DecodeCfg {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
   static constexpr int kHalfChunks = kRowBytes / 32;      // 16-byte chunks per half key row
@@ -84,14 +97,19 @@ struct DecodeCfg {
   static constexpr int kKBoxes = kRowBytes / 128;
   static constexpr int kKBoxBytes = kBlock * 128;
   static constexpr int kStageBytes = 2 * kBlock * kRowBytes;   // one block of K and of V
-  static constexpr int kWarps = 8;                        // warps per CTA
+  // Consumer (compute) warps per CTA.  With the producer warp the CTA has 12
+  // warps (three per SM sub-partition, 168 registers each) for 4-row tiles,
+  // whose register-q path fits that budget; wider tiles keep 255 registers
+  // with 7 + 1 warps.
+  static constexpr int kWarps = R == 4 ? 11 : 7;
   // A 192 KB ring per CTA (one CTA per SM): 3 blocks in flight per warp for
   // 256-byte rows, so a 19-way split of an 8K context has every block in
   // flight at once and longer contexts keep two prefetched per warp.
   static constexpr int kStagesRaw = 196608 / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 6 ? 6 : kStagesRaw);
   static constexpr int kStages = kWarps * kStagesPerWarp;
-  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kConsumerThreads = kWarps * 32;
+  static constexpr int kThreads = kConsumerThreads + 32;  // + one TMA producer warp
   static constexpr int kDPL = D / 32;                     // output columns per lane
   static constexpr int kPairs = kDPL / 2;
   static_assert((kHalfChunks & (kHalfChunks - 1)) == 0, "chunks per half row: power of two");
@@ -99,14 +117,14 @@ struct DecodeCfg {
 
 template <typename T, int D, int R>
 struct DecodeSmem {
-  using C = DecodeCfg<T, D>;
+  using C = DecodeCfg<T, D, R>;
   static constexpr int kStageArea = C::kStages * C::kStageBytes;
   static constexpr int kMergeBytes = C::kWarps * R * (D + 2) * 4;
   static constexpr int kRingBytes = kStageArea > kMergeBytes ? kStageArea : kMergeBytes;
   static constexpr int kQOff = kRingBytes;
   static constexpr int kPOff = kQOff + R * D * 4;
   static constexpr int kBarOff = kPOff + C::kWarps * kBlock * R * 8;
-  static constexpr int kBytes = kBarOff + C::kStages * 8;
+  static constexpr int kBytes = kBarOff + 2 * C::kStages * 8;   // full[] and empty[]
   static constexpr int kAlloc = kBytes + 1024;            // slack to align the base to 1 KB
 };
 
@@ -176,10 +194,10 @@ __device__ __forceinline__ void load_v_pairs(const uint8_t* vrow, int lane,
 }
 
 template <typename T, int D, int R>
-__global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
+__global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
-  using C = DecodeCfg<T, D>;
+  using C = DecodeCfg<T, D, R>;
   using Sm = DecodeSmem<T, D, R>;
   constexpr int P = C::kStagesPerWarp;
   // Register-q path for one token of a 4-query-head GQA group in bf16 (the
@@ -193,29 +211,49 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
   float* q_s = reinterpret_cast<float*>(smem + Sm::kQOff);
   float* p_s = reinterpret_cast<float*>(smem + Sm::kPOff);   // [warp][key][row] (p, p)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
+  uint64_t* empty = full + C::kStages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool producer = warp == C::kWarps;
   const int g = blockIdx.x % a.hkv;
   const int s = blockIdx.x / a.hkv;
   const int z = blockIdx.y;
   const int r = blockIdx.z;
 
+  // ---- set-up that reads no input: under programmatic dependent launch it
+  //      overlaps the tail of the previous kernel in the stream ----
+  if (producer && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
   // ---- request geometry (uniform over the CTA); inputs only after the wait ----
   pdl_wait_primary();
   pdl_launch_dependents();
-  // This warp's first 32 block-table entries, fetched speculatively for the
-  // split range a context of max_seq_len keys would give, in flight together
-  // with the metadata; kept if the real range starts at the same block (so
-  // the K/V loads can be issued as soon as the metadata arrives).
+  // The block-table entries of each consumer warp's first two blocks,
+  // fetched speculatively (producer lane w for warp w) for the split range a
+  // context of max_seq_len keys would give, in flight together with the
+  // metadata; kept if the real range starts at the same block, so the first
+  // K/V loads go out as soon as the metadata arrives.
   const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
-  int spec_b0;
-  int32_t spec_entry = 0;
-  {
+  int spec_b0 = -1;
+  int32_t spec_e0 = 0, spec_e1 = 0;
+  bool spec_v0 = false, spec_v1 = false;              // loaded (inside the bound)
+  if (producer && lane < C::kWarps) {
     const int nb_spec = min((a.max_seq_len + kBlock - 1) / kBlock, a.max_blocks_per_seq);
     const int per_spec = a.num_splits > 1 ? (nb_spec + a.num_splits - 1) / a.num_splits : nb_spec;
     spec_b0 = min(s * per_spec, nb_spec);
-    const int bb = spec_b0 + warp + C::kWarps * lane;
-    if (bb < nb_spec) spec_entry = __ldg(table + bb);
+    const int bb = spec_b0 + lane;
+    spec_v0 = bb < nb_spec;
+    spec_v1 = bb + C::kWarps < nb_spec;
+    if (spec_v0) spec_e0 = __ldg(table + bb);
+    if (spec_v1) spec_e1 = __ldg(table + bb + C::kWarps);
   }
   const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
   const int n = q1 - q0;
@@ -249,7 +287,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
   }
   if (b0 >= b1) {
     // empty split: partial (o = 0, lse = -inf) so the combine weighs it 0
-    for (int rho = warp; rho < nrows; rho += C::kWarps) {
+    for (int rho = warp; rho < nrows && warp < C::kWarps; rho += C::kWarps) {
       const int rr = rho0 + rho;
       const int64_t w = ws_row(a, s, r, rr / group, g * group + rr % group);
 #pragma unroll
@@ -262,82 +300,25 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
   const int nt = b1 - b0;                              // one block per stage
   const int my_tiles = nt > warp ? (nt - warp + C::kWarps - 1) / C::kWarps : 0;
 
-  // q elements this thread stages: raw loads issued before the table lookup
-  // and the K/V loads (so they do not queue behind them); first used, and
-  // converted, only after the first K/V loads are in flight
-  constexpr int kQPer = (R * D + C::kThreads - 1) / C::kThreads;
+  // q elements this thread stages (generic path), loaded before the causal
+  // limits are worked out so the loads are in flight meanwhile
+  constexpr int kQPer = kFast ? 1 : (R * D + C::kConsumerThreads - 1) / C::kConsumerThreads;
   T qraw[kQPer];
+  if constexpr (!kFast) {
 #pragma unroll
-  for (int u = 0; u < kQPer; ++u) {
-    const int e = threadIdx.x + u * C::kThreads;
-    const int rho = e / D, d = e % D;
-    if (e < R * D && rho < nrows) {
-      const int rr = rho0 + rho;
-      const int64_t t = q0 + rr / group;
-      const int h = g * group + rr % group;
-      qraw[u] = static_cast<const T*>(a.q)[(t * a.hq + h) * D + d];
-    } else {
-      qraw[u] = T(0.f);
-    }
-  }
-
-  // ---- barriers first, so the loads start while q is staged ----
-  if (lane == 0) {
-    if (warp == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-    }
-    for (int i = 0; i < P; ++i) mbar_init(&full[warp * P + i], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  const uint64_t pol = l2_policy_evict_first();
-  // Block-table entries of this warp's blocks, 32 per refill: lane l holds the
-  // entry of the warp's tile (base + l), block b0 + warp + kWarps * (base + l).
-  int32_t entry = spec_entry;
-  int entry_base = (spec_b0 == b0) ? 0 : -1;
-  auto issue = [&](int j) {            // warp-uniform call
-    if (j >= my_tiles) return;
-    if ((j & ~31) != entry_base) {
-      entry_base = j & ~31;
-      const int bb = b0 + warp + C::kWarps * (entry_base + lane);
-      entry = (bb < b1) ? __ldg(table + bb) : 0;
-    }
-    int id = __shfl_sync(0xffffffffu, entry, j & 31);
-    if (lane == 0) {
-      const int st = warp * P + (j % P);
-      uint8_t* ks = smem + st * C::kStageBytes;
-      uint8_t* vs = ks + kBlock * C::kRowBytes;
-      if (id < 0 || id >= a.num_blocks) {
-        raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
-        id = 0;
+    for (int u = 0; u < kQPer; ++u) {
+      const int e = threadIdx.x + u * C::kConsumerThreads;
+      const int rho = e / D, d = e % D;
+      if (!producer && e < R * D && rho < nrows) {
+        const int rr = rho0 + rho;
+        const int64_t t = q0 + rr / group;
+        const int h = g * group + rr % group;
+        qraw[u] = static_cast<const T*>(a.q)[(t * a.hq + h) * D + d];
+      } else {
+        qraw[u] = T(0.f);
       }
-      fence_proxy_async_smem();        // earlier generic reads of this stage before the refill
-      mbar_arrive_expect_tx(&full[st], 2 * kBlock * C::kRowBytes);
-#pragma unroll
-      for (int b = 0; b < C::kKBoxes; ++b)
-        tma_load_3d(ks + b * C::kKBoxBytes, &kmap, &full[st], b * C::kKBoxElems, g, id * kBlock,
-                    pol);
-      tma_load_3d(vs, &vmap, &full[st], 0, g, id * kBlock, pol);
     }
-    __syncwarp();
-  };
-#pragma unroll
-  for (int j = 0; j < P; ++j) issue(j);
-
-  // ---- stage q rows (pre-scaled into the log2 domain) ----
-#pragma unroll
-  for (int u = 0; u < kQPer; ++u) {
-    const int e = threadIdx.x + u * C::kThreads;
-    if (e < R * D) q_s[q_index<T, D>(e / D, e % D)] = static_cast<float>(qraw[u]) * a.scale_log2;
   }
-  // causal limit of each row: keys < lim[rho] are visible
-  int lim[R];
-#pragma unroll
-  for (int rho = 0; rho < R; ++rho)
-    lim[rho] = min(key_end, a.causal ? (L - n + (rho0 + rho) / group + 1) : L);
-  __syncthreads();
 
   float m[R], l[R];
   f32x2 acc[R][C::kPairs];
@@ -363,254 +344,341 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
   f32x2 acc2[kFast ? C::kDPL : 1][2];                  // [column][row pair (0,1) | (2,3)]
   float m_mine = -INFINITY, l_mine = 0.f;
   int lim_mine = 0;
-  if constexpr (kFast) {
+  // causal limit of each row: keys < lim[rho] are visible
+  int lim[R];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int cc = 0; cc < kFastChunks; ++cc)
-#pragma unroll
-        for (int p2 = 0; p2 < 4; ++p2) {
-          const int d = 8 * (dc + 8 * cc) + 2 * p2;
-          qr[r][cc * 4 + p2] = pack2(q_s[q_index<T, D>(r, d)], q_s[q_index<T, D>(r, d + 1)]);
-        }
-#pragma unroll
-    for (int c = 0; c < C::kDPL; ++c) acc2[c][0] = acc2[c][1] = 0ull;
-    lim_mine = min(key_end, a.causal ? (L - n + (rho0 + my_r) / group + 1) : L);
-  }
-  int j = 0;
-  for (; j < my_tiles; ++j) {
-    const int blk = b0 + warp + C::kWarps * j;
-    const int st = warp * P + (j % P);
-    const bool got = mbar_wait(&full[st], (j / P) & 1);
-    if (!__all_sync(0xffffffffu, got)) {
-      if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
-      break;
-    }
-    const uint8_t* ks = smem + st * C::kStageBytes;
-    const uint8_t* vs = ks + kBlock * C::kRowBytes;
-    const int key0 = blk * kBlock;
-    const int nvalid = min(kBlock, key_end - key0);
+  for (int rho = 0; rho < R; ++rho)
+    lim[rho] = min(key_end, a.causal ? (L - n + (rho0 + rho) / group + 1) : L);
 
+  if (producer) {
+    // ---- TMA producer: lane w feeds consumer warp w (blocks b0 + w + kWarps*j).
+    //      It polls the "empty" barrier of the warp's next stage without
+    //      blocking and, once the stage is released, issues the block's K and V
+    //      loads; lanes whose stages are free issue together.  The compute
+    //      warps never stall behind the TMA unit's queue. ----
+    const uint64_t pol = l2_policy_evict_first();
+    const int w = lane;
+    const int tiles = (w < C::kWarps && nt > w) ? (nt - w + C::kWarps - 1) / C::kWarps : 0;
+    auto entry_of = [&](int jj) -> int32_t {
+      return jj < tiles ? __ldg(table + b0 + w + C::kWarps * jj) : 0;
+    };
+    const bool spec_ok = spec_b0 == b0;
+    int32_t e_cur = spec_ok && spec_v0 ? spec_e0 : entry_of(0);
+    int32_t e_next = spec_ok && spec_v1 ? spec_e1 : entry_of(1);
+    int jj = 0;
+    unsigned long long t_progress = 0;
+    while (__any_sync(0xffffffffu, jj < tiles)) {
+      bool ready = false;
+      if (jj < tiles) {
+        const int st = w * P + jj % P;
+        ready = jj < P || mbar_ready(&empty[st], ((jj / P) - 1) & 1);
+        if (ready) {
+          int id = e_cur;
+          if (id < 0 || id >= a.num_blocks) {
+            raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
+            id = 0;
+          }
+          uint8_t* ks = smem + st * C::kStageBytes;
+          uint8_t* vs = ks + kBlock * C::kRowBytes;
+          fence_proxy_async_smem();    // the warp's reads of this stage before the refill
+          mbar_arrive_expect_tx(&full[st], 2 * kBlock * C::kRowBytes);
+#pragma unroll
+          for (int b = 0; b < C::kKBoxes; ++b)
+            tma_load_3d(ks + b * C::kKBoxBytes, &kmap, &full[st], b * C::kKBoxElems, g,
+                        id * kBlock, pol);
+          tma_load_3d(vs, &vmap, &full[st], 0, g, id * kBlock, pol);
+          ++jj;
+          e_cur = e_next;
+          e_next = entry_of(jj + 1);
+        }
+      }
+      if (__any_sync(0xffffffffu, ready)) {
+        t_progress = 0;
+      } else {
+        // nothing released yet: back off briefly; give up after ~2 s without progress
+        const unsigned long long now = globaltimer();
+        if (t_progress == 0) t_progress = now;
+        if (now - t_progress > kWaitLimitNs) {
+          if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    // every load this lane issued has landed before the merge reuses the ring
+    // (a no-op unless a consumer gave up early); bounded like every wait
+    for (int q = 0; q < P; ++q) {
+      const int c = jj > q ? (jj - q + P - 1) / P : 0;   // loads issued into stage q
+      if (c > 0 && !mbar_wait(&full[w * P + q], (c - 1) & 1)) break;
+    }
+    __syncwarp();
+  } else {
     if constexpr (kFast) {
-      // ---- scores: partial dots of 4 keys x 4 rows over this lane's slice ----
-      f32x2 part[4][4];
+      // this lane's q slice of all four rows straight from global memory (no
+      // CTA-wide staging), pre-scaled into the log2 domain
+      uint4 qv[4][kFastChunks];
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
+      for (int r4 = 0; r4 < 4; ++r4) {
+        const int rr = rho0 + r4;
+        const int64_t qrow =
+            (static_cast<int64_t>(q0 + rr / group) * a.hq + g * group + rr % group) * D;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) part[t][r] = 0ull;
+        for (int cc = 0; cc < kFastChunks; ++cc)
+          qv[r4][cc] = r4 < nrows ? __ldg(reinterpret_cast<const uint4*>(
+                                        static_cast<const T*>(a.q) + qrow + 8 * (dc + 8 * cc)))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int key = kg * 4 + t;
-        const uint8_t* kline = ks + key * 128;
-        const int kswz = key & 7;
+      for (int r4 = 0; r4 < 4; ++r4)
 #pragma unroll
         for (int cc = 0; cc < kFastChunks; ++cc) {
-          const int chunk = dc + 8 * cc;
-          const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
-                                                            (((chunk & 7) ^ kswz) << 4));
+          const uint32_t wq[4] = {qv[r4][cc].x, qv[r4][cc].y, qv[r4][cc].z, qv[r4][cc].w};
+#pragma unroll
+          for (int p2 = 0; p2 < 4; ++p2)
+            qr[r4][cc * 4 + p2] =
+                pack2(bf16_lo(wq[p2]) * a.scale_log2, bf16_hi(wq[p2]) * a.scale_log2);
+        }
+#pragma unroll
+      for (int c = 0; c < C::kDPL; ++c) acc2[c][0] = acc2[c][1] = 0ull;
+      lim_mine = min(key_end, a.causal ? (L - n + (rho0 + my_r) / group + 1) : L);
+    } else {
+      // ---- stage q rows (pre-scaled into the log2 domain), consumer warps only ----
+#pragma unroll
+      for (int u = 0; u < kQPer; ++u) {
+        const int e = threadIdx.x + u * C::kConsumerThreads;
+        if (e < R * D) q_s[q_index<T, D>(e / D, e % D)] = static_cast<float>(qraw[u]) * a.scale_log2;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(C::kConsumerThreads) : "memory");
+    }
+    int j = 0;
+    for (; j < my_tiles; ++j) {
+      const int blk = b0 + warp + C::kWarps * j;
+      const int st = warp * P + (j % P);
+      const bool got = mbar_wait(&full[st], (j / P) & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+        break;
+      }
+      const uint8_t* ks = smem + st * C::kStageBytes;
+      const uint8_t* vs = ks + kBlock * C::kRowBytes;
+      const int key0 = blk * kBlock;
+      const int nvalid = min(kBlock, key_end - key0);
+
+      if constexpr (kFast) {
+        // ---- scores: partial dots of 4 keys x 4 rows over this lane's slice ----
+        f32x2 part[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) part[t][r] = 0ull;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int key = kg * 4 + t;
+          const uint8_t* kline = ks + key * 128;
+          const int kswz = key & 7;
+#pragma unroll
+          for (int cc = 0; cc < kFastChunks; ++cc) {
+            const int chunk = dc + 8 * cc;
+            const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
+                                                              (((chunk & 7) ^ kswz) << 4));
+            const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
+            const f32x2 k45 = bf16x2_to_f32x2(kc.z), k67 = bf16x2_to_f32x2(kc.w);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              fma2(part[t][r], qr[r][cc * 4 + 0], k01);
+              fma2(part[t][r], qr[r][cc * 4 + 1], k23);
+              fma2(part[t][r], qr[r][cc * 4 + 2], k45);
+              fma2(part[t][r], qr[r][cc * 4 + 3], k67);
+            }
+          }
+        }
+        // ---- transpose-reduce over the 8 slice lanes (xor 4, 2, 1): values
+        //      v = row * 4 + key end up summed, two per lane (row my_r, keys
+        //      kk0 and kk0 + 1) ----
+        float sv[16];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float2 x = unpack2(part[t][r]);
+            sv[r * 4 + t] = x.x + x.y;
+          }
+        float s8[8], s4[4], s2[2];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float send = fb2 ? sv[i] : sv[i + 8], keep = fb2 ? sv[i + 8] : sv[i];
+          s8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float send = fb1 ? s8[i] : s8[i + 4], keep = fb1 ? s8[i + 4] : s8[i];
+          s4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float send = fb0 ? s4[i] : s4[i + 2], keep = fb0 ? s4[i + 2] : s4[i];
+          s2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        }
+        // ---- online softmax of row my_r (the 8 lanes holding it share m) ----
+        const float x0 = key0 + kk0 < lim_mine ? s2[0] : -INFINITY;
+        const float x1 = key0 + kk0 + 1 < lim_mine ? s2[1] : -INFINITY;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(m_mine, mx);
+        const float msafe = mnew == -INFINITY ? 0.f : mnew;
+        const float alpha = ex2(m_mine - msafe);
+        const float p0 = ex2(x0 - msafe), p1 = ex2(x1 - msafe);
+        l_mine = l_mine * alpha + (p0 + p1);
+        m_mine = mnew;
+        float* pw = p_s + warp * kPWarpFloats;           // [16 keys][4 rows], then alpha[4]
+        pw[kk0 * 4 + my_r] = p0;
+        pw[(kk0 + 1) * 4 + my_r] = p1;
+        if (kg == 0 && fb0 == 0) pw[kBlock * 4 + my_r] = alpha;
+        __syncwarp();
+        const ulonglong2 al = *reinterpret_cast<const ulonglong2*>(pw + kBlock * 4);
+#pragma unroll
+        for (int c = 0; c < C::kDPL; ++c) {
+          mul2(acc2[c][0], al.x);
+          mul2(acc2[c][1], al.y);
+        }
+        // ---- P.V: lane owns columns lane*kDPL.., rows paired in each FMA ----
+        auto pv_fast = [&](int jj) {
+          const ulonglong2 pp = *reinterpret_cast<const ulonglong2*>(pw + jj * 4);
+          f32x2 v[C::kPairs];
+          load_v_pairs<T, D>(vs + jj * C::kRowBytes, lane, v);
+#pragma unroll
+          for (int e = 0; e < C::kPairs; ++e) {
+            const float2 vf = unpack2(v[e]);
+            const f32x2 va = pack2(vf.x, vf.x), vb = pack2(vf.y, vf.y);
+            fma2(acc2[2 * e][0], pp.x, va);
+            fma2(acc2[2 * e][1], pp.y, va);
+            fma2(acc2[2 * e + 1][0], pp.x, vb);
+            fma2(acc2[2 * e + 1][1], pp.y, vb);
+          }
+        };
+        if (nvalid == kBlock) {
+#pragma unroll
+          for (int jj = 0; jj < kBlock; ++jj) pv_fast(jj);
+        } else {
+#pragma unroll 4
+          for (int jj = 0; jj < nvalid; ++jj) pv_fast(jj);
+        }
+      } else {
+      // ---- scores: lane owns key key0 + kl, half of its row; halves summed by shuffle ----
+      f32x2 sc2[R];
+#pragma unroll
+      for (int rho = 0; rho < R; ++rho) sc2[rho] = 0ull;
+      const uint8_t* kline = ks + kl * 128;              // this key's line in each K box
+      const int kswz = kl & 7;                           // its swizzle phase
+#pragma unroll
+      for (int c = 0; c < C::kHalfChunks; ++c) {
+        const int chunk = half * C::kHalfChunks + c;     // 16-byte chunk of the full row
+        const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
+                                                          (((chunk & 7) ^ kswz) << 4));
+        if constexpr (sizeof(T) == 4) {
+          const f32x2 k01 = pack2(__uint_as_float(kc.x), __uint_as_float(kc.y));
+          const f32x2 k23 = pack2(__uint_as_float(kc.z), __uint_as_float(kc.w));
+#pragma unroll
+          for (int rho = 0; rho < R; ++rho) {
+            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
+            fma2(sc2[rho], qa.x, k01);
+            fma2(sc2[rho], qa.y, k23);
+          }
+        } else {
           const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
           const f32x2 k45 = bf16x2_to_f32x2(kc.z), k67 = bf16x2_to_f32x2(kc.w);
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            fma2(part[t][r], qr[r][cc * 4 + 0], k01);
-            fma2(part[t][r], qr[r][cc * 4 + 1], k23);
-            fma2(part[t][r], qr[r][cc * 4 + 2], k45);
-            fma2(part[t][r], qr[r][cc * 4 + 3], k67);
+          for (int rho = 0; rho < R; ++rho) {
+            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
+            const ulonglong2 qb =
+                *reinterpret_cast<const ulonglong2*>(q_s + rho * D + D / 2 + chunk * 4);
+            fma2(sc2[rho], qa.x, k01);
+            fma2(sc2[rho], qa.y, k23);
+            fma2(sc2[rho], qb.x, k45);
+            fma2(sc2[rho], qb.y, k67);
           }
         }
       }
-      // ---- transpose-reduce over the 8 slice lanes (xor 4, 2, 1): values
-      //      v = row * 4 + key end up summed, two per lane (row my_r, keys
-      //      kk0 and kk0 + 1) ----
-      float sv[16];
+
+      // ---- online softmax update (per row; m uniform over the warp).  Every
+      //      row of the tile is computed (rows past nrows have q = 0 and are
+      //      never stored), so the rows' shuffle and exp chains interleave ----
+      const int key = key0 + kl;
+      float* pw = p_s + ((warp * kBlock + kl) * R) * 2;
+      float sv[R], mx[R];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float2 x = unpack2(part[t][r]);
-          sv[r * 4 + t] = x.x + x.y;
-        }
-      float s8[8], s4[4], s2[2];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float send = fb2 ? sv[i] : sv[i + 8], keep = fb2 ? sv[i + 8] : sv[i];
-        s8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      for (int rho = 0; rho < R; ++rho) {
+        const float2 t2 = unpack2(sc2[rho]);
+        sv[rho] = t2.x + t2.y;
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float send = fb1 ? s8[i] : s8[i + 4], keep = fb1 ? s8[i + 4] : s8[i];
-        s4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      for (int rho = 0; rho < R; ++rho) sv[rho] += __shfl_xor_sync(0xffffffffu, sv[rho], 16);
+#pragma unroll
+      for (int rho = 0; rho < R; ++rho) {
+        sv[rho] = key < lim[rho] ? sv[rho] : -INFINITY;
+        mx[rho] = sv[rho];
       }
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float send = fb0 ? s4[i] : s4[i + 2], keep = fb0 ? s4[i + 2] : s4[i];
-        s2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+      for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+        for (int rho = 0; rho < R; ++rho)
+          mx[rho] = fmaxf(mx[rho], __shfl_xor_sync(0xffffffffu, mx[rho], o));
       }
-      // ---- online softmax of row my_r (the 8 lanes holding it share m) ----
-      const float x0 = key0 + kk0 < lim_mine ? s2[0] : -INFINITY;
-      const float x1 = key0 + kk0 + 1 < lim_mine ? s2[1] : -INFINITY;
-      float mx = fmaxf(x0, x1);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float mnew = fmaxf(m_mine, mx);
-      const float msafe = mnew == -INFINITY ? 0.f : mnew;
-      const float alpha = ex2(m_mine - msafe);
-      const float p0 = ex2(x0 - msafe), p1 = ex2(x1 - msafe);
-      l_mine = l_mine * alpha + (p0 + p1);
-      m_mine = mnew;
-      float* pw = p_s + warp * kPWarpFloats;           // [16 keys][4 rows], then alpha[4]
-      pw[kk0 * 4 + my_r] = p0;
-      pw[(kk0 + 1) * 4 + my_r] = p1;
-      if (kg == 0 && fb0 == 0) pw[kBlock * 4 + my_r] = alpha;
+#pragma unroll
+      for (int rho = 0; rho < R; ++rho) {
+        const float mnew = fmaxf(m[rho], mx[rho]);
+        const float msafe = mnew == -INFINITY ? 0.f : mnew;
+        const float alpha = ex2(m[rho] - msafe);
+        const float p = ex2(sv[rho] - msafe);
+        l[rho] = l[rho] * alpha + (half == 0 ? p : 0.f);
+        m[rho] = mnew;
+        const f32x2 a2 = pack2(alpha, alpha);
+#pragma unroll
+        for (int e = 0; e < C::kPairs; ++e) mul2(acc[rho][e], a2);
+        if (half == 0) *reinterpret_cast<float2*>(pw + rho * 2) = make_float2(p, p);
+      }
       __syncwarp();
-      const ulonglong2 al = *reinterpret_cast<const ulonglong2*>(pw + kBlock * 4);
+
+      // ---- P.V: lane owns output columns lane*kDPL .. +kDPL-1 ----
+      auto pv_key = [&](int jj) {
+        const float* pr = p_s + ((warp * kBlock + jj) * R) * 2;
+        f32x2 pp[R];
 #pragma unroll
-      for (int c = 0; c < C::kDPL; ++c) {
-        mul2(acc2[c][0], al.x);
-        mul2(acc2[c][1], al.y);
-      }
-      // ---- P.V: lane owns columns lane*kDPL.., rows paired in each FMA ----
-      auto pv_fast = [&](int jj) {
-        const ulonglong2 pp = *reinterpret_cast<const ulonglong2*>(pw + jj * 4);
+        for (int r2 = 0; r2 < R; r2 += 2) {
+          const ulonglong2 t = *reinterpret_cast<const ulonglong2*>(pr + r2 * 2);
+          pp[r2] = t.x;
+          pp[r2 + 1] = t.y;
+        }
         f32x2 v[C::kPairs];
         load_v_pairs<T, D>(vs + jj * C::kRowBytes, lane, v);
 #pragma unroll
-        for (int e = 0; e < C::kPairs; ++e) {
-          const float2 vf = unpack2(v[e]);
-          const f32x2 va = pack2(vf.x, vf.x), vb = pack2(vf.y, vf.y);
-          fma2(acc2[2 * e][0], pp.x, va);
-          fma2(acc2[2 * e][1], pp.y, va);
-          fma2(acc2[2 * e + 1][0], pp.x, vb);
-          fma2(acc2[2 * e + 1][1], pp.y, vb);
+        for (int rho = 0; rho < R; ++rho) {
+#pragma unroll
+          for (int e = 0; e < C::kPairs; ++e) fma2(acc[rho][e], pp[rho], v[e]);
         }
       };
       if (nvalid == kBlock) {
+        // a full block: fully unrolled, so its loads are issued ahead of the FMAs
 #pragma unroll
-        for (int jj = 0; jj < kBlock; ++jj) pv_fast(jj);
+        for (int jj = 0; jj < kBlock; ++jj) pv_key(jj);
       } else {
 #pragma unroll 4
-        for (int jj = 0; jj < nvalid; ++jj) pv_fast(jj);
+        for (int jj = 0; jj < nvalid; ++jj) pv_key(jj);
       }
-    } else {
-    // ---- scores: lane owns key key0 + kl, half of its row; halves summed by shuffle ----
-    f32x2 sc2[R];
-#pragma unroll
-    for (int rho = 0; rho < R; ++rho) sc2[rho] = 0ull;
-    const uint8_t* kline = ks + kl * 128;              // this key's line in each K box
-    const int kswz = kl & 7;                           // its swizzle phase
-#pragma unroll
-    for (int c = 0; c < C::kHalfChunks; ++c) {
-      const int chunk = half * C::kHalfChunks + c;     // 16-byte chunk of the full row
-      const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
-                                                        (((chunk & 7) ^ kswz) << 4));
-      if constexpr (sizeof(T) == 4) {
-        const f32x2 k01 = pack2(__uint_as_float(kc.x), __uint_as_float(kc.y));
-        const f32x2 k23 = pack2(__uint_as_float(kc.z), __uint_as_float(kc.w));
-#pragma unroll
-        for (int rho = 0; rho < R; ++rho) {
-          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
-          fma2(sc2[rho], qa.x, k01);
-          fma2(sc2[rho], qa.y, k23);
-        }
-      } else {
-        const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
-        const f32x2 k45 = bf16x2_to_f32x2(kc.z), k67 = bf16x2_to_f32x2(kc.w);
-#pragma unroll
-        for (int rho = 0; rho < R; ++rho) {
-          const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
-          const ulonglong2 qb =
-              *reinterpret_cast<const ulonglong2*>(q_s + rho * D + D / 2 + chunk * 4);
-          fma2(sc2[rho], qa.x, k01);
-          fma2(sc2[rho], qa.y, k23);
-          fma2(sc2[rho], qb.x, k45);
-          fma2(sc2[rho], qb.y, k67);
-        }
-      }
+      }  // generic path
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);   // stage free for the producer
     }
-
-    // ---- online softmax update (per row; m uniform over the warp).  Every
-    //      row of the tile is computed (rows past nrows have q = 0 and are
-    //      never stored), so the rows' shuffle and exp chains interleave ----
-    const int key = key0 + kl;
-    float* pw = p_s + ((warp * kBlock + kl) * R) * 2;
-    float sv[R], mx[R];
-#pragma unroll
-    for (int rho = 0; rho < R; ++rho) {
-      const float2 t2 = unpack2(sc2[rho]);
-      sv[rho] = t2.x + t2.y;
-    }
-#pragma unroll
-    for (int rho = 0; rho < R; ++rho) sv[rho] += __shfl_xor_sync(0xffffffffu, sv[rho], 16);
-#pragma unroll
-    for (int rho = 0; rho < R; ++rho) {
-      sv[rho] = key < lim[rho] ? sv[rho] : -INFINITY;
-      mx[rho] = sv[rho];
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-#pragma unroll
-      for (int rho = 0; rho < R; ++rho)
-        mx[rho] = fmaxf(mx[rho], __shfl_xor_sync(0xffffffffu, mx[rho], o));
-    }
-#pragma unroll
-    for (int rho = 0; rho < R; ++rho) {
-      const float mnew = fmaxf(m[rho], mx[rho]);
-      const float msafe = mnew == -INFINITY ? 0.f : mnew;
-      const float alpha = ex2(m[rho] - msafe);
-      const float p = ex2(sv[rho] - msafe);
-      l[rho] = l[rho] * alpha + (half == 0 ? p : 0.f);
-      m[rho] = mnew;
-      const f32x2 a2 = pack2(alpha, alpha);
-#pragma unroll
-      for (int e = 0; e < C::kPairs; ++e) mul2(acc[rho][e], a2);
-      if (half == 0) *reinterpret_cast<float2*>(pw + rho * 2) = make_float2(p, p);
-    }
-    __syncwarp();
-
-    // ---- P.V: lane owns output columns lane*kDPL .. +kDPL-1 ----
-    auto pv_key = [&](int jj) {
-      const float* pr = p_s + ((warp * kBlock + jj) * R) * 2;
-      f32x2 pp[R];
-#pragma unroll
-      for (int r2 = 0; r2 < R; r2 += 2) {
-        const ulonglong2 t = *reinterpret_cast<const ulonglong2*>(pr + r2 * 2);
-        pp[r2] = t.x;
-        pp[r2 + 1] = t.y;
-      }
-      f32x2 v[C::kPairs];
-      load_v_pairs<T, D>(vs + jj * C::kRowBytes, lane, v);
-#pragma unroll
-      for (int rho = 0; rho < R; ++rho) {
-#pragma unroll
-        for (int e = 0; e < C::kPairs; ++e) fma2(acc[rho][e], pp[rho], v[e]);
-      }
-    };
-    if (nvalid == kBlock) {
-      // a full block: fully unrolled, so its loads are issued ahead of the FMAs
-#pragma unroll
-      for (int jj = 0; jj < kBlock; ++jj) pv_key(jj);
-    } else {
-#pragma unroll 4
-      for (int jj = 0; jj < nvalid; ++jj) pv_key(jj);
-    }
-    }  // generic path
-    __syncwarp();
-    issue(j + P);                      // refill the stage just consumed
-  }
-  if (j < my_tiles && lane == 0) {
-    // gave up early: let this warp's loads still in flight land before the
-    // shared memory is reused (bounded again)
-    for (int jj = j; jj < min(my_tiles, j + P); ++jj)
-      if (!mbar_wait(&full[warp * P + (jj % P)], (jj / P) & 1)) break;
-  }
+  }  // consumer warps
 
   // ---- merge the warps' states (shared memory reused) ----
   __syncthreads();
   float* mw = reinterpret_cast<float*>(smem);
   float* lw = mw + C::kWarps * R;
   float* aw = lw + C::kWarps * R;
-  if constexpr (kFast) {
+  if (kFast && !producer) {
     float lt = l_mine + __shfl_xor_sync(0xffffffffu, l_mine, 1);
     lt += __shfl_xor_sync(0xffffffffu, lt, 8);
     lt += __shfl_xor_sync(0xffffffffu, lt, 16);
@@ -629,7 +697,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
   }
 #pragma unroll
   for (int rho = 0; rho < R; ++rho) {
-    if (!kFast && rho < nrows) {
+    if (!kFast && !producer && rho < nrows) {
       const float lt = warp_sum(l[rho]);
       if (lane == 0) {
         mw[warp * R + rho] = m[rho];
@@ -642,7 +710,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 1)
     }
   }
   __syncthreads();
-  for (int rho = warp; rho < nrows; rho += C::kWarps) {
+  for (int rho = warp; rho < nrows && !producer; rho += C::kWarps) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, mw[w * R + rho]);
@@ -771,7 +839,7 @@ template <typename T, int D, int R>
 static cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int row_tiles, bool pdl,
                                    cudaStream_t stream) {
-  using C = DecodeCfg<T, D>;
+  using C = DecodeCfg<T, D, R>;
   using Sm = DecodeSmem<T, D, R>;
   cudaError_t e = ensure_smem_attr<T, D, R>();
   if (e != cudaSuccess) return e;
