@@ -72,8 +72,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 3-D map over one cache tensor viewed as [num_slots, num_kv_heads, head_dim]
 // (innermost first for TMA); a box covers 16 slots (one block) of one kv
-// head: the whole row unswizzled (V), or a 128-byte slice of it with the 128B
-// swizzle (K).
+// head: the whole row unswizzled (decode kernel), or a 128-byte slice of it
+// with the 128B swizzle (prefill tensor-core operands).
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_slots, int hkv, int d,
                       bool bf16, bool swizzle128) {
   auto fn = encode_fn();
@@ -254,9 +254,11 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
   }
   a.flag = error_flag;
   a.num_blocks = num_blocks;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
 
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, bf16, true) ||
+  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, bf16, false) ||
       !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, bf16, false))
     return PKV_ERR_CUDA;
 
@@ -264,11 +266,12 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
   cudaError_t e = launch_decode(a, kmap, vmap, bf16, head_dim, /*pdl=*/true, st);
   if (e == cudaSuccess && splits > 1) e = launch_combine(a, bf16, head_dim, st);
   if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ) {
-    CUtensorMap qmap, vmap_sw;
+    CUtensorMap qmap, kmap_sw, vmap_sw;
     if (num_tokens > 0x7FFFFFFFll || !encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim) ||
+        !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, bf16, true) ||
         !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, bf16, true))
       return PKV_ERR_CUDA;
-    e = launch_prefill(a, qmap, kmap, vmap_sw, st);
+    e = launch_prefill(a, qmap, kmap_sw, vmap_sw, st);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -43,6 +43,8 @@ struct AttnArgs {
   float* ws_lse;          // [S][num_seqs][kDecodeMaxQ][hq] (log2 domain)
   int32_t* flag;
   int64_t num_blocks;
+  const void* k_cache;    // cache bases, for L2 prefetch hints
+  const void* v_cache;
 };
 
 // ---------------------------------------------------------------------------
@@ -153,6 +155,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Bring the 128-byte line holding p into L2 (a hint: no data is returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Programmatic dependent launch: let the next kernel in the stream start its

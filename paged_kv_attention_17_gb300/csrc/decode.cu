@@ -17,17 +17,20 @@
 //   * Warp-specialised CTA: consumer warps (11 for 4-row tiles, 7 otherwise)
 //     each own a private ring of shared-memory stages, one 16-token block of
 //     K and of V per stage, with a "full" and an "empty" mbarrier per stage
-//     (one waiter each, so parity waits cannot alias).  One producer warp
-//     fetches the block table (32 entries per load, one per lane) and its
-//     lane 0 issues every TMA tensor load - one 16-row box per block for V,
-//     two swizzled boxes for K - in the order the consumers take the blocks
-//     (block b0 + i to warp i % warps), refilling a stage as soon as it is
-//     released.  Only the producer ever waits on the TMA unit's queue.
-//   * Barrier set-up and the tensor-map prefetch read no input, so they run
-//     before the programmatic-dependent-launch wait.
+//     (one waiter each, so parity waits cannot alias).  Lane w of one
+//     producer warp feeds consumer warp w (blocks b0 + w, b0 + w + warps,
+//     ...): it fetches their block-table entries ahead of use, polls the
+//     warp's "empty" barriers and issues one TMA box per block for K and one
+//     for V as soon as a stage is released.  Only the producer ever waits on
+//     the TMA unit's queue, whose per-operation cost is why a block takes
+//     two boxes and no more.
+//   * Before the programmatic-dependent-launch wait (while the previous
+//     kernel finishes) the CTA sets up its barriers, prefetches the tensor
+//     maps and warms L2 with the K/V blocks it will most likely read; every
+//     input it then uses is read after the wait.
 //   * Generic path: a warp takes one 16-key block per stage; lanes j and
 //     j + 16 dot the two halves of key j's row against q in shared memory
-//     (K arrives in 128B-swizzled boxes, so the lanes' chunk reads do not
+//     (each lane's chunk order is rotated by its key, so the reads do not
 //     conflict), one shuffle adds the halves, the row max is a shuffle tree,
 //     exp2 works in the log2 domain, then lanes own D/32 output columns for
 //     P.V.
@@ -89,13 +92,11 @@ template <typename T, int D, int R = 4>
 struct DecodeCfg {
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
   static constexpr int kHalfChunks = kRowBytes / 32;      // 16-byte chunks per half key row
-  // K arrives as 128-byte-wide TMA boxes with the 128B swizzle (16-byte chunk
-  // c of row j stored at chunk c ^ (j % 8) of its 128-byte line), so lanes on
-  // 16 different keys can all read one logical chunk without bank conflicts
-  // while every lane of a half-warp reads the same q chunk (a broadcast).
-  static constexpr int kKBoxElems = 128 / static_cast<int>(sizeof(T));
-  static constexpr int kKBoxes = kRowBytes / 128;
-  static constexpr int kKBoxBytes = kBlock * 128;
+  // K and V each arrive as one unswizzled TMA box per block (16 rows of the
+  // head's kRowBytes): the register-q path has the 8 lanes of a quarter-warp
+  // read 8 consecutive 16-byte chunks of one key row, the generic path
+  // rotates each lane's chunk order by its key, so neither conflicts on
+  // shared-memory banks.
   static constexpr int kStageBytes = 2 * kBlock * kRowBytes;   // one block of K and of V
   // Consumer (compute) warps per CTA.  With the producer warp the CTA has 12
   // warps (three per SM sub-partition, 168 registers each) for 4-row tiles,
@@ -108,6 +109,9 @@ struct DecodeCfg {
   static constexpr int kStagesRaw = 196608 / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 6 ? 6 : kStagesRaw);
   static constexpr int kStages = kWarps * kStagesPerWarp;
+  // Blocks per CTA warmed into L2 before the dependent-launch wait (a
+  // bounded share of L2 over all resident CTAs).
+  static constexpr int kPrefetchBlocks = 32;
   static constexpr int kConsumerThreads = kWarps * 32;
   static constexpr int kThreads = kConsumerThreads + 32;  // + one TMA producer warp
   static constexpr int kDPL = D / 32;                     // output columns per lane
@@ -232,6 +236,45 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
+  if (producer && z == 0) {
+    // ---- L2 warm-up while the previous kernel finishes: the K/V blocks this
+    //      CTA will most likely read (the split range a context of
+    //      max_seq_len keys gives, cut at the request's length and at
+    //      kPrefetchBlocks) are prefetched into L2.  The table and lengths
+    //      read here may still change before the wait, so they only steer
+    //      prefetches: every value used below is re-read after the wait, and
+    //      L2 stays coherent with the previous kernel's writes.  Only the
+    //      first row tile of a request this kernel will run warms L2 (the
+    //      others share its blocks or exit at once). ----
+    const int nb_spec = min((a.max_seq_len + kBlock - 1) / kBlock, a.max_blocks_per_seq);
+    const int per_spec = a.num_splits > 1 ? (nb_spec + a.num_splits - 1) / a.num_splits : nb_spec;
+    const int sb0 = min(s * per_spec, nb_spec);
+    // L2-only loads (ld.global.cg): nothing read before the wait may sit in L1,
+    // where the read-only loads after the wait could find a stale copy
+    const int len_hint = min(max(__ldcg(a.seq_lens + r), 0), a.max_seq_len);
+    const int n_hint = __ldcg(a.qsl + r + 1) - __ldcg(a.qsl + r);
+    const bool runs_here = n_hint >= 1 && (n_hint <= kDecodeMaxQ || a.long_rows);
+    const int sb1 = !runs_here ? sb0
+                               : min(min(sb0 + per_spec, (len_hint + kBlock - 1) / kBlock),
+                                     sb0 + C::kPrefetchBlocks);
+    constexpr int kLines = C::kRowBytes / 128 > 0 ? C::kRowBytes / 128 : 1;  // lines per row
+    const int64_t head_off = static_cast<int64_t>(g) * C::kRowBytes;
+    const int64_t slot_bytes = static_cast<int64_t>(a.hkv) * C::kRowBytes;
+    for (int base = sb0; base < sb1; base += 32) {
+      const int32_t e = base + lane < sb1 ? __ldcg(table + base + lane) : -1;
+      for (int i = 0; i < 32 && base + i < sb1; ++i) {
+        const int32_t id = __shfl_sync(0xffffffffu, e, i);
+        if (id < 0 || id >= a.num_blocks) continue;
+        for (int u = lane; u < kBlock * kLines; u += 32) {
+          const int64_t off = (static_cast<int64_t>(id) * kBlock + u / kLines) * slot_bytes +
+                              head_off + (u % kLines) * 128;
+          prefetch_l2(static_cast<const uint8_t*>(a.k_cache) + off);
+          prefetch_l2(static_cast<const uint8_t*>(a.v_cache) + off);
+        }
+      }
+    }
+  }
 
   // ---- request geometry (uniform over the CTA); inputs only after the wait ----
   pdl_wait_primary();
@@ -241,7 +284,6 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   // context of max_seq_len keys would give, in flight together with the
   // metadata; kept if the real range starts at the same block, so the first
   // K/V loads go out as soon as the metadata arrives.
-  const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
   int spec_b0 = -1;
   int32_t spec_e0 = 0, spec_e1 = 0;
   bool spec_v0 = false, spec_v1 = false;              // loaded (inside the bound)
@@ -380,12 +422,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
           }
           uint8_t* ks = smem + st * C::kStageBytes;
           uint8_t* vs = ks + kBlock * C::kRowBytes;
-          fence_proxy_async_smem();    // the warp's reads of this stage before the refill
+          if (jj >= P) fence_proxy_async_smem();   // the warp's reads of the stage before a refill
           mbar_arrive_expect_tx(&full[st], 2 * kBlock * C::kRowBytes);
-#pragma unroll
-          for (int b = 0; b < C::kKBoxes; ++b)
-            tma_load_3d(ks + b * C::kKBoxBytes, &kmap, &full[st], b * C::kKBoxElems, g,
-                        id * kBlock, pol);
+          tma_load_3d(ks, &kmap, &full[st], 0, g, id * kBlock, pol);
           tma_load_3d(vs, &vmap, &full[st], 0, g, id * kBlock, pol);
           ++jj;
           e_cur = e_next;
@@ -474,13 +513,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const int key = kg * 4 + t;
-          const uint8_t* kline = ks + key * 128;
-          const int kswz = key & 7;
+          const uint8_t* krow = ks + key * C::kRowBytes;
 #pragma unroll
           for (int cc = 0; cc < kFastChunks; ++cc) {
             const int chunk = dc + 8 * cc;
-            const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
-                                                              (((chunk & 7) ^ kswz) << 4));
+            const uint4 kc = *reinterpret_cast<const uint4*>(krow + chunk * 16);
             const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
             const f32x2 k45 = bf16x2_to_f32x2(kc.z), k67 = bf16x2_to_f32x2(kc.w);
 #pragma unroll
@@ -570,13 +607,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       f32x2 sc2[R];
 #pragma unroll
       for (int rho = 0; rho < R; ++rho) sc2[rho] = 0ull;
-      const uint8_t* kline = ks + kl * 128;              // this key's line in each K box
-      const int kswz = kl & 7;                           // its swizzle phase
+      const uint8_t* krow = ks + kl * C::kRowBytes;      // this key's row
 #pragma unroll
       for (int c = 0; c < C::kHalfChunks; ++c) {
-        const int chunk = half * C::kHalfChunks + c;     // 16-byte chunk of the full row
-        const uint4 kc = *reinterpret_cast<const uint4*>(kline + (chunk >> 3) * C::kKBoxBytes +
-                                                          (((chunk & 7) ^ kswz) << 4));
+        // 16-byte chunk of the full row, order rotated by the key (bank spread)
+        const int chunk = half * C::kHalfChunks + ((c + kl) & (C::kHalfChunks - 1));
+        const uint4 kc = *reinterpret_cast<const uint4*>(krow + chunk * 16);
         if constexpr (sizeof(T) == 4) {
           const f32x2 k01 = pack2(__uint_as_float(kc.x), __uint_as_float(kc.y));
           const f32x2 k23 = pack2(__uint_as_float(kc.z), __uint_as_float(kc.w));
@@ -748,6 +784,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   }
 }
 
+// Decode rows per request the combine grid covers: no row index reaches
+// max_query_len, and decode-class requests have at most kDecodeMaxQ.
+__host__ __device__ __forceinline__ int combine_rows(int max_query_len) {
+  return max_query_len < 1 ? 1 : (max_query_len > kDecodeMaxQ ? kDecodeMaxQ : max_query_len);
+}
+
 // Log-sum-exp merge of the split partials: for each (request, decode row,
 // q head), M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s.
 // One CTA of 4 warps per row: warp w takes splits s = w, w + 4, ...; all of a
@@ -762,8 +804,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   const int64_t item = blockIdx.x;
   const int h = static_cast<int>(item % a.hq);
   const int64_t ri = item / a.hq;
-  const int i = static_cast<int>(ri % kDecodeMaxQ);
-  const int r = static_cast<int>(ri / kDecodeMaxQ);
+  const int qrows = combine_rows(a.max_query_len);
+  const int i = static_cast<int>(ri % qrows);
+  const int r = static_cast<int>(ri / qrows);
   if (r >= a.num_seqs) return;
   const int S = a.num_splits;                          // <= kMaxSplits = 64
   // Partials are loaded before the row is known to exist (rows of requests
@@ -923,7 +966,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 }
 
 cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStream_t stream) {
-  const int64_t items = static_cast<int64_t>(a.num_seqs) * kDecodeMaxQ * a.hq;
+  const int64_t items = static_cast<int64_t>(a.num_seqs) * combine_rows(a.max_query_len) * a.hq;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(items));
   cfg.blockDim = dim3(128);
