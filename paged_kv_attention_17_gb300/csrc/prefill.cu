@@ -10,20 +10,26 @@
 //   * "Attention over a block table, not a contiguous tensor" - every K/V tile
 //     is gathered block by block through the request's block table.
 //
-// One CTA = (tile of 128 query rows of one request, one query head).
-//   warps 0-3 (128 threads): one query row per thread - softmax on the S row
-//     read from TMEM, O-row rescale in TMEM, P row written to shared memory,
-//     epilogue;
-//   warp 4: TMA producer - Q once (two 64-column boxes, 128B swizzle), then per
-//     128-key tile 8 blocks x 2 column halves of K and of V through the block
-//     table into a 2-stage ring;
-//   warp 5: allocates TMEM (S: columns 0-127, O: columns 128-255) and one lane
-//     issues the tcgen05.mma instructions: S = Q K^T (A, B K-major), then
-//     O += P V (P K-major, V MN-major), committing to mbarriers.
-// Blocks past the context are fetched at an out-of-range coordinate (TMA fills
-// zeros) and V rows past the last valid key are zeroed before P.V, so no stale
-// cache contents can reach the output.  Every wait is bounded (about 2 s); on
-// expiry PKV_FLAG_TIMEOUT is set and the CTA winds down without hanging.
+// One CTA = (tile of 128 query rows of one request, two query heads that share
+// a KV head), so every K/V tile feeds two S = Q K^T products.
+//   warps 0-3 and 4-7: one softmax warpgroup per query head, one query row per
+//     thread - the S row is read from TMEM (four 32-column loads, one wait),
+//     masked only on tiles that cross the causal edge, exponentiated in the
+//     log2 domain and written back into TMEM as bf16 P, which aliases the
+//     first 64 columns of its own S;
+//   warp 8: TMA producer - both heads' Q tiles once (64-column boxes, 128B
+//     swizzle), then per 128-key tile 8 blocks x 2 column halves of K and of V
+//     through the block table into a 2-stage ring, K and V with separate
+//     barriers so S can start before V lands;
+//   warp 9: allocates 512 TMEM columns (S/P and O per head) and one lane issues
+//     tcgen05.mma in a ping-pong order - P0 V(k), S0(k+1), P1 V(k), S1(k+1) - so
+//     one head's softmax overlaps the other head's MMAs; P.V takes P straight
+//     from TMEM as the A operand, V from shared memory (MN-major).
+// The running max is a lagged reference: a row moves it (and rescales its O
+// accumulator and l) only when a tile's max exceeds it by more than 8 log2
+// units, so every p = 2^(s - reference) stays at most 2^8 - far from overflow
+// in fp32 and in the bf16 P - and o = acc / l does not depend on which
+// reference acc and l share: the same online softmax with fewer O rescales.
 #include <algorithm>
 
 #include "common.cuh"
