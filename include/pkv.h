@@ -99,11 +99,13 @@ pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_m
  * "Inside the engine ...", section "Prefill has a full grid; decode at batch 1
  * has almost none": split the KV axis when there are too few query rows to
  * fill the GPU; at high batch the grid is already full and the split is
- * turned off.  With U = num_seqs x num_kv_heads decode work units and C the
- * decode CTAs device `device` holds at once (SM count x resident CTAs per SM):
- * 1 when U >= C (the grid is already full), else ceil(C / U) to fill the
- * device once; never fewer than 8 blocks (128 keys) per split nor more than
- * 64 splits.  Returns 0 for invalid arguments or device.
+ * turned off.  With U = num_seqs x num_kv_heads x row tiles of decode work
+ * units and C the decode CTAs device `device` holds at once (SM count x
+ * resident CTAs per SM), T = floor(7 C / 8): max(1, floor(T / U)), so one
+ * wave of split CTAs leaves some SMs free for the combine kernel and the next
+ * launch to start early (1 once the grid is nearly full);
+ * never fewer than 8 blocks (128 keys) per split nor more than 64 splits.
+ * Returns 0 for invalid arguments or device.
  */
 int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_heads,
                    int num_kv_heads, int head_dim, int device);

@@ -109,9 +109,10 @@ struct DecodeCfg {
   static constexpr int kStagesRaw = 196608 / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 6 ? 6 : kStagesRaw);
   static constexpr int kStages = kWarps * kStagesPerWarp;
-  // Blocks per CTA warmed into L2 before the dependent-launch wait (a
-  // bounded share of L2 over all resident CTAs).
-  static constexpr int kPrefetchBlocks = 32;
+  // Blocks per CTA warmed into L2 before the dependent-launch wait: each
+  // consumer warp's first block.  Warming more floods the memory queues that
+  // the previous kernel's last loads (the split combine) wait in.
+  static constexpr int kPrefetchBlocks = kWarps;
   static constexpr int kConsumerThreads = kWarps * 32;
   static constexpr int kThreads = kConsumerThreads + 32;  // + one TMA producer warp
   static constexpr int kDPL = D / 32;                     // output columns per lane

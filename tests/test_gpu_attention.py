@@ -145,6 +145,19 @@ def test_split_count_changes_nothing():
             assert np.abs(a - b).max() <= 1e-3 + 2 ** -7 * np.abs(a).max()
 
 
+def test_split_heuristic_rule():
+    # one wave of split CTAs over 7/8 of the SMs (one decode CTA per SM), at
+    # least 8 blocks per split, split off once the grid is nearly full
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    target = sms * 7 // 8
+    # batch 1, 8 KV heads, GQA group 4 (one 4-row tile): U = 8
+    assert pkv.pkv_num_splits(1, 1, 8192, 32, 8, 128) == min(64, max(1, target // 8))
+    # a short context caps the split at 8 blocks (128 keys) per split
+    assert pkv.pkv_num_splits(1, 1, 300, 32, 8, 128) == 2
+    # 64 decodes x 8 KV heads fill the device: no split
+    assert pkv.pkv_num_splits(64, 1, 4096, 32, 8, 128) == 1
+
+
 def test_block_permutation_is_bit_identical():
     # "paging changes only the access pattern": relocate every physical block
     # and rewrite the tables; with a fixed split count the result is identical
