@@ -157,6 +157,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Read-only load issued where it stands in the program (volatile asm): used
+// for loads that must be in flight early rather than next to their first use.
+__device__ __forceinline__ int32_t ld_early(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // Bring the 128-byte line holding p into L2 (a hint: no data is returned).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -16,14 +16,15 @@
 //     byte fetched from HBM feeds all query heads that share the kv head.
 //   * Warp-specialised CTA: consumer warps (11 for 4-row tiles, 7 otherwise)
 //     each own a private ring of shared-memory stages, one 16-token block of
-//     K and of V per stage, with a "full" and an "empty" mbarrier per stage
-//     (one waiter each, so parity waits cannot alias).  Lane w of one
+//     K and of V per stage, with "K full", "V full" and "empty" mbarriers per
+//     stage (one waiter each, so parity waits cannot alias).  Lane w of one
 //     producer warp feeds consumer warp w (blocks b0 + w, b0 + w + warps,
 //     ...): it fetches their block-table entries ahead of use, polls the
 //     warp's "empty" barriers and issues one TMA box per block for K and one
-//     for V as soon as a stage is released.  Only the producer ever waits on
-//     the TMA unit's queue, whose per-operation cost is why a block takes
-//     two boxes and no more.
+//     for V as soon as a stage is released (K and V complete separate
+//     barriers, so a warp computes its scores while V lands).  Only the
+//     producer ever waits on the TMA unit's queue, whose per-operation cost
+//     is why a block takes two boxes and no more.
 //   * Before the programmatic-dependent-launch wait (while the previous
 //     kernel finishes) the CTA sets up its barriers, prefetches the tensor
 //     maps and warms L2 with the K/V blocks it will most likely read; every
@@ -129,7 +130,7 @@ struct DecodeSmem {
   static constexpr int kQOff = kRingBytes;
   static constexpr int kPOff = kQOff + R * D * 4;
   static constexpr int kBarOff = kPOff + C::kWarps * kBlock * R * 8;
-  static constexpr int kBytes = kBarOff + 2 * C::kStages * 8;   // full[] and empty[]
+  static constexpr int kBytes = kBarOff + 3 * C::kStages * 8;   // kfull[], vfull[], empty[]
   static constexpr int kAlloc = kBytes + 1024;            // slack to align the base to 1 KB
 };
 
@@ -215,8 +216,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* q_s = reinterpret_cast<float*>(smem + Sm::kQOff);
   float* p_s = reinterpret_cast<float*>(smem + Sm::kPOff);   // [warp][key][row] (p, p)
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);
-  uint64_t* empty = full + C::kStages;
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);   // K of a stage landed
+  uint64_t* vfull = kfull + C::kStages;                                 // V of a stage landed
+  uint64_t* empty = vfull + C::kStages;                                 // stage released
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = warp == C::kWarps;
@@ -231,7 +233,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
       mbar_init(&empty[i], 1);
     }
     fence_mbar_init();
@@ -295,8 +298,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     const int bb = spec_b0 + lane;
     spec_v0 = bb < nb_spec;
     spec_v1 = bb + C::kWarps < nb_spec;
-    if (spec_v0) spec_e0 = __ldg(table + bb);
-    if (spec_v1) spec_e1 = __ldg(table + bb + C::kWarps);
+    if (spec_v0) spec_e0 = ld_early(table + bb);
+    if (spec_v1) spec_e1 = ld_early(table + bb + C::kWarps);
   }
   const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
   const int n = q1 - q0;
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     const int w = lane;
     const int tiles = (w < C::kWarps && nt > w) ? (nt - w + C::kWarps - 1) / C::kWarps : 0;
     auto entry_of = [&](int jj) -> int32_t {
-      return jj < tiles ? __ldg(table + b0 + w + C::kWarps * jj) : 0;
+      return jj < tiles ? ld_early(table + b0 + w + C::kWarps * jj) : 0;
     };
     const bool spec_ok = spec_b0 == b0;
     int32_t e_cur = spec_ok && spec_v0 ? spec_e0 : entry_of(0);
@@ -424,9 +427,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
           uint8_t* ks = smem + st * C::kStageBytes;
           uint8_t* vs = ks + kBlock * C::kRowBytes;
           if (jj >= P) fence_proxy_async_smem();   // the warp's reads of the stage before a refill
-          mbar_arrive_expect_tx(&full[st], 2 * kBlock * C::kRowBytes);
-          tma_load_3d(ks, &kmap, &full[st], 0, g, id * kBlock, pol);
-          tma_load_3d(vs, &vmap, &full[st], 0, g, id * kBlock, pol);
+          // K and V on their own barriers: all ready lanes' K boxes go out
+          // first, and a consumer starts its scores while V is landing
+          mbar_arrive_expect_tx(&kfull[st], kBlock * C::kRowBytes);
+          tma_load_3d(ks, &kmap, &kfull[st], 0, g, id * kBlock, pol);
+          mbar_arrive_expect_tx(&vfull[st], kBlock * C::kRowBytes);
+          tma_load_3d(vs, &vmap, &vfull[st], 0, g, id * kBlock, pol);
           ++jj;
           e_cur = e_next;
           e_next = entry_of(jj + 1);
@@ -449,7 +455,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     // (a no-op unless a consumer gave up early); bounded like every wait
     for (int q = 0; q < P; ++q) {
       const int c = jj > q ? (jj - q + P - 1) / P : 0;   // loads issued into stage q
-      if (c > 0 && !mbar_wait(&full[w * P + q], (c - 1) & 1)) break;
+      if (c > 0 && (!mbar_wait(&kfull[w * P + q], (c - 1) & 1) ||
+                    !mbar_wait(&vfull[w * P + q], (c - 1) & 1)))
+        break;
     }
     __syncwarp();
   } else {
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     for (; j < my_tiles; ++j) {
       const int blk = b0 + warp + C::kWarps * j;
       const int st = warp * P + (j % P);
-      const bool got = mbar_wait(&full[st], (j / P) & 1);
+      const bool got = mbar_wait(&kfull[st], (j / P) & 1);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
         break;
@@ -580,6 +588,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
         for (int c = 0; c < C::kDPL; ++c) {
           mul2(acc2[c][0], al.x);
           mul2(acc2[c][1], al.y);
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], (j / P) & 1))) {
+          if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+          break;
         }
         // ---- P.V: lane owns columns lane*kDPL.., rows paired in each FMA ----
         auto pv_fast = [&](int jj) {
@@ -678,6 +690,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       }
       __syncwarp();
 
+      if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], (j / P) & 1))) {
+        if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+        break;
+      }
       // ---- P.V: lane owns output columns lane*kDPL .. +kDPL-1 ----
       auto pv_key = [&](int jj) {
         const float* pr = p_s + ((warp * kBlock + jj) * R) * 2;
