@@ -227,6 +227,42 @@ def _launches_per_step(splits, meta):
     return n
 
 
+def step_percentiles(run_steps, per_rep, device, reps=60):
+    """p10 / p50 / p90 of the per-step time over individually timed replays of
+    `per_rep` steps each (outside the main timed region)."""
+    import torch
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run_steps(per_rep)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / per_rep)
+    times.sort()
+    pick = lambda q: round(times[min(len(times) - 1, int(q * len(times)))], 6)  # noqa: E731
+    return [pick(0.1), pick(0.5), pick(0.9)]
+
+
+def mixed_roofline(w, hq, hkv, d, esize, ms_step, peaks):
+    """A mixed step is bound by the slower of its two classes: t* = max(KV bytes
+    of the decode-class requests / HBM peak, causal FLOPs of the long requests /
+    bf16 peak); the fraction is t* over the measured step, with each class's
+    rate over the whole step beside it."""
+    dec = [r for r in w.requests if r.scheduled <= 4]
+    pre = [r for r in w.requests if r.scheduled > 4]
+    b = kv_bytes(dec, hkv, d, esize)
+    f = causal_flops(pre, hq, d)
+    t_b = b / (float(peaks["hbm_gbs"]) * 1e9)
+    t_f = f / (float(peaks["bf16_tflops"]) * 1e12)
+    t_star = max(t_b, t_f)
+    return {"t_star_ms": round(t_star * 1e3, 6), "frac": round(t_star / (ms_step / 1e3), 4),
+            "bound": "hbm" if t_b >= t_f else "tensor",
+            "decode_kv_bytes": b, "chunk_flops": f,
+            "decode_gbs_over_step": round(b / 1e9 / (ms_step / 1e3), 1),
+            "chunk_tflops_over_step": round(f / 1e12 / (ms_step / 1e3), 1)}
+
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -324,6 +360,7 @@ def run_gpu(args, rank, world, local_rank):
     if int(flag.item()) != 0:
         raise RuntimeError(f"device error flag {int(flag.item())}")
     ms_step = ms_total / args.steps
+    pct = step_percentiles(run_steps, G if use_graph else 1, device)
     bytes_step = kv_bytes(w.requests, hkv, d, esize)
     flops_step = causal_flops(w.requests, hq, d)
     decode_like = m0["max_query_len"] <= 4
@@ -394,7 +431,10 @@ def run_gpu(args, rank, world, local_rank):
                    "cuda_graph": use_graph, "parallelism": f"replicas x{world}"},
         "roofline": roof, "e2e": e2e,
         "gpu_launches": _launches_per_step(splits, m0) * args.steps,
+        "ms_per_step_p10_p50_p90": pct,
     }
+    if name == "mixed_chunked":
+        result["mixed_roofline"] = mixed_roofline(w, hq, hkv, d, esize, ms_step, peaks)
     if clk is not None:
         result["clocks"] = clk
     return result, w
@@ -524,6 +564,23 @@ def cpu_baseline(name, seconds):
                       f"BLAS threads) over the cache the oracle scatter wrote; scatter untimed"}
 
 
+def cpu_baseline_one_thread(name, seconds):
+    """The same oracle timing with one BLAS/OpenMP thread, in a child process
+    (thread pools are fixed when numpy loads)."""
+    import subprocess
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = (f"import json, bench; r = bench.cpu_baseline({name!r}, {seconds!r}); "
+            f"print(json.dumps({{'value': r['value'], 'unit': r['unit']}}))")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                             text=True, timeout=120 + 4 * seconds)
+        res = json.loads(out.stdout.strip().splitlines()[-1])
+        res["cores"] = 1
+        return res
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError):
+        return None
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -579,6 +636,10 @@ def main(argv=None):
             result["prefill"] = run_secondary_prefill(local_rank)
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+            if args.workload in ("decode_8k", "batched_decode_64"):
+                one = cpu_baseline_one_thread(args.workload, args.cpu_seconds / 2)
+                if one is not None:
+                    result["cpu_baseline"]["one_thread"] = one
         if rank == 0:
             print(json.dumps(result), flush=True)
         return 0
