@@ -27,14 +27,15 @@ __global__ void __launch_bounds__(256) kv_write_kernel(
        i += stride) {
     const int64_t t = i / chunks_per_row;
     const int64_t c = i - t * chunks_per_row;
+    // the row loads do not depend on the slot: all three in flight together
     const int64_t slot = __ldg(slots + t);
+    const uint4 kv = __ldcs(k_new + i);     // read once: streaming
+    const uint4 vv = __ldcs(v_new + i);
     if (slot < 0) continue;                 // padding token: nothing to write
     if (slot >= num_slots) {                // outside the cache: skip, report
       if (c == 0) raise_flag(flag, PKV_FLAG_BAD_SLOT);
       continue;
     }
-    const uint4 kv = __ldcs(k_new + i);     // read once: streaming
-    const uint4 vv = __ldcs(v_new + i);
     k_cache[slot * chunks_per_row + c] = kv;
     v_cache[slot * chunks_per_row + c] = vv;
   }
