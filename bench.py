@@ -360,7 +360,7 @@ def run_gpu(args, rank, world, local_rank):
     if int(flag.item()) != 0:
         raise RuntimeError(f"device error flag {int(flag.item())}")
     ms_step = ms_total / args.steps
-    pct = step_percentiles(run_steps, G if use_graph else 1, device)
+    pct = step_percentiles(run_steps, G if use_graph else 8, device)
     bytes_step = kv_bytes(w.requests, hkv, d, esize)
     flops_step = causal_flops(w.requests, hq, d)
     decode_like = m0["max_query_len"] <= 4

@@ -19,8 +19,10 @@ __global__ void __launch_bounds__(256) kv_write_kernel(
     const int64_t* __restrict__ slots, int64_t num_tokens, uint4* __restrict__ k_cache,
     uint4* __restrict__ v_cache, int64_t num_slots, uint32_t chunks_per_row,
     int32_t* flag) {
+  // Let the next kernel (attention) launch and run its set-up at once: its own
+  // dependency wait still returns only after this grid completes.
+  pdl_launch_dependents();
   pdl_wait_primary();        // inputs and cache are safe to touch only after the predecessor
-  pdl_launch_dependents();   // let the attention kernel launch and set up meanwhile
   const int64_t total = num_tokens * chunks_per_row;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
