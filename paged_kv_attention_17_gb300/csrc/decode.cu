@@ -815,8 +815,10 @@ template <typename T, int D>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   constexpr int kDPL = D / 32;
   __shared__ float red[4][D + 1];
-  pdl_wait_primary();
+  // the next kernel may launch at once; its dependency wait still returns only
+  // after this grid completes
   pdl_launch_dependents();
+  pdl_wait_primary();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = blockIdx.x;
   const int h = static_cast<int>(item % a.hq);
