@@ -209,7 +209,7 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
     return PKV_ERR_INVALID_ARG;
   if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
   const int64_t num_slots = num_blocks * kBlock;
-  if (num_slots > 0xFFFFFFFFll) return PKV_ERR_UNSUPPORTED;
+  if (num_slots > 0x7FFFFFFFll) return PKV_ERR_UNSUPPORTED;   // TMA row coordinates are int32
 
   int splits = num_splits;
   if (splits == 0) {

@@ -29,6 +29,11 @@
 //     kernel finishes) the CTA sets up its barriers, prefetches the tensor
 //     maps and warms L2 with the K/V blocks it will most likely read; every
 //     input it then uses is read after the wait.
+//   * In split launches each consumer warp's first block is loaded right
+//     after the wait from the block id read before it, and kept only if the
+//     metadata and table read after the wait confirm it; otherwise that fill
+//     is discarded (its stage's phases then run one ahead, and the warp is
+//     told so only once the discarded fill has landed).
 //   * Generic path: a warp takes one 16-key block per stage; lanes j and
 //     j + 16 dot the two halves of key j's row against q in shared memory
 //     (each lane's chunk order is rotated by its key, so the reads do not
@@ -130,7 +135,10 @@ struct DecodeSmem {
   static constexpr int kQOff = kRingBytes;
   static constexpr int kPOff = kQOff + R * D * 4;
   static constexpr int kBarOff = kPOff + C::kWarps * kBlock * R * 8;
-  static constexpr int kBytes = kBarOff + 3 * C::kStages * 8;   // kfull[], vfull[], empty[]
+  // kfull[], vfull[], empty[], then per consumer warp the barrier and the
+  // verdict of its speculative first block
+  static constexpr int kSpecOff = kBarOff + 3 * C::kStages * 8;
+  static constexpr int kBytes = kSpecOff + C::kWarps * 8 + C::kWarps * 4;
   static constexpr int kAlloc = kBytes + 1024;            // slack to align the base to 1 KB
 };
 
@@ -199,7 +207,9 @@ __device__ __forceinline__ void load_v_pairs(const uint8_t* vrow, int lane,
   }
 }
 
-template <typename T, int D, int R>
+// SPEC: build with the speculative first blocks (used for split launches of
+// 4-row tiles; unsplit launches run the build without, which measures faster)
+template <typename T, int D, int R, bool SPEC>
 __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
@@ -210,6 +220,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   // decode hot case); every other shape takes the generic path below.
   constexpr bool kFast = sizeof(T) == 2 && R == 4;
   constexpr int kFastChunks = D / 64;                 // 16-byte chunks of q/K per lane
+  // speculative first blocks (below) for the 4-row tiles of split launches,
+  // where each CTA's first block is on the critical path; wider tiles keep
+  // their registers for the generic path
+  constexpr bool kSpec = SPEC && R == 4;
+  // whether this CTA may speculate (same answer on every thread)
+  const bool spec_possible = kSpec && a.num_splits > 1 && blockIdx.y == 0;
   constexpr int kPWarpFloats = kBlock * R * 2;        // p_s floats per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -219,6 +235,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + Sm::kBarOff);   // K of a stage landed
   uint64_t* vfull = kfull + C::kStages;                                 // V of a stage landed
   uint64_t* empty = vfull + C::kStages;                                 // stage released
+  uint64_t* spec_bar = reinterpret_cast<uint64_t*>(smem + Sm::kSpecOff);
+  int* spec_state = reinterpret_cast<int*>(spec_bar + C::kWarps);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = warp == C::kWarps;
@@ -235,12 +253,15 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&kfull[i], 1);
       mbar_init(&vfull[i], 1);
+      if (i < C::kWarps) mbar_init(&spec_bar[i], 1);
       mbar_init(&empty[i], 1);
     }
     fence_mbar_init();
   }
   __syncthreads();
   const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
+  int32_t e_hint = 0;                  // producer lane w: hinted entry of warp w's first block
+  bool hint_ok = false;
   if (producer && z == 0) {
     // ---- L2 warm-up while the previous kernel finishes: the K/V blocks this
     //      CTA will most likely read (the split range a context of
@@ -267,6 +288,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     const int64_t slot_bytes = static_cast<int64_t>(a.hkv) * C::kRowBytes;
     for (int base = sb0; base < sb1; base += 32) {
       const int32_t e = base + lane < sb1 ? __ldcg(table + base + lane) : -1;
+      if (spec_possible && base == sb0 && lane < C::kWarps && base + lane < sb1) {
+        e_hint = e;
+        hint_ok = true;
+      }
       for (int i = 0; i < 32 && base + i < sb1; ++i) {
         const int32_t id = __shfl_sync(0xffffffffu, e, i);
         if (id < 0 || id >= a.num_blocks) continue;
@@ -283,6 +308,32 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   // ---- request geometry (uniform over the CTA); inputs only after the wait ----
   pdl_wait_primary();
   pdl_launch_dependents();
+  // Speculative first block: producer lane w loads warp w's first block of the
+  // hinted split range into the warp's stage 0 at once - the K/V data is read
+  // after the wait, only the block id comes from the hint.  The block is kept
+  // (used) only if the metadata and table read below confirm that block id as
+  // the warp's first; otherwise the stage's first fill is wasted and the
+  // stage's phases shift by one.  An out-of-range hint loads rows -16..-1,
+  // which TMA fills with zeros without reading memory.
+  bool spec_issued = false;
+  if (producer && hint_ok) {
+    uint8_t* ks = smem + (lane * P) * C::kStageBytes;
+    uint8_t* vs = ks + kBlock * C::kRowBytes;
+    const int row = (e_hint >= 0 && e_hint < a.num_blocks) ? e_hint * kBlock : -kBlock;
+    const uint64_t pol0 = l2_policy_evict_first();
+    mbar_arrive_expect_tx(&kfull[lane * P], kBlock * C::kRowBytes);
+    tma_load_3d(ks, &kmap, &kfull[lane * P], 0, g, row, pol0);
+    mbar_arrive_expect_tx(&vfull[lane * P], kBlock * C::kRowBytes);
+    tma_load_3d(vs, &vmap, &vfull[lane * P], 0, g, row, pol0);
+    spec_issued = true;
+  }
+  // every exit from here on first lets a speculative load land (bounded)
+  auto drain_spec = [&]() {
+    if (spec_issued) {
+      mbar_wait(&kfull[lane * P], 0);
+      mbar_wait(&vfull[lane * P], 0);
+    }
+  };
   // The block-table entries of each consumer warp's first two blocks,
   // fetched speculatively (producer lane w for warp w) for the split range a
   // context of max_seq_len keys would give, in flight together with the
@@ -304,25 +355,39 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
   const int n = q1 - q0;
   const int L = __ldg(a.seq_lens + r);
-  if (n == 0) return;
+  if (n == 0) {
+    drain_spec();
+    return;
+  }
   if (n < 0 || q0 < 0 || q1 > a.num_tokens || n > L || n > a.max_query_len) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && z == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
+    drain_spec();
     return;
   }
   const bool decode_class = n <= kDecodeMaxQ;
-  if (!decode_class && !a.long_rows) return;          // the prefill kernel owns it
+  if (!decode_class && !a.long_rows) {                // the prefill kernel owns it
+    drain_spec();
+    return;
+  }
   const bool split_mode = decode_class && a.num_splits > 1;
-  if (!split_mode && s != 0) return;
+  if (!split_mode && s != 0) {
+    drain_spec();
+    return;
+  }
   const int group = a.group;
   const int rows_total = group * n;
   const int rho0 = z * R;
-  if (rho0 >= rows_total) return;
+  if (rho0 >= rows_total) {
+    drain_spec();
+    return;
+  }
   const int nrows = min(R, rows_total - rho0);
   const int i_last = (rho0 + nrows - 1) / group;
   const int kv_len = a.causal ? (L - n + i_last + 1) : L;
   const int nblk = (kv_len + kBlock - 1) / kBlock;
   if (nblk > a.max_blocks_per_seq) {
     if (threadIdx.x == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
+    drain_spec();
     return;
   }
   int b0 = 0, b1 = nblk;
@@ -340,6 +405,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       for (int e = 0; e < C::kDPL; ++e) a.ws_o[w * D + lane * C::kDPL + e] = 0.f;
       if (lane == 0) a.ws_lse[w] = -INFINITY;
     }
+    drain_spec();
     return;
   }
   const int key_end = min(kv_len, b1 * kBlock);       // keys of this split: [b0*16, key_end)
@@ -409,15 +475,40 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       return jj < tiles ? ld_early(table + b0 + w + C::kWarps * jj) : 0;
     };
     const bool spec_ok = spec_b0 == b0;
-    int32_t e_cur = spec_ok && spec_v0 ? spec_e0 : entry_of(0);
-    int32_t e_next = spec_ok && spec_v1 ? spec_e1 : entry_of(1);
-    int jj = 0;
+    // verdict on the speculative first block: 0 none, 1 used as tile 0,
+    // 2 wasted (stage 0's phases then run one ahead of its tiles)
+    const bool used = spec_issued && spec_ok && tiles > 0 && spec_v0 && spec_e0 == e_hint;
+    const int verdict = !spec_issued ? 0 : (used ? 1 : 2);
+    if (verdict == 2) {
+      // a wasted fill lands before the verdict is published (the consumer's
+      // parity waits on stage 0 rely on it), bounded like every wait
+      if (!mbar_wait(&kfull[w * P], 0) || !mbar_wait(&vfull[w * P], 0))
+        raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+    }
+    if (spec_possible && w < C::kWarps) {
+      spec_state[w] = verdict;
+      mbar_arrive(&spec_bar[w]);
+    }
+    if (used && (e_hint < 0 || e_hint >= a.num_blocks)) raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
+    const int shift0 = verdict == 2;
+    int jj = used ? 1 : 0;
+    int32_t e_cur, e_next;
+    if (used) {
+      e_cur = spec_ok && spec_v1 ? spec_e1 : entry_of(1);
+      e_next = entry_of(2);
+    } else {
+      e_cur = spec_ok && spec_v0 ? spec_e0 : entry_of(0);
+      e_next = spec_ok && spec_v1 ? spec_e1 : entry_of(1);
+    }
     unsigned long long t_progress = 0;
     while (__any_sync(0xffffffffu, jj < tiles)) {
       bool ready = false;
       if (jj < tiles) {
         const int st = w * P + jj % P;
         ready = jj < P || mbar_ready(&empty[st], ((jj / P) - 1) & 1);
+        // a wasted speculative fill must land before stage 0 is filled again
+        if (ready && jj == 0 && shift0)
+          ready = mbar_ready(&kfull[st], 0) && mbar_ready(&vfull[st], 0);
         if (ready) {
           int id = e_cur;
           if (id < 0 || id >= a.num_blocks) {
@@ -454,7 +545,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     // every load this lane issued has landed before the merge reuses the ring
     // (a no-op unless a consumer gave up early); bounded like every wait
     for (int q = 0; q < P; ++q) {
-      const int c = jj > q ? (jj - q + P - 1) / P : 0;   // loads issued into stage q
+      const int c = (jj > q ? (jj - q + P - 1) / P : 0) + (q == 0 ? shift0 : 0);  // fills of stage q
       if (c > 0 && (!mbar_wait(&kfull[w * P + q], (c - 1) & 1) ||
                     !mbar_wait(&vfull[w * P + q], (c - 1) & 1)))
         break;
@@ -498,11 +589,23 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       }
       asm volatile("bar.sync 1, %0;" ::"n"(C::kConsumerThreads) : "memory");
     }
+    // the producer's verdict on this warp's speculative first block
+    int shift0 = 0;
+    if (spec_possible && my_tiles > 0) {
+      if (!mbar_wait(&spec_bar[warp], 0)) {
+        if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+      }
+      // "wasted" is published only once that fill (phase 0 of stage 0) has
+      // landed, so stage 0 is then in phase 1 or just past it, and the
+      // parity-1 wait for tile 0 cannot pass early
+      shift0 = spec_state[warp] == 2 ? 1 : 0;
+    }
     int j = 0;
     for (; j < my_tiles; ++j) {
       const int blk = b0 + warp + C::kWarps * j;
       const int st = warp * P + (j % P);
-      const bool got = mbar_wait(&kfull[st], (j / P) & 1);
+      const int ph = (j / P + (j % P == 0 ? shift0 : 0)) & 1;   // phase of this fill
+      const bool got = mbar_wait(&kfull[st], ph);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
         break;
@@ -589,7 +692,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
           mul2(acc2[c][0], al.x);
           mul2(acc2[c][1], al.y);
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], (j / P) & 1))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], ph))) {
           if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
           break;
         }
@@ -690,7 +793,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       }
       __syncwarp();
 
-      if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], (j / P) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], ph))) {
         if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
         break;
       }
@@ -883,7 +986,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
-template <typename T, int D, int R>
+template <typename T, int D, int R, bool SPEC = false>
 static cudaError_t ensure_smem_attr() {
   using Sm = DecodeSmem<T, D, R>;
   static unsigned done = 0;                 // one bit per device already configured
@@ -891,19 +994,19 @@ static cudaError_t ensure_smem_attr() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 32 && ((done >> dev) & 1u)) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_kernel<T, D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Sm::kAlloc);
+  e = cudaFuncSetAttribute(decode_kernel<T, D, R, SPEC>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kAlloc);
   if (e == cudaSuccess && dev < 32) done |= 1u << dev;
   return e;
 }
 
-template <typename T, int D, int R>
+template <typename T, int D, int R, bool SPEC>
 static cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int row_tiles, bool pdl,
                                    cudaStream_t stream) {
   using C = DecodeCfg<T, D, R>;
   using Sm = DecodeSmem<T, D, R>;
-  cudaError_t e = ensure_smem_attr<T, D, R>();
+  cudaError_t e = ensure_smem_attr<T, D, R, SPEC>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(a.hkv * a.num_splits), static_cast<unsigned>(row_tiles),
@@ -916,7 +1019,7 @@ static cudaError_t launch_decode_t(const AttnArgs& a, const CUtensorMap& kmap,
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<T, D, R>, kmap, vmap, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<T, D, R, SPEC>, kmap, vmap, a);
 }
 
 template <typename T, int D>
@@ -924,9 +1027,11 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
                                    const CUtensorMap& vmap, int R, int row_tiles, bool pdl,
                                    cudaStream_t stream) {
   switch (R) {
-    case 4: return launch_decode_t<T, D, 4>(a, kmap, vmap, row_tiles, pdl, stream);
-    case 8: return launch_decode_t<T, D, 8>(a, kmap, vmap, row_tiles, pdl, stream);
-    default: return launch_decode_t<T, D, 16>(a, kmap, vmap, row_tiles, pdl, stream);
+    case 4:
+      return a.num_splits > 1 ? launch_decode_t<T, D, 4, true>(a, kmap, vmap, row_tiles, pdl, stream)
+                              : launch_decode_t<T, D, 4, false>(a, kmap, vmap, row_tiles, pdl, stream);
+    case 8: return launch_decode_t<T, D, 8, false>(a, kmap, vmap, row_tiles, pdl, stream);
+    default: return launch_decode_t<T, D, 16, false>(a, kmap, vmap, row_tiles, pdl, stream);
   }
 }
 
@@ -942,13 +1047,13 @@ int decode_ctas_per_sm(int head_dim) {
       e = ensure_smem_attr<__nv_bfloat16, 128, 4>();
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, decode_kernel<__nv_bfloat16, 128, 4>, DecodeCfg<__nv_bfloat16, 128>::kThreads,
+            &n, decode_kernel<__nv_bfloat16, 128, 4, false>, DecodeCfg<__nv_bfloat16, 128>::kThreads,
             DecodeSmem<__nv_bfloat16, 128, 4>::kAlloc);
     } else {
       e = ensure_smem_attr<__nv_bfloat16, 64, 4>();
       if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, decode_kernel<__nv_bfloat16, 64, 4>, DecodeCfg<__nv_bfloat16, 64>::kThreads,
+            &n, decode_kernel<__nv_bfloat16, 64, 4, false>, DecodeCfg<__nv_bfloat16, 64>::kThreads,
             DecodeSmem<__nv_bfloat16, 64, 4>::kAlloc);
     }
     if (e != cudaSuccess || n < 1) {

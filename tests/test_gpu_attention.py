@@ -158,6 +158,24 @@ def test_split_heuristic_rule():
     assert pkv.pkv_num_splits(64, 1, 4096, 32, 8, 128) == 1
 
 
+@pytest.mark.parametrize("seed", range(3))
+def test_ragged_splits_first_block_speculation(seed):
+    # each split's first blocks are loaded from the pre-launch table reading
+    # for the split range max_seq_len would give, and kept only when the real
+    # metadata confirms them: ragged lengths with several splits make the
+    # ranges of all but the first split differ (the speculative fills wasted)
+    w = workloads.random_small(60 + seed, dtype="bf16", hq=32, hkv=8, d=128, num_seqs=8,
+                               max_ctx=1500)
+    dev = device_inputs(w)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    for s in (2, 3, 5, 9):
+        out, lse, flag = run_step(dev, num_splits=s, write=(s == 2))
+        torch.cuda.synchronize()
+        assert int(flag.item()) == 0
+        _check(out, o_ref, "bf16")
+        _check_lse(lse, lse_ref)
+
+
 def test_block_permutation_is_bit_identical():
     # "paging changes only the access pattern": relocate every physical block
     # and rewrite the tables; with a fixed split count the result is identical
