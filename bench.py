@@ -440,13 +440,66 @@ def run_gpu(args, rank, world, local_rank):
     return result, w
 
 
+def run_e2e_graphs(args, w, reps, common, bytes_step):
+    """Decode steps through the package's CUDA-graph runner: per step the
+    packed inputs (Q, new K/V, metadata) are staged in pinned host memory and
+    one graph replay writes and attends, its kernels reading those inputs and
+    writing the output rows in pinned host memory over the host-device link."""
+    import torch
+
+    from paged_kv_attention_17_gb300.graphs import DecodeGraphRunner
+    m0 = reps[0]["meta"]
+    width = int(reps[0]["block_table"].shape[1])
+    n = w.num_seqs
+    runner = DecodeGraphRunner(common["k_cache"], common["v_cache"], w.num_q_heads,
+                               w.softmax_scale, width, m0["max_seq_len"], max_batch=n)
+    hq = common["q"].cpu()
+    hk, hv = common["k_new"].cpu(), common["v_new"].cpu()
+    packed = [runner.pack(n, hq, hk, hv, r["slot_mapping"].cpu(), r["seq_lens"].cpu(),
+                          r["block_table"].cpu()) for r in reps]
+    steps = []
+
+    def one(i):
+        st = runner.begin(n)
+        runner.stage(st, packed[i % len(packed)])
+        runner.launch(st)
+        steps.append(st)
+
+    k = min(args.steps, 2000)
+    for i in range(min(20, k)):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(k):
+        one(i)
+    e1.record()
+    _, fl = runner.result(steps[-1])
+    torch.cuda.synchronize()
+    if fl != 0:
+        raise RuntimeError(f"device error flag {fl} in the graph runner")
+    ms = e0.elapsed_time(e1) / k
+    b = runner.layouts[runner.sizes[-1]].b
+    h2d = runner.layouts[b].nbytes
+    d2h = b * w.num_q_heads * w.head_dim * common["q"].element_size() + 4
+    return {"value": round((bytes_step / 1e9) / (ms / 1e3), 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
+            "ms_per_step": round(ms, 6),
+            "mode": "CUDA-graph runner: per step the packed inputs are staged in pinned host "
+                    "memory and one replay writes and attends, reading them and writing the "
+                    "output rows in pinned host memory over NVLink-C2C"}
+
+
 def run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, flops_step,
             decode_like):
     """Per step: pinned host -> device copies of the step's inputs (Q, new K/V,
-    metadata), the two API calls, device -> host copy of the output."""
+    metadata), the two API calls, device -> host copy of the output.  Decode
+    steps go through the CUDA-graph runner instead (run_e2e_graphs)."""
     import torch
 
     import paged_kv_attention_17_gb300 as pkv
+    if decode_like and w.num_seqs <= 512:
+        return run_e2e_graphs(args, w, reps, common, bytes_step)
     host = {k: common[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
     hreps = [{k: r[k].cpu().pin_memory() for k in ("qsl", "seq_lens", "block_table", "slot_mapping")}
              for r in reps]

@@ -141,7 +141,9 @@ size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_
  *                     sees no key).
  *   k_cache, v_cache  device [num_blocks, 16, num_kv_heads, head_dim], dtype.
  *   query_start_loc   device int32 [num_seqs + 1], nondecreasing, [0] = 0,
- *                     [num_seqs] = num_tokens.
+ *                     [num_seqs] <= num_tokens (rows of q/out past it, such
+ *                     as a captured graph's padding rows, are neither read
+ *                     nor written).
  *   seq_lens          device int32 [num_seqs].
  *   block_table       device int32 [num_seqs, max_blocks_per_seq].
  *   max_query_len     host: >= every n (bounds the prefill grid).

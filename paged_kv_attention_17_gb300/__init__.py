@@ -6,10 +6,12 @@ compute runs in hand-written CUDA kernels behind the C ABI of
 ``include/pkv.h`` (``_lib/libpkv.so``); this package is its Python binding
 (``pkv_write``, ``pkv_attention_varlen``, ``pkv_num_splits``,
 ``pkv_workspace_bytes``, ``pkv_status_string``) and the runner-side metadata
-builder (``metadata.build``).  PyTorch supplies device memory and streams.
+builder (``metadata.build``), and a decode runner that replays steps from a
+ladder of captured CUDA graphs (``graphs.DecodeGraphRunner``).  PyTorch supplies
+device memory, streams and graph capture.
 """
 
-from . import metadata  # noqa: F401
+from . import graphs, metadata  # noqa: F401
 from ._binding import (EXPORTS, FLAG_BAD_BLOCK, FLAG_BAD_LENGTHS, FLAG_BAD_SLOT,  # noqa: F401
                        FLAG_TIMEOUT, PKV_DECODE_MAX_QLEN, PkvError, lib, pkv_attention_varlen,
                        pkv_attention_varlen_noalloc,
