@@ -24,6 +24,10 @@ Modules, each citing the passage it follows:
   log-sum-exp merge (sections "Never materialise the TxT matrix" and
   "Prefill has a full grid; decode at batch 1 has almost none").
 
+* ``fp8`` - E4M3 codes of an 8-bit KV cache with per-tensor scales (the
+  reading taken for the FP8 KV cache the "Model execution" page names; pinned
+  in ``tests/test_oracle_fp8.py``).
+
 Pins (``tests/test_oracle.py``) tie these to what the pages and mathematics fix:
 the printed flatten example, torch's float64 scaled-dot-product attention on the
 contiguous equivalent, closed forms (uniform weights -> prefix mean, one key ->

@@ -51,8 +51,13 @@ def gather(cache: np.ndarray, table_row, seq_len: int, block_size: int) -> np.nd
 def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, *,
               num_q_heads: int, num_kv_heads: int, softmax_scale: float,
               causal: bool = True, block_size: int = 16, dtype: str = "f32",
-              tokens=None, row_chunk: int = 512):
+              tokens=None, row_chunk: int = 512, kv_dtype: str | None = None,
+              k_scale: float = 1.0, v_scale: float = 1.0):
     """Attention output of the flat batch.
+
+    With ``kv_dtype="e4m3"`` the caches hold 8-bit E4M3 codes and a cached K
+    (V) element is ``k_scale`` (``v_scale``) times the code's value
+    (``oracle.fp8``); q stays in ``dtype``.
 
     Returns ``(o, lse)``: o float64 [N, Hq, D], lse float64 [N, Hq].  With
     ``tokens`` (an iterable of flat-batch indices) only those rows are
@@ -77,8 +82,13 @@ def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, *,
             rows = rows[wanted[start:end]]
         if rows.size == 0:
             continue
-        K = upcast(gather(k_cache, block_table[r], L, block_size), dtype)   # [L, Hkv, D]
-        V = upcast(gather(v_cache, block_table[r], L, block_size), dtype)
+        if kv_dtype == "e4m3":
+            from . import fp8
+            K = k_scale * fp8.decode(gather(k_cache, block_table[r], L, block_size))
+            V = v_scale * fp8.decode(gather(v_cache, block_table[r], L, block_size))
+        else:
+            K = upcast(gather(k_cache, block_table[r], L, block_size), dtype)   # [L, Hkv, D]
+            V = upcast(gather(v_cache, block_table[r], L, block_size), dtype)
         for c0 in range(0, rows.size, row_chunk):
             ri = rows[c0:c0 + row_chunk]
             pos = L - n + ri                                  # position of each row
@@ -107,11 +117,20 @@ def paged_step(workload, tokens=None):
     slot mapping, then attend.  Returns (o, lse, k_cache, v_cache, meta)."""
     from . import flatten as fl
     meta = fl.flatten(workload.requests, workload.block_size)
-    kc = fl.write(workload.k_pool, workload.k_new, meta["slot_mapping"])
-    vc = fl.write(workload.v_pool, workload.v_new, meta["slot_mapping"])
+    kv = getattr(workload, "kv_dtype", None)
+    k_new, v_new = workload.k_new, workload.v_new
+    if kv == "e4m3":
+        # the write stores each new element as the code of value / scale
+        from . import fp8
+        k_new = fp8.quantize(upcast(k_new, workload.dtype).astype(np.float32), workload.k_scale)
+        v_new = fp8.quantize(upcast(v_new, workload.dtype).astype(np.float32), workload.v_scale)
+    kc = fl.write(workload.k_pool, k_new, meta["slot_mapping"])
+    vc = fl.write(workload.v_pool, v_new, meta["slot_mapping"])
     o, lse = attention(workload.q, kc, vc, meta["query_start_loc"], meta["seq_lens"],
                        meta["block_table"], num_q_heads=workload.num_q_heads,
                        num_kv_heads=workload.num_kv_heads,
                        softmax_scale=workload.softmax_scale, causal=workload.causal,
-                       block_size=workload.block_size, dtype=workload.dtype, tokens=tokens)
+                       block_size=workload.block_size, dtype=workload.dtype, tokens=tokens,
+                       kv_dtype=kv, k_scale=getattr(workload, "k_scale", 1.0),
+                       v_scale=getattr(workload, "v_scale", 1.0))
     return o, lse, kc, vc, meta

@@ -57,7 +57,7 @@ class Workload:
     q: np.ndarray                   # [N, Hq, D]  float32 or uint16 (bf16 bits)
     k_new: np.ndarray               # [N, Hkv, D]
     v_new: np.ndarray               # [N, Hkv, D]
-    k_pool: np.ndarray              # [num_blocks, 16, Hkv, D]
+    k_pool: np.ndarray              # [num_blocks, 16, Hkv, D] (uint8 E4M3 codes for kv_dtype e4m3)
     v_pool: np.ndarray              # [num_blocks, 16, Hkv, D]
     softmax_scale: float
     causal: bool = True
@@ -65,6 +65,9 @@ class Workload:
     # Extra schedules with the same shape on disjoint blocks of the same pool
     # (index 0 is ``requests``); used to keep repeated timed steps L2-cold.
     replicas: list[list[Request]] = field(default_factory=list)
+    kv_dtype: str | None = None     # None: caches in `dtype`; "e4m3": 8-bit codes + scales
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def num_tokens(self) -> int:
@@ -89,6 +92,15 @@ def _values(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
     return x if dtype == "f32" else f32_to_bf16_bits(x)
 
 
+def _codes(rng: np.random.Generator, shape) -> np.ndarray:
+    # random 8-bit E4M3 codes: random sign, exponent field 4..8, any mantissa
+    # (magnitudes 1/8 .. 3.75); drawn as bit fields, no rounding involved
+    sign = rng.integers(0, 2, size=shape, dtype=np.uint8)
+    exp = rng.integers(4, 9, size=shape, dtype=np.uint8)
+    man = rng.integers(0, 8, size=shape, dtype=np.uint8)
+    return (sign << 7) | (exp << 3) | man
+
+
 def _blocks_needed(tokens: int, block_size: int) -> int:
     # number of whole blocks that hold `tokens` tokens (pool sizing only)
     return -(-tokens // block_size)
@@ -107,7 +119,8 @@ def _assign(perm: np.ndarray, start: int, shape: list[tuple[int, int]],
 def build(name: str, dtype: str, hq: int, hkv: int, d: int,
           shape: list[tuple[int, int]], seed: int = 0, pool_blocks: int | None = None,
           replicas: int = 1, scale: float | None = None, causal: bool = True,
-          lengths_drawn: bool = False, rng: np.random.Generator | None = None) -> Workload:
+          lengths_drawn: bool = False, rng: np.random.Generator | None = None,
+          kv_dtype: str | None = None, k_scale: float = 1.0, v_scale: float = 1.0) -> Workload:
     """Lay out a workload from a list of (computed, scheduled) pairs.
 
     The pool holds ``replicas`` disjoint copies of the schedule's blocks (or
@@ -123,8 +136,11 @@ def build(name: str, dtype: str, hq: int, hkv: int, d: int,
         reqs, start = _assign(perm, start, shape, BLOCK_SIZE)
         reps.append(reqs)
     n = sum(s for _, s in shape)
-    k_pool = _values(rng, (num_blocks, BLOCK_SIZE, hkv, d), dtype)
-    v_pool = _values(rng, (num_blocks, BLOCK_SIZE, hkv, d), dtype)
+    pool_shape = (num_blocks, BLOCK_SIZE, hkv, d)
+    if kv_dtype == "e4m3":
+        k_pool, v_pool = _codes(rng, pool_shape), _codes(rng, pool_shape)
+    else:
+        k_pool, v_pool = _values(rng, pool_shape, dtype), _values(rng, pool_shape, dtype)
     q = _values(rng, (n, hq, d), dtype)
     k_new = _values(rng, (n, hkv, d), dtype)
     v_new = _values(rng, (n, hkv, d), dtype)
@@ -132,7 +148,8 @@ def build(name: str, dtype: str, hq: int, hkv: int, d: int,
                     num_blocks=num_blocks, requests=reps[0], q=q, k_new=k_new, v_new=v_new,
                     k_pool=k_pool, v_pool=v_pool,
                     softmax_scale=float(scale if scale is not None else 1.0 / np.sqrt(d)),
-                    causal=causal, replicas=reps)
+                    causal=causal, replicas=reps, kv_dtype=kv_dtype, k_scale=float(k_scale),
+                    v_scale=float(v_scale))
 
 
 # ---------------------------------------------------------------------------
