@@ -94,6 +94,32 @@ pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_m
                      int32_t* error_flag, void* stream);
 
 /*
+ * pkv_write_e4m3 - pkv_write into an 8-bit E4M3 cache.
+ *
+ * "Model execution", section "Where it breaks" (an FP8 KV cache is a backend
+ * feature) and "Anatomy of a serving engine", the FP8-cache exercise of its
+ * KV-memory arithmetic: the cache holds one byte per element.  The pages fix
+ * no format; this library reads it as E4M3 (sign, 4 exponent bits with bias
+ * 7, 3 mantissa bits; subnormals m/8 * 2^-6; largest finite 448; no
+ * infinities; S.1111.111 is NaN) with one fp32 scale per cache tensor: a
+ * stored code c stands for scale * value(c).  Element x is stored as the
+ * nearest code (ties to the even mantissa, magnitudes beyond 448 saturate to
+ * 448) of x / scale, the division correctly rounded in fp32.
+ *
+ *   k_new, v_new   device, [num_tokens, num_kv_heads, head_dim], src_dtype
+ *                  (PKV_F32 or PKV_BF16).
+ *   k_cache, v_cache  device uint8 [num_blocks, block_size, num_kv_heads,
+ *                  head_dim].
+ *   k_scale, v_scale  finite, > 0.
+ *   num_kv_heads * head_dim must be a multiple of 16 (else
+ *   PKV_ERR_UNSUPPORTED).  slot_mapping, error_flag and the rest as pkv_write.
+ */
+pkv_status pkv_write_e4m3(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                          int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                          int block_size, int num_kv_heads, int head_dim, pkv_dtype src_dtype,
+                          float k_scale, float v_scale, int32_t* error_flag, void* stream);
+
+/*
  * pkv_num_splits - how many KV splits the decode path should use.
  *
  * "Inside the engine ...", section "Prefill has a full grid; decode at batch 1
@@ -164,6 +190,32 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
                                 float softmax_scale, int causal, int num_splits,
                                 void* workspace, size_t workspace_bytes, int32_t* error_flag,
                                 int64_t num_blocks, pkv_dtype dtype, void* stream);
+
+/*
+ * pkv_attention_varlen_e4m3 - pkv_attention_varlen over an E4M3 cache.
+ *
+ * The cache format of pkv_write_e4m3: key j stands for k_scale * value(code),
+ * value j for v_scale * value(code), so
+ *   out[t, h, :] = v_scale * sum_j softmax_j(softmax_scale * k_scale *
+ *                  q[t,h,:] . value(K code_j)) value(V code_j)
+ * (lse_out: the natural-log log-sum-exp of those scaled scores).  Codes are
+ * widened to fp32 in registers; the arithmetic is that of the bf16 path.
+ *   q, out            device bf16 [num_tokens, num_q_heads, head_dim].
+ *   k_cache, v_cache  device uint8 [num_blocks, 16, num_kv_heads, head_dim].
+ *   k_scale, v_scale  finite, > 0 (else PKV_ERR_INVALID_ARG).
+ * Everything else as pkv_attention_varlen, workspace included.  Requests
+ * with n > PKV_DECODE_MAX_QLEN run on the decode kernel's CUDA-core tiles
+ * (no tensor-core prefill for this format).
+ */
+pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const void* v_cache,
+                                     void* out, float* lse_out, const int32_t* query_start_loc,
+                                     const int32_t* seq_lens, const int32_t* block_table,
+                                     int max_blocks_per_seq, int num_seqs, int64_t num_tokens,
+                                     int max_query_len, int max_seq_len, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     float softmax_scale, float k_scale, float v_scale, int causal,
+                                     int num_splits, void* workspace, size_t workspace_bytes,
+                                     int32_t* error_flag, int64_t num_blocks, void* stream);
 
 /*
  * pkv_attention_varlen_noalloc - pkv_attention_varlen without a caller

@@ -22,8 +22,9 @@ PKV_DECODE_MAX_QLEN = 4
 FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/pkv.h declares.
-EXPORTS = ("pkv_write", "pkv_num_splits", "pkv_workspace_bytes", "pkv_attention_varlen",
-           "pkv_attention_varlen_noalloc", "pkv_status_string")
+EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_num_splits", "pkv_workspace_bytes",
+           "pkv_attention_varlen", "pkv_attention_varlen_e4m3", "pkv_attention_varlen_noalloc",
+           "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -43,6 +44,10 @@ def lib() -> ctypes.CDLL:
         vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
         L.pkv_write.argtypes = [vp, vp, vp, i64, vp, vp, i64, i32, i32, i32, i32, vp, vp]
         L.pkv_write.restype = i32
+        f32 = ctypes.c_float
+        L.pkv_write_e4m3.argtypes = [vp, vp, vp, i64, vp, vp, i64, i32, i32, i32, i32, f32, f32,
+                                     vp, vp]
+        L.pkv_write_e4m3.restype = i32
         L.pkv_num_splits.argtypes = [i32] * 7
         L.pkv_num_splits.restype = i32
         L.pkv_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -51,6 +56,10 @@ def lib() -> ctypes.CDLL:
                                            i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, sz,
                                            vp, i64, i32, vp]
         L.pkv_attention_varlen.restype = i32
+        L.pkv_attention_varlen_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
+                                                i32, i32, i32, i32, i32, f32, f32, f32, i32, i32,
+                                                vp, sz, vp, i64, vp]
+        L.pkv_attention_varlen_e4m3.restype = i32
         L.pkv_attention_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
                                                    i32, i32, i32, i32, i32, i32, ctypes.c_float,
                                                    i32, i32, vp, i64, i32, vp]
@@ -100,6 +109,20 @@ def pkv_write(k_new, v_new, slot_mapping, k_cache, v_cache, error_flag=None, str
     _check("pkv_write", code)
 
 
+def pkv_write_e4m3(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                   error_flag=None, stream=None):
+    """pkv_write into uint8 caches of E4M3 codes: slot slot_mapping[t] gets the
+    codes of k_new[t] / k_scale and v_new[t] / v_scale (inputs fp32 or bf16)."""
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 caches are uint8 tensors of codes")
+    nb, bs, hkv, d = k_cache.shape
+    code = lib().pkv_write_e4m3(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                int(slot_mapping.numel()), _ptr(k_cache), _ptr(v_cache), int(nb),
+                                int(bs), int(hkv), int(d), _dtype_code(k_new.dtype),
+                                float(k_scale), float(v_scale), _ptr(error_flag), _stream(stream))
+    _check("pkv_write_e4m3", code)
+
+
 def pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
                    device=None) -> int:
     dev = torch.cuda.current_device() if device is None else int(device)
@@ -139,6 +162,37 @@ def pkv_attention_varlen(q, k_cache, v_cache, out, query_start_loc, seq_lens, bl
         float(softmax_scale), 1 if causal else 0, splits, _ptr(workspace), int(ws_bytes),
         _ptr(error_flag), int(nb), _dtype_code(q.dtype), _stream(stream))
     _check("pkv_attention_varlen", code)
+    return out
+
+
+def pkv_attention_varlen_e4m3(q, k_cache, v_cache, out, query_start_loc, seq_lens, block_table,
+                              max_query_len, max_seq_len, softmax_scale, k_scale, v_scale,
+                              causal=True, num_splits=0, workspace=None, lse_out=None,
+                              error_flag=None, stream=None):
+    """pkv_attention_varlen over uint8 caches of E4M3 codes (key code c stands
+    for k_scale * value(c), value code c for v_scale * value(c)); q and out
+    are bf16.  Workspace handling as pkv_attention_varlen."""
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 caches are uint8 tensors of codes")
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("q and out are bf16 for E4M3 caches")
+    n_tok, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    num_seqs = int(seq_lens.numel())
+    splits = int(num_splits)
+    if splits == 0 and num_seqs > 0:
+        splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, hq, hkv, d, q.device.index)
+    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().pkv_attention_varlen_e4m3(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
+        _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]), num_seqs, int(n_tok),
+        int(max_query_len), int(max_seq_len), int(hq), int(hkv), int(d), int(bs),
+        float(softmax_scale), float(k_scale), float(v_scale), 1 if causal else 0, splits,
+        _ptr(workspace), int(ws_bytes), _ptr(error_flag), int(nb), _stream(stream))
+    _check("pkv_attention_varlen_e4m3", code)
     return out
 
 

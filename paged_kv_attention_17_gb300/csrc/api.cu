@@ -12,9 +12,14 @@ namespace pkv {
 cudaError_t launch_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
                             int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_slots,
                             uint32_t row_bytes, int32_t* flag, int num_sms, cudaStream_t stream);
+cudaError_t launch_kv_write_e4m3(const void* k_new, const void* v_new, bool src_bf16,
+                                 const int64_t* slots, int64_t num_tokens, void* k_cache,
+                                 void* v_cache, int64_t num_slots, uint32_t row_elems,
+                                 float k_scale, float v_scale, int32_t* flag, int num_sms,
+                                 cudaStream_t stream);
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          bool bf16, int head_dim, bool pdl, cudaStream_t stream);
-cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStream_t stream);
+                          ElemType et, int head_dim, bool pdl, cudaStream_t stream);
+cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStream_t stream);
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
 int decode_ctas_per_sm(int head_dim);
 bool prefill_supported(int head_dim, bool bf16, int group);
@@ -75,17 +80,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // head: the whole row unswizzled (decode kernel), or a 128-byte slice of it
 // with the 128B swizzle (prefill tensor-core operands).
 bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_slots, int hkv, int d,
-                      bool bf16, bool swizzle128) {
+                      ElemType et, bool swizzle128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t es = bf16 ? 2 : 4;
+  const cuuint64_t es = et == ElemType::kF32 ? 4 : (et == ElemType::kBf16 ? 2 : 1);
+  const CUtensorMapDataType dt = et == ElemType::kF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : et == ElemType::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
                         static_cast<cuuint64_t>(num_slots)};
   cuuint64_t strides[2] = {d * es, static_cast<cuuint64_t>(hkv) * d * es};
   const cuuint32_t inner = swizzle128 ? static_cast<cuuint32_t>(128 / es) : static_cast<cuuint32_t>(d);
   cuuint32_t box[3] = {inner, 1, static_cast<cuuint32_t>(kBlock)};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+  CUresult r = fn(map, dt, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -109,6 +117,112 @@ bool encode_q_map(CUtensorMap* map, const void* q, int64_t num_tokens, int hq, i
 }
 
 bool valid_dtype(pkv_dtype dt) { return dt == PKV_F32 || dt == PKV_BF16; }
+
+bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
+
+static pkv_status attention(const void* q, const void* k_cache, const void* v_cache, void* out,
+                            float* lse_out, const int32_t* query_start_loc,
+                            const int32_t* seq_lens, const int32_t* block_table,
+                            int max_blocks_per_seq, int num_seqs, int64_t num_tokens,
+                            int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+                            int head_dim, int block_size, float softmax_scale, float k_scale,
+                            float v_scale, int causal, int num_splits, void* workspace,
+                            size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+                            ElemType et, void* stream) {
+  // ---- host-checkable arguments ----
+  if (num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
+      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_splits < 0 ||
+      num_splits > kMaxSplits || num_blocks < 1 || max_seq_len < 0 || max_query_len < 0 ||
+      !std::isfinite(softmax_scale))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlock || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
+  if (max_query_len < 1 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !out || !query_start_loc || !seq_lens || !block_table)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(query_start_loc, 4) || !aligned(seq_lens, 4) || !aligned(block_table, 4) ||
+      (lse_out && !aligned(lse_out, 4)) || (error_flag && !aligned(error_flag, 4)))
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  const int64_t num_slots = num_blocks * kBlock;
+  if (num_slots > 0x7FFFFFFFll) return PKV_ERR_UNSUPPORTED;   // TMA row coordinates are int32
+
+  int splits = num_splits;
+  if (splits == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
+                            head_dim, dev);
+  }
+  if (splits < 1) return PKV_ERR_CUDA;
+  const size_t need = pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return PKV_ERR_WORKSPACE;
+
+  const bool bf16 = et == ElemType::kBf16;
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.out = out;
+  a.lse_out = lse_out;
+  a.qsl = query_start_loc;
+  a.seq_lens = seq_lens;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.max_query_len = max_query_len;
+  a.max_seq_len = max_seq_len;
+  a.hq = num_q_heads;
+  a.hkv = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.scale_log2 = softmax_scale * k_scale * kLog2e;
+  a.v_scale = v_scale;
+  a.causal = causal ? 1 : 0;
+  a.num_splits = splits;
+  // the tensor-core softmax takes the row max before scaling: positive scales only
+  const bool tc_prefill =
+      prefill_supported(head_dim, bf16, num_q_heads / num_kv_heads) && softmax_scale > 0.f;
+  // E4M3 caches: decode rows take the register-q tiles, longer requests the
+  // CUDA-core tiles of the same kernel
+  a.long_rows = tc_prefill ? 0 : (et == ElemType::kE4m3 ? (max_query_len > kDecodeMaxQ) : 1);
+  if (need > 0) {
+    const size_t rows = static_cast<size_t>(splits) * num_seqs * kDecodeMaxQ * num_q_heads;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        align256(rows * head_dim * sizeof(float)));
+  }
+  a.flag = error_flag;
+  a.num_blocks = num_blocks;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+
+  CUtensorMap kmap, vmap;
+  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, false) ||
+      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, false))
+    return PKV_ERR_CUDA;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(a, kmap, vmap, et, head_dim, /*pdl=*/true, st);
+  if (e == cudaSuccess && splits > 1) e = launch_combine(a, et, head_dim, st);
+  if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ) {
+    CUtensorMap qmap, kmap_sw, vmap_sw;
+    if (num_tokens > 0x7FFFFFFFll || !encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim) ||
+        !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
+        !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
+      return PKV_ERR_CUDA;
+    e = launch_prefill(a, qmap, kmap_sw, vmap_sw, st);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
 
 }  // namespace
 
@@ -146,6 +260,30 @@ pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_m
   cudaError_t e = launch_kv_write(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache,
                                   num_blocks * kBlock, static_cast<uint32_t>(row_bytes), error_flag,
                                   sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_write_e4m3(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                          int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
+                          int block_size, int num_kv_heads, int head_dim, pkv_dtype src_dtype,
+                          float k_scale, float v_scale, int32_t* error_flag, void* stream) {
+  if (num_tokens < 0 || num_blocks < 1 || num_kv_heads < 1 || head_dim < 1 ||
+      !valid_dtype(src_dtype) || !valid_scale(k_scale) || !valid_scale(v_scale))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlock) return PKV_ERR_UNSUPPORTED;
+  const int64_t row_elems = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (row_elems % 16 != 0 || row_elems > 0x7FFFFFFFll) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8) || (error_flag && !aligned(error_flag, 4)))
+    return PKV_ERR_INVALID_ARG;
+  const int sms = current_sms();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  cudaError_t e = launch_kv_write_e4m3(k_new, v_new, src_dtype == PKV_BF16, slot_mapping,
+                                       num_tokens, k_cache, v_cache, num_blocks * kBlock,
+                                       static_cast<uint32_t>(row_elems), k_scale, v_scale,
+                                       error_flag, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -192,96 +330,29 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
                                 float softmax_scale, int causal, int num_splits, void* workspace,
                                 size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
                                 pkv_dtype dtype, void* stream) {
-  // ---- host-checkable arguments ----
-  if (!valid_dtype(dtype) || num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
-      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_splits < 0 ||
-      num_splits > kMaxSplits || num_blocks < 1 || max_seq_len < 0 || max_query_len < 0 ||
-      !std::isfinite(softmax_scale))
-    return PKV_ERR_INVALID_ARG;
-  if (block_size != kBlock || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
-  if (max_query_len < 1 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
-  if (!q || !k_cache || !v_cache || !out || !query_start_loc || !seq_lens || !block_table)
-    return PKV_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(query_start_loc, 4) || !aligned(seq_lens, 4) || !aligned(block_table, 4) ||
-      (lse_out && !aligned(lse_out, 4)) || (error_flag && !aligned(error_flag, 4)))
-    return PKV_ERR_INVALID_ARG;
-  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
-  const int64_t num_slots = num_blocks * kBlock;
-  if (num_slots > 0x7FFFFFFFll) return PKV_ERR_UNSUPPORTED;   // TMA row coordinates are int32
+  if (!valid_dtype(dtype)) return PKV_ERR_INVALID_ARG;
+  return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                   max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                   num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, 1.f, 1.f,
+                   causal, num_splits, workspace, workspace_bytes, error_flag, num_blocks,
+                   dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32, stream);
+}
 
-  int splits = num_splits;
-  if (splits == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-      cudaGetLastError();
-      return PKV_ERR_CUDA;
-    }
-    splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
-                            head_dim, dev);
-  }
-  if (splits < 1) return PKV_ERR_CUDA;
-  const size_t need = pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
-  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
-    return PKV_ERR_WORKSPACE;
-
-  const bool bf16 = dtype == PKV_BF16;
-  AttnArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.q = q;
-  a.out = out;
-  a.lse_out = lse_out;
-  a.qsl = query_start_loc;
-  a.seq_lens = seq_lens;
-  a.block_table = block_table;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_seqs = num_seqs;
-  a.num_tokens = num_tokens;
-  a.max_query_len = max_query_len;
-  a.max_seq_len = max_seq_len;
-  a.hq = num_q_heads;
-  a.hkv = num_kv_heads;
-  a.group = num_q_heads / num_kv_heads;
-  a.scale_log2 = softmax_scale * kLog2e;
-  a.causal = causal ? 1 : 0;
-  a.num_splits = splits;
-  // the tensor-core softmax takes the row max before scaling: positive scales only
-  const bool tc_prefill =
-      prefill_supported(head_dim, bf16, num_q_heads / num_kv_heads) && softmax_scale > 0.f;
-  a.long_rows = tc_prefill ? 0 : 1;
-  if (need > 0) {
-    const size_t rows = static_cast<size_t>(splits) * num_seqs * kDecodeMaxQ * num_q_heads;
-    a.ws_o = static_cast<float*>(workspace);
-    a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        align256(rows * head_dim * sizeof(float)));
-  }
-  a.flag = error_flag;
-  a.num_blocks = num_blocks;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-
-  CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, bf16, false) ||
-      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, bf16, false))
-    return PKV_ERR_CUDA;
-
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(a, kmap, vmap, bf16, head_dim, /*pdl=*/true, st);
-  if (e == cudaSuccess && splits > 1) e = launch_combine(a, bf16, head_dim, st);
-  if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ) {
-    CUtensorMap qmap, kmap_sw, vmap_sw;
-    if (num_tokens > 0x7FFFFFFFll || !encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim) ||
-        !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, bf16, true) ||
-        !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, bf16, true))
-      return PKV_ERR_CUDA;
-    e = launch_prefill(a, qmap, kmap_sw, vmap_sw, st);
-  }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return PKV_ERR_CUDA;
-  }
-  return PKV_OK;
+pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const void* v_cache,
+                                     void* out, float* lse_out, const int32_t* query_start_loc,
+                                     const int32_t* seq_lens, const int32_t* block_table,
+                                     int max_blocks_per_seq, int num_seqs, int64_t num_tokens,
+                                     int max_query_len, int max_seq_len, int num_q_heads,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     float softmax_scale, float k_scale, float v_scale, int causal,
+                                     int num_splits, void* workspace, size_t workspace_bytes,
+                                     int32_t* error_flag, int64_t num_blocks, void* stream) {
+  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_INVALID_ARG;
+  return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                   max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                   num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, k_scale,
+                   v_scale, causal, num_splits, workspace, workspace_bytes, error_flag,
+                   num_blocks, ElemType::kE4m3, stream);
 }
 
 }  // extern "C"

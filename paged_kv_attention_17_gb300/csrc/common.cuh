@@ -12,6 +12,14 @@
 
 namespace pkv {
 
+// One 8-bit E4M3 code of an FP8 KV cache (the value is decoded in registers).
+struct e4m3_t {
+  uint8_t bits;
+};
+
+// Cache element type of a launch.
+enum class ElemType { kF32, kBf16, kE4m3 };
+
 constexpr int kBlock = 16;                       // tokens per KV-cache block
 constexpr int kDecodeMaxQ = PKV_DECODE_MAX_QLEN; // decode-class bound on q_len
 constexpr int kMaxSplits = 64;
@@ -35,7 +43,8 @@ struct AttnArgs {
   int max_query_len;
   int max_seq_len;        // host bound on seq_lens (speculative table prefetch)
   int hq, hkv, group;
-  float scale_log2;       // softmax_scale * log2(e): scores live in the log2 domain
+  float scale_log2;       // softmax_scale * log2(e) (* k_scale for E4M3 caches): log2-domain scores
+  float v_scale;          // output multiplier: v_scale for E4M3 caches, else 1
   int causal;
   int num_splits;         // >= 1
   int long_rows;          // decode kernel also runs requests with q_len > kDecodeMaxQ
@@ -67,6 +76,32 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 // bf16 pair (packed in a 32-bit word, element 0 in the low half) -> two floats
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two E4M3 codes (element 0 in the low byte of the 16-bit value) -> two
+// floats, through the hardware E4M3x2 -> f16x2 conversion (exact: every E4M3
+// value is an f16 value).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "r"(two_codes));
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  return make_float2(lo, hi);
+}
+
+// Two floats -> two E4M3 codes (a in the low byte): round to nearest even,
+// magnitudes beyond 448 saturate to 448, NaN stays NaN.
+__device__ __forceinline__ uint32_t float2_to_e4m3x2(float a, float b) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tcvt.u32.u16 %0, c;\n\t}"
+      : "=r"(r)
+      : "f"(b), "f"(a));
+  return r;
+}
 
 // ---------------------------------------------------------------------------
 // mbarrier (shared memory, CTA scope)

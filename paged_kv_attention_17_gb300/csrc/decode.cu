@@ -48,9 +48,24 @@
 //   * Each warp keeps its own (m, l, acc); the warps are merged through shared
 //     memory at the end (same algebra as the split merge).
 //   * Bounded mbarrier waits: a stuck pipeline sets PKV_FLAG_TIMEOUT and exits.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace pkv {
+
+// Element type of the cache (float, bf16 or an E4M3 code) and of q / out
+// (the same, except bf16 for E4M3 caches).
+template <typename T>
+constexpr bool kIsE4m3 = std::is_same<T, e4m3_t>::value;
+template <typename T>
+struct QType {
+  using type = T;
+};
+template <>
+struct QType<e4m3_t> {
+  using type = __nv_bfloat16;
+};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -142,13 +157,13 @@ struct DecodeSmem {
   static constexpr int kAlloc = kBytes + 1024;            // slack to align the base to 1 KB
 };
 
-// Position of q element (row, d) in shared memory.  fp32: plain rows.  bf16: a
-// 16-byte key chunk holds 8 elements whose fp32 q counterparts (32 bytes) are
-// stored as two 16-byte halves in separate regions, so the rotated chunk reads
-// of 8 lanes hit 8 distinct bank groups.
+// Position of q element (row, d) in shared memory.  fp32 and E4M3 caches:
+// plain rows.  bf16: a 16-byte key chunk holds 8 elements whose fp32 q
+// counterparts (32 bytes) are stored as two 16-byte halves in separate
+// regions, so the rotated chunk reads of 8 lanes hit 8 distinct bank groups.
 template <typename T, int D>
 __device__ __forceinline__ int q_index(int row, int d) {
-  if constexpr (sizeof(T) == 4) {
+  if constexpr (sizeof(T) == 4 || kIsE4m3<T>) {
     return row * D + d;
   } else {
     const int c = d >> 3, w = d & 7;
@@ -196,6 +211,16 @@ __device__ __forceinline__ void load_v_pairs(const uint8_t* vrow, int lane,
       v[0] = t.x;
       v[1] = t.y;
     }
+  } else if constexpr (kIsE4m3<T>) {
+    if constexpr (C::kPairs == 1) {
+      const float2 f = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vrow + lane * 2));
+      v[0] = pack2(f.x, f.y);
+    } else {
+      const uint32_t c4 = *reinterpret_cast<const uint32_t*>(vrow + lane * 4);
+      const float2 f0 = e4m3x2_to_float2(c4 & 0xffffu), f1 = e4m3x2_to_float2(c4 >> 16);
+      v[0] = pack2(f0.x, f0.y);
+      v[1] = pack2(f1.x, f1.y);
+    }
   } else {
     if constexpr (C::kPairs == 1) {
       v[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(vrow + lane * 4));
@@ -218,8 +243,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   constexpr int P = C::kStagesPerWarp;
   // Register-q path for one token of a 4-query-head GQA group in bf16 (the
   // decode hot case); every other shape takes the generic path below.
-  constexpr bool kFast = sizeof(T) == 2 && R == 4;
-  constexpr int kFastChunks = D / 64;                 // 16-byte chunks of q/K per lane
+  using QT = typename QType<T>::type;                  // q / out element type
+  constexpr bool kFast = (sizeof(T) == 2 || kIsE4m3<T>) && R == 4;
+  constexpr int kFastChunks = D / 64;                 // 16-byte q chunks per row and lane
   // speculative first blocks (below) for the 4-row tiles of split launches,
   // where each CTA's first block is on the critical path; wider tiles keep
   // their registers for the generic path
@@ -415,7 +441,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   // q elements this thread stages (generic path), loaded before the causal
   // limits are worked out so the loads are in flight meanwhile
   constexpr int kQPer = kFast ? 1 : (R * D + C::kConsumerThreads - 1) / C::kConsumerThreads;
-  T qraw[kQPer];
+  QT qraw[kQPer];
   if constexpr (!kFast) {
 #pragma unroll
     for (int u = 0; u < kQPer; ++u) {
@@ -425,9 +451,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
         const int rr = rho0 + rho;
         const int64_t t = q0 + rr / group;
         const int h = g * group + rr % group;
-        qraw[u] = static_cast<const T*>(a.q)[(t * a.hq + h) * D + d];
+        qraw[u] = static_cast<const QT*>(a.q)[(t * a.hq + h) * D + d];
       } else {
-        qraw[u] = T(0.f);
+        qraw[u] = QT(0.f);
       }
     }
   }
@@ -564,7 +590,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < kFastChunks; ++cc)
           qv[r4][cc] = r4 < nrows ? __ldg(reinterpret_cast<const uint4*>(
-                                        static_cast<const T*>(a.q) + qrow + 8 * (dc + 8 * cc)))
+                                        static_cast<const QT*>(a.q) + qrow +
+                                        (kIsE4m3<T> ? (D / 8) * dc + 8 * cc : 8 * (dc + 8 * cc))))
                                   : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
@@ -626,6 +653,28 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
         for (int t = 0; t < 4; ++t) {
           const int key = kg * 4 + t;
           const uint8_t* krow = ks + key * C::kRowBytes;
+          if constexpr (kIsE4m3<T>) {
+            // this lane's D/8 consecutive codes of the key (16 or 8 bytes)
+            uint32_t w[D / 32];
+            if constexpr (D == 128) {
+              const uint4 kc = *reinterpret_cast<const uint4*>(krow + dc * 16);
+              w[0] = kc.x; w[1] = kc.y; w[2] = kc.z; w[3] = kc.w;
+            } else {
+              const uint2 kc = *reinterpret_cast<const uint2*>(krow + dc * 8);
+              w[0] = kc.x; w[1] = kc.y;
+            }
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+              const float2 f0 = e4m3x2_to_float2(w[i] & 0xffffu);
+              const float2 f1 = e4m3x2_to_float2(w[i] >> 16);
+              const f32x2 ka = pack2(f0.x, f0.y), kb = pack2(f1.x, f1.y);
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                fma2(part[t][r], qr[r][2 * i], ka);
+                fma2(part[t][r], qr[r][2 * i + 1], kb);
+              }
+            }
+          } else {
 #pragma unroll
           for (int cc = 0; cc < kFastChunks; ++cc) {
             const int chunk = dc + 8 * cc;
@@ -639,6 +688,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
               fma2(part[t][r], qr[r][cc * 4 + 2], k45);
               fma2(part[t][r], qr[r][cc * 4 + 3], k67);
             }
+          }
           }
         }
         // ---- transpose-reduce over the 8 slice lanes (xor 4, 2, 1): values
@@ -737,6 +787,27 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
             const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 4);
             fma2(sc2[rho], qa.x, k01);
             fma2(sc2[rho], qa.y, k23);
+          }
+        } else if constexpr (kIsE4m3<T>) {
+          // 16 codes = dims 16 chunk .. 16 chunk + 15
+          const uint32_t w[4] = {kc.x, kc.y, kc.z, kc.w};
+          f32x2 kp[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f0 = e4m3x2_to_float2(w[i] & 0xffffu);
+            const float2 f1 = e4m3x2_to_float2(w[i] >> 16);
+            kp[2 * i] = pack2(f0.x, f0.y);
+            kp[2 * i + 1] = pack2(f1.x, f1.y);
+          }
+#pragma unroll
+          for (int rho = 0; rho < R; ++rho) {
+            const ulonglong2* qp = reinterpret_cast<const ulonglong2*>(q_s + rho * D + chunk * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const ulonglong2 qq = qp[i];
+              fma2(sc2[rho], qq.x, kp[2 * i]);
+              fma2(sc2[rho], qq.y, kp[2 * i + 1]);
+            }
           }
         } else {
           const f32x2 k01 = bf16x2_to_f32x2(kc.x), k23 = bf16x2_to_f32x2(kc.y);
@@ -884,7 +955,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
           o[e] = fmaf(f, aw[(w * R + rho) * D + lane * C::kDPL + e], o[e]);
       }
     }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const float inv = lsum > 0.f ? a.v_scale / lsum : 0.f;   // v_scale: E4M3 caches
     const float lse2 = lsum > 0.f ? M + lg2(lsum) : -INFINITY;
     const int rr = rho0 + rho;
     const int i = rr / group;
@@ -898,7 +969,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       const int64_t t = q0 + i;
 #pragma unroll
       for (int e = 0; e < C::kDPL; ++e)
-        store_elem<T>(a.out, (t * a.hq + h) * D + lane * C::kDPL + e, o[e] * inv);
+        store_elem<QT>(a.out, (t * a.hq + h) * D + lane * C::kDPL + e, o[e] * inv);
       if (a.lse_out != nullptr && lane == 0) a.lse_out[t * a.hq + h] = lse2 * kLn2;
     }
   }
@@ -1076,20 +1147,25 @@ int decode_rows_per_tile(int group, int max_query_len, bool long_rows) {
 }
 
 cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          bool bf16, int head_dim, bool pdl, cudaStream_t stream) {
+                          ElemType et, int head_dim, bool pdl, cudaStream_t stream) {
   const int R = decode_rows_per_tile(a.group, a.max_query_len, a.long_rows != 0);
   const int qmax = a.long_rows ? a.max_query_len : min(a.max_query_len, kDecodeMaxQ);
   const int row_tiles = (a.group * (qmax < 1 ? 1 : qmax) + R - 1) / R;
   if (row_tiles > 65535 || a.num_seqs > 65535) return cudaErrorInvalidConfiguration;
-  if (bf16) {
+  if (et == ElemType::kBf16) {
     return head_dim == 128 ? launch_decode_d<__nv_bfloat16, 128>(a, kmap, vmap, R, row_tiles, pdl, stream)
                            : launch_decode_d<__nv_bfloat16, 64>(a, kmap, vmap, R, row_tiles, pdl, stream);
+  }
+  if (et == ElemType::kE4m3) {
+    return head_dim == 128 ? launch_decode_d<e4m3_t, 128>(a, kmap, vmap, R, row_tiles, pdl, stream)
+                           : launch_decode_d<e4m3_t, 64>(a, kmap, vmap, R, row_tiles, pdl, stream);
   }
   return head_dim == 128 ? launch_decode_d<float, 128>(a, kmap, vmap, R, row_tiles, pdl, stream)
                          : launch_decode_d<float, 64>(a, kmap, vmap, R, row_tiles, pdl, stream);
 }
 
-cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStream_t stream) {
+// The combine writes out in the query's type: bf16 for bf16 and E4M3 caches.
+cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(a.num_seqs) * combine_rows(a.max_query_len) * a.hq;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(items));
@@ -1100,7 +1176,7 @@ cudaError_t launch_combine(const AttnArgs& a, bool bf16, int head_dim, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (bf16) {
+  if (et != ElemType::kF32) {
     return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128>, a)
                            : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64>, a);
   }

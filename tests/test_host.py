@@ -32,7 +32,7 @@ def pkv():
 def _header_functions():
     src = open(os.path.join(ROOT, "include", "pkv.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_header_symbol(pkv):
@@ -134,6 +134,51 @@ def test_write_host_validation(pkv):
     assert L.pkv_write(None, vp(16), vp(16), 3, vp(16), vp(16), 4, 16, 8, 128, 1, None, None) == 1
     assert L.pkv_write(vp(16), vp(16), vp(16), -1, vp(16), vp(16), 4, 16, 8, 128, 1, None, None) == 1
     assert L.pkv_write(vp(18), vp(16), vp(16), 3, vp(16), vp(16), 4, 16, 8, 128, 1, None, None) == 1
+
+
+def _attn_e4m3_call(pkv, **over):
+    L = pkv.lib()
+    args = dict(q=16, k=16, v=16, out=16, lse=0, qsl=16, sl=16, bt=16, mbps=4, num_seqs=2,
+                num_tokens=5, max_q=4, max_s=40, hq=8, hkv=2, d=128, bs=16, scale=0.1, ks=0.5,
+                vs=0.25, causal=1, splits=1, ws=0, ws_bytes=0, flag=0, num_blocks=10, stream=0)
+    args.update(over)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.pkv_attention_varlen_e4m3(
+        vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["out"]), vp(args["lse"]),
+        vp(args["qsl"]), vp(args["sl"]), vp(args["bt"]), args["mbps"], args["num_seqs"],
+        args["num_tokens"], args["max_q"], args["max_s"], args["hq"], args["hkv"], args["d"],
+        args["bs"], args["scale"], args["ks"], args["vs"], args["causal"], args["splits"],
+        vp(args["ws"]), args["ws_bytes"], vp(args["flag"]), args["num_blocks"], vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(ks=0.0), 1),                 # scales must be finite and positive
+    (dict(vs=-1.0), 1),
+    (dict(ks=float("inf")), 1),
+    (dict(vs=float("nan")), 1),
+    (dict(d=96), 2),
+    (dict(q=24), 1),
+    (dict(splits=4), 3),
+    (dict(num_tokens=0), 0),
+])
+def test_attention_e4m3_host_validation(pkv, over, code):
+    assert _attn_e4m3_call(pkv, **over) == code
+
+
+def test_write_e4m3_host_validation(pkv):
+    L = pkv.lib()
+    vp = ctypes.c_void_p
+    ok = (4, 16, 8, 128, 1, 1.0, 1.0, None, None)
+    assert L.pkv_write_e4m3(None, None, None, 0, None, None, *ok) == 0
+    assert L.pkv_write_e4m3(vp(16), vp(16), vp(16), 3, vp(16), vp(16),
+                            4, 16, 8, 128, 1, 0.0, 1.0, None, None) == 1
+    assert L.pkv_write_e4m3(vp(16), vp(16), vp(16), 3, vp(16), vp(16),
+                            4, 16, 8, 128, 1, 1.0, float("nan"), None, None) == 1
+    assert L.pkv_write_e4m3(vp(16), vp(16), vp(16), 3, vp(16), vp(16),
+                            4, 16, 8, 128, 5, 1.0, 1.0, None, None) == 1      # source dtype
+    assert L.pkv_write_e4m3(vp(16), vp(16), vp(16), 3, vp(16), vp(16),
+                            4, 16, 1, 8, 1, 1.0, 1.0, None, None) == 2        # row of 8 codes
+    assert L.pkv_write_e4m3(vp(16), vp(16), vp(16), 3, vp(16), vp(24), *ok) == 1
 
 
 def test_num_splits_rejects_bad_args(pkv):

@@ -194,6 +194,15 @@ def prefill_8k(seed: int = 0, replicas: int = 1) -> Workload:
     return build("prefill_8k", "bf16", 32, 8, 128, [(0, 8192)], seed=seed, replicas=replicas)
 
 
+def decode_8k_e4m3(seed: int = 0, replicas: int = 1) -> Workload:
+    """decode_8k over an 8-bit E4M3 cache (codes of magnitude 1/8 .. 3.75,
+    k_scale = v_scale = 0.5): half the cache bytes per key."""
+    assert 1 <= replicas <= 8
+    return build("decode_8k_e4m3", "bf16", 32, 8, 128, [(8191, 1)], seed=seed,
+                 pool_blocks=4096, replicas=replicas, kv_dtype="e4m3", k_scale=0.5,
+                 v_scale=0.5)
+
+
 NAMED = {
     "tiny_mixed_f32": tiny_mixed_f32,
     "decode_8k": decode_8k,
@@ -205,7 +214,8 @@ NAMED = {
 
 def random_small(seed: int, dtype: str = "bf16", hq: int = 4, hkv: int = 2, d: int = 128,
                  num_seqs: int = 5, max_ctx: int = 200, max_new: int = 40,
-                 causal: bool = True, spare_blocks: int = 7) -> Workload:
+                 causal: bool = True, spare_blocks: int = 7, kv_dtype: str | None = None,
+                 k_scale: float = 1.0, v_scale: float = 1.0) -> Workload:
     """A random small flat batch with ragged lengths (decodes, tails, prefills,
     empty requests) for parity sweeps."""
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -223,4 +233,5 @@ def random_small(seed: int, dtype: str = "bf16", hq: int = 4, hkv: int = 2, d: i
             shape.append((int(rng.integers(0, max_ctx)), 0))
     need = sum(_blocks_needed(c + s, BLOCK_SIZE) for c, s in shape)
     return build(f"random_small_{seed}", dtype, hq, hkv, d, shape, rng=rng,
-                 pool_blocks=need + spare_blocks, causal=causal)
+                 pool_blocks=need + spare_blocks, causal=causal, kv_dtype=kv_dtype,
+                 k_scale=k_scale, v_scale=v_scale)
