@@ -42,6 +42,8 @@ WORKLOAD_TEXT = {
     "batched_decode_64": "64 decodes, context U[512,4096], GQA 32/8, head_dim 128, bf16",
     "mixed_chunked": "flat batch: 2048-token prefill chunk + 3-token tail on 1000 + 62 decodes "
                      "U[256,2048], GQA 32/8, head_dim 128, bf16",
+    "decode_8k_e4m3": "decode_8k over an 8-bit E4M3 KV cache (k_scale = v_scale = 0.5; q, new "
+                      "K/V and out bf16): 512-block table from a shuffled 8192-block pool",
 }
 
 
@@ -117,9 +119,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_record(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+def traffic_record(kernel_file: str, workload: str):
+    """DRAM bytes per launch of `workload` from the committed ncu summary, if
+    it was taken on the current source of the kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     src = os.path.join(ROOT, "paged_kv_attention_17_gb300", "csrc", kernel_file)
     try:
@@ -129,7 +131,7 @@ def traffic_record(kernel_file: str):
         return None
     for line in text.splitlines():
         m = re.match(r"\|\s*(\S+)\s*\|\s*(\S+)\s*\|\s*(\d+)\s*\|\s*([0-9a-f]{16})\s*\|", line)
-        if m and m.group(1) == kernel_file and m.group(4) == digest:
+        if m and m.group(1) == kernel_file and m.group(2) == workload and m.group(4) == digest:
             return {"workload": m.group(2), "bytes": int(m.group(3))}
     return None
 
@@ -205,8 +207,14 @@ def _device_replicas(w, device):
             return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(device)
         return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
 
+    def cache(x):
+        # E4M3 caches hold their uint8 codes
+        if w.kv_dtype == "e4m3":
+            return torch.from_numpy(np.ascontiguousarray(x)).to(device)
+        return tt(x)
+
     common = {"q": tt(w.q), "k_new": tt(w.k_new), "v_new": tt(w.v_new),
-              "k_cache": tt(w.k_pool), "v_cache": tt(w.v_pool)}
+              "k_cache": cache(w.k_pool), "v_cache": cache(w.v_pool)}
     reps = []
     for reqs in w.replicas:
         m = metadata.build(reqs, w.block_size)
@@ -274,10 +282,11 @@ def run_gpu(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     peaks, peak_src = load_peaks()
     name = args.workload
-    reps_wanted = 8 if name == "decode_8k" else 1
+    reps_wanted = {"decode_8k": 8, "decode_8k_e4m3": 16}.get(name, 1)
     w = workloads.NAMED[name](replicas=reps_wanted) if name != "tiny_mixed_f32" else workloads.NAMED[name]()
     common, reps = _device_replicas(w, device)
-    esize = 2 if w.dtype == "bf16" else 4
+    e4m3 = w.kv_dtype == "e4m3"
+    esize = 1 if e4m3 else (2 if w.dtype == "bf16" else 4)     # cache bytes per element
     m0 = reps[0]["meta"]
     hq, hkv, d = w.num_q_heads, w.num_kv_heads, w.head_dim
     splits = pkv.pkv_num_splits(w.num_seqs, m0["max_query_len"], m0["max_seq_len"], hq, hkv, d,
@@ -288,11 +297,23 @@ def run_gpu(args, rank, world, local_rank):
     flag = torch.zeros(1, dtype=torch.int32, device=device)
 
     def write(rep):
+        if e4m3:
+            pkv.pkv_write_e4m3(common["k_new"], common["v_new"], rep["slot_mapping"],
+                               common["k_cache"], common["v_cache"], w.k_scale, w.v_scale,
+                               error_flag=flag)
+            return
         pkv.pkv_write(common["k_new"], common["v_new"], rep["slot_mapping"], common["k_cache"],
                       common["v_cache"], error_flag=flag)
 
     def attend(rep):
         m = rep["meta"]
+        if e4m3:
+            pkv.pkv_attention_varlen_e4m3(
+                common["q"], common["k_cache"], common["v_cache"], out, rep["qsl"],
+                rep["seq_lens"], rep["block_table"], m["max_query_len"], m["max_seq_len"],
+                w.softmax_scale, w.k_scale, w.v_scale, causal=w.causal, num_splits=splits,
+                workspace=workspace, error_flag=flag)
+            return
         pkv.pkv_attention_varlen(common["q"], common["k_cache"], common["v_cache"], out, rep["qsl"],
                                  rep["seq_lens"], rep["block_table"], m["max_query_len"],
                                  m["max_seq_len"], w.softmax_scale, causal=w.causal,
@@ -407,8 +428,8 @@ def run_gpu(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4)}
         kernel_file = "prefill.cu"
-    tr = traffic_record(kernel_file)
-    roof["traffic"] = tr["bytes"] if tr and tr["workload"] == name else None
+    tr = traffic_record(kernel_file, name)
+    roof["traffic"] = tr["bytes"] if tr else None
     roof["kernel"] = ("pkv_attention_varlen call (split-KV decode kernel + LSE combine), "
                       f"{splits} splits" if decode_like else "pkv_attention_varlen call (prefill)")
     roof["peak_source"] = peak_src
@@ -422,12 +443,14 @@ def run_gpu(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2),
         "unit": "GB/s" if decode_like else "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic: seeded N(0,1) PCG64(0), cast to bf16 (RNE)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else w.dtype,
+        "data": "synthetic: seeded N(0,1) PCG64(0), cast to bf16 (RNE)" + (
+            "; cache codes drawn as E4M3 bit fields (exponent 4..8)" if e4m3 else ""),
         "config": {"workload": f"{name}: {WORKLOAD_TEXT[name]}", "num_splits": splits,
                    "kv_bytes_per_step": bytes_step, "flops_per_step": flops_step,
-                   "l2": ("cold: steps rotate over 8 disjoint 512-block tables of a 268 MB pool"
-                          if name == "decode_8k" else "inputs larger than L2"),
+                   "l2": (f"cold: steps rotate over {len(reps)} disjoint 512-block tables of a "
+                          "268 MB pool" if name.startswith("decode_8k") else
+                          "inputs larger than L2"),
                    "cuda_graph": use_graph, "parallelism": f"replicas x{world}"},
         "roofline": roof, "e2e": e2e,
         "gpu_launches": _launches_per_step(splits, m0) * args.steps,
@@ -451,8 +474,10 @@ def run_e2e_graphs(args, w, reps, common, bytes_step):
     m0 = reps[0]["meta"]
     width = int(reps[0]["block_table"].shape[1])
     n = w.num_seqs
+    scales = (w.k_scale, w.v_scale) if w.kv_dtype == "e4m3" else None
     runner = DecodeGraphRunner(common["k_cache"], common["v_cache"], w.num_q_heads,
-                               w.softmax_scale, width, m0["max_seq_len"], max_batch=n)
+                               w.softmax_scale, width, m0["max_seq_len"], max_batch=n,
+                               kv_scales=scales)
     hq = common["q"].cpu()
     hk, hv = common["k_new"].cpu(), common["v_new"].cpu()
     packed = [runner.pack(n, hq, hk, hv, r["slot_mapping"].cpu(), r["seq_lens"].cpu(),
@@ -567,10 +592,8 @@ def oracle_sampler(name):
     from oracle import flatten as ofl
     from oracle import ref
     w = workloads.NAMED[name]()
-    meta = ofl.flatten(w.requests)
-    kc = ofl.write(w.k_pool, w.k_new, meta["slot_mapping"])
-    vc = ofl.write(w.v_pool, w.v_new, meta["slot_mapping"])
-    esize = 2 if w.dtype == "bf16" else 4
+    _, _, kc, vc, _ = ref.paged_step(w, tokens=[])      # the oracle's write only
+    esize = 1 if w.kv_dtype == "e4m3" else (2 if w.dtype == "bf16" else 4)
 
     def run(sample_keys):
         import numpy as np
@@ -583,7 +606,8 @@ def oracle_sampler(name):
         m = ofl.flatten(reqs)
         ref.attention(w.q, kc, vc, m["query_start_loc"], m["seq_lens"], m["block_table"],
                       num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
-                      softmax_scale=w.softmax_scale, causal=w.causal, dtype=w.dtype)
+                      softmax_scale=w.softmax_scale, causal=w.causal, dtype=w.dtype,
+                      kv_dtype=w.kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale)
         return kv_bytes(reqs, w.num_kv_heads, w.head_dim, esize), causal_flops(
             reqs, w.num_q_heads, w.head_dim)
     full_keys = max(r.computed + r.scheduled for r in w.requests)

@@ -14,6 +14,8 @@ one graph holding a whole decode step on static buffers:
 1. the copy of the step's packed inputs from pinned host memory to the device,
 2. ``pkv_write`` of the new tokens' K/V,
 3. ``pkv_attention_varlen`` (one query token per request),
+
+(``pkv_write_e4m3`` and ``pkv_attention_varlen_e4m3`` over an 8-bit E4M3 cache),
 4. the copy of the output rows (and the error flag) back to pinned host memory.
 
 With ``zero_copy`` the graph has no copy nodes: its kernels read the pinned
@@ -109,8 +111,9 @@ class DecodeGraphRunner:
     """Decode steps (one new token per request) replayed from a ladder of
     captured CUDA graphs over one paged cache.
 
-    k_cache, v_cache: device [num_blocks, 16, hkv, D] (bf16 or fp32), used in
-    place.  max_seq_len bounds every request's context (it sizes the split
+    k_cache, v_cache: device [num_blocks, 16, hkv, D] (bf16 or fp32, or uint8
+    E4M3 codes with ``kv_scales`` = (k_scale, v_scale) and bf16 q / new K/V /
+    out), used in place.  max_seq_len bounds every request's context (it sizes the split
     count at capture).  The output of a step stays valid in the returned host
     tensor until its staging slot is reused (``slots`` steps later).
     zero_copy (default): the kernels use the pinned staging and output in
@@ -119,10 +122,15 @@ class DecodeGraphRunner:
     """
 
     def __init__(self, k_cache, v_cache, num_q_heads, softmax_scale, max_blocks_per_seq,
-                 max_seq_len, max_batch=64, sizes=None, slots=2, zero_copy=True):
+                 max_seq_len, max_batch=64, sizes=None, slots=2, zero_copy=True,
+                 kv_scales=None):
         self.k_cache, self.v_cache = k_cache, v_cache
         self.device = k_cache.device
-        self.dtype = k_cache.dtype
+        self.e4m3 = k_cache.dtype == torch.uint8
+        if self.e4m3 and kv_scales is None:
+            raise ValueError("an E4M3 (uint8) cache needs kv_scales=(k_scale, v_scale)")
+        self.kv_scales = tuple(float(x) for x in kv_scales) if self.e4m3 else None
+        self.dtype = torch.bfloat16 if self.e4m3 else k_cache.dtype   # q / new K/V / out
         _, bs, self.hkv, self.d = k_cache.shape
         if bs != 16:
             raise ValueError("block size must be 16")
@@ -135,7 +143,7 @@ class DecodeGraphRunner:
         self.sizes = sorted({int(s) for s in ladder if 1 <= int(s) <= max_batch})
         if not self.sizes or self.sizes[-1] < max_batch:
             self.sizes.append(int(max_batch))
-        esize = k_cache.element_size()
+        esize = torch.empty((), dtype=self.dtype).element_size()
         self.layouts = {b: InputLayout.of(b, self.hq, self.hkv, self.d, esize, self.max_blocks)
                         for b in self.sizes}
         top = self.layouts[self.sizes[-1]].nbytes
@@ -189,13 +197,23 @@ class DecodeGraphRunner:
             out = self.out[:b]
             self.flag.zero_()
             self.dev_in[:lay.nbytes].copy_(self.host_in[slot][:lay.nbytes], non_blocking=True)
-        B.pkv_write(v["k_new"], v["v_new"], v["slot_mapping"], self.k_cache, self.v_cache,
-                    error_flag=self.flag)
-        B.pkv_attention_varlen(v["q"], self.k_cache, self.v_cache, out,
-                               v["query_start_loc"], v["seq_lens"], v["block_table"], 1,
-                               self.max_seq_len, self.scale, causal=True,
-                               num_splits=self.splits[b], workspace=self.workspace,
-                               error_flag=self.flag)
+        if self.e4m3:
+            ks, vs = self.kv_scales
+            B.pkv_write_e4m3(v["k_new"], v["v_new"], v["slot_mapping"], self.k_cache,
+                             self.v_cache, ks, vs, error_flag=self.flag)
+            B.pkv_attention_varlen_e4m3(v["q"], self.k_cache, self.v_cache, out,
+                                        v["query_start_loc"], v["seq_lens"], v["block_table"], 1,
+                                        self.max_seq_len, self.scale, ks, vs, causal=True,
+                                        num_splits=self.splits[b], workspace=self.workspace,
+                                        error_flag=self.flag)
+        else:
+            B.pkv_write(v["k_new"], v["v_new"], v["slot_mapping"], self.k_cache, self.v_cache,
+                        error_flag=self.flag)
+            B.pkv_attention_varlen(v["q"], self.k_cache, self.v_cache, out,
+                                   v["query_start_loc"], v["seq_lens"], v["block_table"], 1,
+                                   self.max_seq_len, self.scale, causal=True,
+                                   num_splits=self.splits[b], workspace=self.workspace,
+                                   error_flag=self.flag)
         if not self.zero_copy:
             self.host_out[slot][:b].copy_(self.out[:b], non_blocking=True)
             self.host_flag[slot].copy_(self.flag, non_blocking=True)

@@ -56,3 +56,35 @@ def test_graph_runner_steps_match_oracle(zero_copy):
         got_k = kc.view(-1, 8, 128)[torch.from_numpy(slots).cuda()].view(torch.int16).cpu().numpy()
         want_k = kc_ref.reshape(-1, 8, 128)[slots].view(np.int16)
         assert np.array_equal(got_k, want_k)
+
+
+def test_graph_runner_over_an_e4m3_cache():
+    rng = np.random.Generator(np.random.PCG64(6))
+    ctx = rng.integers(1, 700, size=8)
+    w = workloads.build("graphs_e4m3", "bf16", 32, 8, 128, [(int(c) - 1, 1) for c in ctx],
+                        seed=12, kv_dtype="e4m3", k_scale=0.5, v_scale=0.25)
+    kc = torch.from_numpy(w.k_pool).cuda()
+    vc = torch.from_numpy(w.v_pool).cuda()
+    runner = DecodeGraphRunner(kc, vc, 32, w.softmax_scale, 48, 700, max_batch=8,
+                               sizes=[1, 2, 4, 8], kv_scales=(0.5, 0.25))
+    for idx in ([0, 1, 2], list(range(8)), [6, 2]):
+        sub = _subset(w, np.array(idx))
+        meta = metadata.build(sub.requests, sub.block_size)
+        step = runner.begin(len(idx))
+        step.q.copy_(to_torch(sub.q, "bf16", "cpu"))
+        step.k_new.copy_(to_torch(sub.k_new, "bf16", "cpu"))
+        step.v_new.copy_(to_torch(sub.v_new, "bf16", "cpu"))
+        step.slot_mapping.copy_(torch.from_numpy(meta["slot_mapping"]))
+        step.seq_lens.copy_(torch.from_numpy(meta["seq_lens"]))
+        bt = meta["block_table"]
+        step.block_table.zero_()
+        step.block_table[:, :bt.shape[1]].copy_(torch.from_numpy(bt))
+        runner.launch(step)
+        out, flag = runner.result(step)
+        assert flag == 0
+        o_ref, _, kc_ref, _, _ = ref.paged_step(sub)
+        err = np.abs(out.float().numpy().astype(np.float64) - o_ref)
+        assert err.max() <= 1e-2 and err.mean() <= 1e-3, (idx, err.max(), err.mean())
+        slots = meta["slot_mapping"]
+        got_k = kc.view(-1, 8, 128)[torch.from_numpy(slots).cuda()].cpu().numpy()
+        assert np.array_equal(got_k, kc_ref.reshape(-1, 8, 128)[slots])

@@ -196,10 +196,11 @@ def prefill_8k(seed: int = 0, replicas: int = 1) -> Workload:
 
 def decode_8k_e4m3(seed: int = 0, replicas: int = 1) -> Workload:
     """decode_8k over an 8-bit E4M3 cache (codes of magnitude 1/8 .. 3.75,
-    k_scale = v_scale = 0.5): half the cache bytes per key."""
-    assert 1 <= replicas <= 8
+    k_scale = v_scale = 0.5): half the cache bytes per key, so the shuffled
+    pool has 8192 blocks (268 MB, as decode_8k's) and 16 disjoint replicas fit."""
+    assert 1 <= replicas <= 16
     return build("decode_8k_e4m3", "bf16", 32, 8, 128, [(8191, 1)], seed=seed,
-                 pool_blocks=4096, replicas=replicas, kv_dtype="e4m3", k_scale=0.5,
+                 pool_blocks=8192, replicas=replicas, kv_dtype="e4m3", k_scale=0.5,
                  v_scale=0.5)
 
 
@@ -209,6 +210,7 @@ NAMED = {
     "batched_decode_64": batched_decode_64,
     "mixed_chunked": mixed_chunked,
     "prefill_8k": prefill_8k,
+    "decode_8k_e4m3": decode_8k_e4m3,
 }
 
 
