@@ -3,7 +3,8 @@
 This is the textbook computation that "Inside the engine: kernels, CUDA graphs
 and the life of a request" (section "Never materialise the TxT matrix")
 describes before tiling removes it: S = scale * Q K^T over the full [n, L]
-matrix, -inf where the causal mask hides a key, a row-wise softmax, then P V.
+matrix, -inf where the causal mask (or a sliding window) hides a key, a
+row-wise softmax, then P V.
 Used only on tiny inputs, as a second formulation for ``ref`` to agree with.
 """
 
@@ -22,7 +23,7 @@ def _as_f64(x, dtype):
 
 def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, *,
               num_q_heads, num_kv_heads, softmax_scale, causal=True, block_size=16,
-              dtype="f32"):
+              dtype="f32", window=0):
     Q = _as_f64(q, dtype)
     Kc = _as_f64(k_cache, dtype).reshape(-1, num_kv_heads, Q.shape[2])
     Vc = _as_f64(v_cache, dtype).reshape(-1, num_kv_heads, Q.shape[2])
@@ -44,6 +45,10 @@ def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, *,
             if causal:
                 # query i (0-based among the n new tokens) is token L - n + i
                 S = np.where(np.tril(np.ones((n, L), dtype=bool), k=L - n), S, -np.inf)
+            if window > 0:
+                # sliding window: query i drops keys more than window - 1 behind it
+                S = np.where(np.triu(np.ones((n, L), dtype=bool), k=L - n - window + 1), S,
+                             -np.inf)
             P = softmax(S, axis=1)
             out[a:b, h, :] = P @ Vc[slots, kvh, :]
     return out

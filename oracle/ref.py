@@ -17,7 +17,11 @@ Readings taken where the pages are silent:
   sits at position p = L - n + i and, under the causal mask, sees keys 0..p;
 * query head h reads kv head h // (Hq / Hkv) (contiguous GQA groups);
 * the cache is two tensors [num_blocks, block_size, Hkv, D] (K and V), i.e.
-  one row of Hkv * D values per slot.
+  one row of Hkv * D values per slot;
+* a sliding window W > 0 ("Anatomy of a serving engine", section "Where it
+  breaks", names sliding-window attention as a backend-dependent variant and
+  gives no definition) keeps, for the row at position p, only keys j with
+  j > p - W: the W most recent positions, the row's own included.
 
 For every (row, head) the oracle takes pass 1, m = max_j s_j and
 l = sum_j exp(s_j - m), then pass 2, o = sum_j (exp(s_j - m) / l) v_j, and
@@ -52,12 +56,13 @@ def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, *,
               num_q_heads: int, num_kv_heads: int, softmax_scale: float,
               causal: bool = True, block_size: int = 16, dtype: str = "f32",
               tokens=None, row_chunk: int = 512, kv_dtype: str | None = None,
-              k_scale: float = 1.0, v_scale: float = 1.0):
+              k_scale: float = 1.0, v_scale: float = 1.0, window: int = 0):
     """Attention output of the flat batch.
 
     With ``kv_dtype="e4m3"`` the caches hold 8-bit E4M3 codes and a cached K
     (V) element is ``k_scale`` (``v_scale``) times the code's value
-    (``oracle.fp8``); q stays in ``dtype``.
+    (``oracle.fp8``); q stays in ``dtype``.  ``window`` > 0 hides every key
+    j <= p - window from the row at position p (on top of the causal mask).
 
     Returns ``(o, lse)``: o float64 [N, Hq, D], lse float64 [N, Hq].  With
     ``tokens`` (an iterable of flat-batch indices) only those rows are
@@ -94,6 +99,8 @@ def attention(q, k_cache, v_cache, query_start_loc, seq_lens, block_table, *,
             pos = L - n + ri                                  # position of each row
             visible = pos + 1 if causal else np.full(ri.shape, L)
             mask = np.arange(L)[None, :] < visible[:, None]   # [rows, L]
+            if window > 0:
+                mask &= np.arange(L)[None, :] > (pos - window)[:, None]
             for h in range(hq):
                 g = h // group
                 s = softmax_scale * (qf[start + ri, h, :] @ K[:, g, :].T)   # [rows, L]
@@ -132,5 +139,6 @@ def paged_step(workload, tokens=None):
                        softmax_scale=workload.softmax_scale, causal=workload.causal,
                        block_size=workload.block_size, dtype=workload.dtype, tokens=tokens,
                        kv_dtype=kv, k_scale=getattr(workload, "k_scale", 1.0),
-                       v_scale=getattr(workload, "v_scale", 1.0))
+                       v_scale=getattr(workload, "v_scale", 1.0),
+                       window=getattr(workload, "window", 0))
     return o, lse, kc, vc, meta

@@ -173,6 +173,109 @@ def test_bf16_path_matches_brute_force():
 # Closed forms and stated invariants
 # --------------------------------------------------------------------------
 
+# --------------------------------------------------------------------------
+# Sliding window (reading: row at position p keeps keys j > p - W)
+# --------------------------------------------------------------------------
+
+def _sdpa_window(q, kc, vc, reqs, hq, hkv, scale, window):
+    """torch float64 SDPA with an explicit boolean band mask per request."""
+    out = np.zeros_like(q)
+    kflat = torch.from_numpy(kc.reshape(-1, hkv, kc.shape[-1]))
+    vflat = torch.from_numpy(vc.reshape(-1, hkv, vc.shape[-1]))
+    t0 = 0
+    for r in reqs:
+        n, L = r.scheduled, r.computed + r.scheduled
+        if n == 0:
+            continue
+        base = r.blocks[0] * 16
+        pos = torch.arange(L - n, L)[:, None]
+        key = torch.arange(L)[None, :]
+        mask = (key <= pos) & (key > pos - window)
+        Q = torch.from_numpy(q[t0:t0 + n]).permute(1, 0, 2)[None]
+        K = kflat[base:base + L].permute(1, 0, 2)[None]
+        V = vflat[base:base + L].permute(1, 0, 2)[None]
+        o = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=scale,
+                                           enable_gqa=True)
+        out[t0:t0 + n] = o[0].permute(1, 0, 2).numpy()
+        t0 += n
+    return out
+
+
+@pytest.mark.parametrize("window", [1, 2, 7, 16, 17, 40, 1000])
+def test_window_matches_torch_sdpa_band_mask(window):
+    rng = np.random.default_rng(50 + window)
+    shape = [(0, 32), (39, 1), (45, 3), (5, 11), (17, 16), (0, 1), (70, 2)]
+    reqs, kc, vc, q = _contiguous_case(rng, 4, 2, 16, shape)
+    o, _ = _ref(q, kc, vc, reqs, 4, 2, 0.25, True, window=window)
+    want = _sdpa_window(q, kc, vc, reqs, 4, 2, 0.25, window)
+    assert np.abs(o - want).max() < 1e-12
+
+
+@pytest.mark.parametrize("window", [1, 5, 16, 33])
+def test_window_matches_brute_force_paged(window):
+    w = workloads.random_small(12, dtype="f32", hq=4, hkv=2, d=16, num_seqs=6, max_ctx=70)
+    meta = flatten.flatten(w.requests)
+    args = (w.q, w.k_pool, w.v_pool, meta["query_start_loc"], meta["seq_lens"],
+            meta["block_table"])
+    kw = dict(num_q_heads=4, num_kv_heads=2, softmax_scale=w.softmax_scale, dtype="f32",
+              window=window)
+    o, _ = ref.attention(*args, **kw)
+    assert np.abs(o - brute.attention(*args, **kw)).max() < 1e-12
+
+
+def test_window_of_one_returns_the_rows_own_value():
+    rng = np.random.default_rng(7)
+    reqs, kc, vc, q = _contiguous_case(rng, 4, 2, 16, [(20, 3), (0, 5)])
+    o, lse = _ref(q, kc, vc, reqs, 4, 2, 0.25, True, window=1)
+    vflat, kflat = vc.reshape(-1, 2, 16), kc.reshape(-1, 2, 16)
+    t = 0
+    for r in reqs:
+        L, n = r.computed + r.scheduled, r.scheduled
+        for i in range(n):
+            slot = r.blocks[0] * 16 + L - n + i
+            for h in range(4):
+                assert np.array_equal(o[t, h], vflat[slot, h // 2])
+                assert abs(lse[t, h] - 0.25 * q[t, h] @ kflat[slot, h // 2]) < 1e-12
+            t += 1
+
+
+def test_window_zero_query_gives_the_window_mean():
+    rng = np.random.default_rng(8)
+    reqs, kc, vc, q = _contiguous_case(rng, 2, 1, 8, [(40, 4), (3, 2)])
+    q[:] = 0.0
+    o, lse = _ref(q, kc, vc, reqs, 2, 1, 0.125, True, window=9)
+    vflat = vc.reshape(-1, 1, 8)
+    t = 0
+    for r in reqs:
+        L, n = r.computed + r.scheduled, r.scheduled
+        for i in range(n):
+            p = L - n + i
+            lo = max(0, p - 9 + 1)
+            base = r.blocks[0] * 16
+            assert np.allclose(o[t, 0], vflat[base + lo:base + p + 1, 0].mean(axis=0),
+                               atol=1e-13, rtol=0)
+            assert abs(lse[t, 0] - math.log(p + 1 - lo)) < 1e-13
+            t += 1
+
+
+def test_window_equals_plain_attention_over_the_last_keys():
+    # a decode row with window W sees exactly what a request holding only the
+    # last W keys sees without a window (positions shift, the values do not)
+    rng = np.random.default_rng(9)
+    L, W = 77, 21
+    reqs, kc, vc, q = _contiguous_case(rng, 4, 2, 16, [(L - 1, 1)])
+    o, lse = _ref(q, kc, vc, reqs, 4, 2, 0.25, True, window=W)
+    kf, vf = kc.reshape(-1, 2, 16), vc.reshape(-1, 2, 16)
+    nb = -(-W // 16)
+    k2 = np.zeros((nb * 16, 2, 16))
+    v2 = np.zeros((nb * 16, 2, 16))
+    k2[:W], v2[:W] = kf[L - W:L], vf[L - W:L]
+    short = [_req(W - 1, 1, range(nb))]
+    o2, lse2 = _ref(q, k2.reshape(nb, 16, 2, 16), v2.reshape(nb, 16, 2, 16), short, 4, 2,
+                    0.25, True)
+    assert np.abs(o - o2).max() < 1e-13 and np.abs(lse - lse2).max() < 1e-13
+
+
 def test_zero_query_gives_prefix_mean_and_log_count():
     # all scores equal -> uniform weights over the visible keys
     rng = np.random.default_rng(1)

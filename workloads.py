@@ -66,6 +66,7 @@ class Workload:
     # (index 0 is ``requests``); used to keep repeated timed steps L2-cold.
     replicas: list[list[Request]] = field(default_factory=list)
     kv_dtype: str | None = None     # None: caches in `dtype`; "e4m3": 8-bit codes + scales
+    window: int = 0                 # > 0: sliding window of that many positions
     k_scale: float = 1.0
     v_scale: float = 1.0
 
@@ -120,7 +121,8 @@ def build(name: str, dtype: str, hq: int, hkv: int, d: int,
           shape: list[tuple[int, int]], seed: int = 0, pool_blocks: int | None = None,
           replicas: int = 1, scale: float | None = None, causal: bool = True,
           lengths_drawn: bool = False, rng: np.random.Generator | None = None,
-          kv_dtype: str | None = None, k_scale: float = 1.0, v_scale: float = 1.0) -> Workload:
+          kv_dtype: str | None = None, k_scale: float = 1.0, v_scale: float = 1.0,
+          window: int = 0) -> Workload:
     """Lay out a workload from a list of (computed, scheduled) pairs.
 
     The pool holds ``replicas`` disjoint copies of the schedule's blocks (or
@@ -149,7 +151,7 @@ def build(name: str, dtype: str, hq: int, hkv: int, d: int,
                     k_pool=k_pool, v_pool=v_pool,
                     softmax_scale=float(scale if scale is not None else 1.0 / np.sqrt(d)),
                     causal=causal, replicas=reps, kv_dtype=kv_dtype, k_scale=float(k_scale),
-                    v_scale=float(v_scale))
+                    v_scale=float(v_scale), window=int(window))
 
 
 # ---------------------------------------------------------------------------
@@ -217,7 +219,7 @@ NAMED = {
 def random_small(seed: int, dtype: str = "bf16", hq: int = 4, hkv: int = 2, d: int = 128,
                  num_seqs: int = 5, max_ctx: int = 200, max_new: int = 40,
                  causal: bool = True, spare_blocks: int = 7, kv_dtype: str | None = None,
-                 k_scale: float = 1.0, v_scale: float = 1.0) -> Workload:
+                 k_scale: float = 1.0, v_scale: float = 1.0, window: int = 0) -> Workload:
     """A random small flat batch with ragged lengths (decodes, tails, prefills,
     empty requests) for parity sweeps."""
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -236,4 +238,4 @@ def random_small(seed: int, dtype: str = "bf16", hq: int = 4, hkv: int = 2, d: i
     need = sum(_blocks_needed(c + s, BLOCK_SIZE) for c, s in shape)
     return build(f"random_small_{seed}", dtype, hq, hkv, d, shape, rng=rng,
                  pool_blocks=need + spare_blocks, causal=causal, kv_dtype=kv_dtype,
-                 k_scale=k_scale, v_scale=v_scale)
+                 k_scale=k_scale, v_scale=v_scale, window=window)
