@@ -192,6 +192,33 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
                                 int64_t num_blocks, pkv_dtype dtype, void* stream);
 
 /*
+ * pkv_attention_varlen_window - pkv_attention_varlen with a sliding window.
+ *
+ * "Anatomy of a serving engine", section "Where it breaks": sliding-window
+ * attention is a variant some backends support; the pages give no
+ * definition.  Reading taken: with window W > 0 the new token at position
+ * p = L - n + i sees only keys j with p - W < j (the W most recent
+ * positions, itself included), on top of the causal limit j <= p (or j < L
+ * with causal == 0).  window == 0 is pkv_attention_varlen exactly.  Key
+ * blocks wholly below a tile's window start are not read, and the automatic
+ * split count is sized for a context of window + PKV_DECODE_MAX_QLEN keys.
+ * Windows shorter than 128 keys run every request on the split-KV kernel's
+ * CUDA-core tiles (fp32 P) instead of the tensor-core prefill.
+ *   window  >= 0 (negative: PKV_ERR_INVALID_ARG).
+ * Everything else as pkv_attention_varlen.
+ */
+pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const void* v_cache,
+                                       void* out, float* lse_out,
+                                       const int32_t* query_start_loc, const int32_t* seq_lens,
+                                       const int32_t* block_table, int max_blocks_per_seq,
+                                       int num_seqs, int64_t num_tokens, int max_query_len,
+                                       int max_seq_len, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float softmax_scale,
+                                       int causal, int window, int num_splits, void* workspace,
+                                       size_t workspace_bytes, int32_t* error_flag,
+                                       int64_t num_blocks, pkv_dtype dtype, void* stream);
+
+/*
  * pkv_attention_varlen_e4m3 - pkv_attention_varlen over an E4M3 cache.
  *
  * The cache format of pkv_write_e4m3: key j stands for k_scale * value(code),

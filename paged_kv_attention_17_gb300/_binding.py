@@ -23,8 +23,8 @@ FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_num_splits", "pkv_workspace_bytes",
-           "pkv_attention_varlen", "pkv_attention_varlen_e4m3", "pkv_attention_varlen_noalloc",
-           "pkv_status_string")
+           "pkv_attention_varlen", "pkv_attention_varlen_window", "pkv_attention_varlen_e4m3",
+           "pkv_attention_varlen_noalloc", "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -56,6 +56,10 @@ def lib() -> ctypes.CDLL:
                                            i32, i32, i32, i32, ctypes.c_float, i32, i32, vp, sz,
                                            vp, i64, i32, vp]
         L.pkv_attention_varlen.restype = i32
+        L.pkv_attention_varlen_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
+                                                  i32, i32, i32, i32, i32, i32, f32, i32, i32,
+                                                  i32, vp, sz, vp, i64, i32, vp]
+        L.pkv_attention_varlen_window.restype = i32
         L.pkv_attention_varlen_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, i32,
                                                 i32, i32, i32, i32, i32, f32, f32, f32, i32, i32,
                                                 vp, sz, vp, i64, vp]
@@ -135,26 +139,46 @@ def pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, num_splits) -> int:
                                          int(num_splits)))
 
 
+def split_span(max_seq_len, window=0) -> int:
+    """The context length the automatic split count is sized for: a window
+    bounds the keys a decode row reads to window + PKV_DECODE_MAX_QLEN."""
+    if 0 < window < max_seq_len - PKV_DECODE_MAX_QLEN:
+        return int(window) + PKV_DECODE_MAX_QLEN
+    return int(max_seq_len)
+
+
 def pkv_attention_varlen(q, k_cache, v_cache, out, query_start_loc, seq_lens, block_table,
                          max_query_len, max_seq_len, softmax_scale, causal=True, num_splits=0,
-                         workspace=None, lse_out=None, error_flag=None, stream=None):
+                         workspace=None, lse_out=None, error_flag=None, stream=None, window=0):
     """Attention of the flat batch q [N, Hq, D] over the paged cache into out.
 
     Metadata tensors are int32 on the device.  ``workspace`` is a uint8 device
     tensor of at least ``pkv_workspace_bytes(...)`` bytes; if None and one is
     needed it is allocated with torch here (allocate it yourself to capture the
-    call in a CUDA graph).
+    call in a CUDA graph).  ``window`` > 0 calls pkv_attention_varlen_window:
+    the row at position p sees keys j > p - window only.
     """
     n_tok, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     num_seqs = int(seq_lens.numel())
     splits = int(num_splits)
     if splits == 0 and num_seqs > 0:
-        splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, hq, hkv, d, q.device.index)
+        splits = pkv_num_splits(num_seqs, max_query_len, split_span(max_seq_len, window), hq, hkv,
+                                d, q.device.index)
     need = pkv_workspace_bytes(num_seqs, hq, d, splits)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if window:
+        code = lib().pkv_attention_varlen_window(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out),
+            _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]),
+            num_seqs, int(n_tok), int(max_query_len), int(max_seq_len), int(hq), int(hkv), int(d),
+            int(bs), float(softmax_scale), 1 if causal else 0, int(window), splits,
+            _ptr(workspace), int(ws_bytes), _ptr(error_flag), int(nb), _dtype_code(q.dtype),
+            _stream(stream))
+        _check("pkv_attention_varlen_window", code)
+        return out
     code = lib().pkv_attention_varlen(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
         _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]), num_seqs, int(n_tok),

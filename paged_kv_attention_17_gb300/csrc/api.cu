@@ -32,6 +32,7 @@ using namespace pkv;
 namespace {
 
 constexpr int kMinBlocksPerSplit = 8;    // 128 keys
+constexpr int kTcMinWindow = 128;        // shortest window the tensor-core prefill takes
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -126,11 +127,11 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
                             int max_blocks_per_seq, int num_seqs, int64_t num_tokens,
                             int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
                             int head_dim, int block_size, float softmax_scale, float k_scale,
-                            float v_scale, int causal, int num_splits, void* workspace,
-                            size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
-                            ElemType et, void* stream) {
+                            float v_scale, int causal, int window, int num_splits,
+                            void* workspace, size_t workspace_bytes, int32_t* error_flag,
+                            int64_t num_blocks, ElemType et, void* stream) {
   // ---- host-checkable arguments ----
-  if (num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
+  if (window < 0 || num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
       num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_splits < 0 ||
       num_splits > kMaxSplits || num_blocks < 1 || max_seq_len < 0 || max_query_len < 0 ||
       !std::isfinite(softmax_scale))
@@ -155,8 +156,11 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
       cudaGetLastError();
       return PKV_ERR_CUDA;
     }
-    splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads,
-                            head_dim, dev);
+    // a window bounds the keys a decode row reads: size the split by that span
+    const int span = window > 0 && window < max_seq_len - kDecodeMaxQ
+                         ? window + kDecodeMaxQ : max_seq_len;
+    splits = pkv_num_splits(num_seqs, max_query_len, span, num_q_heads, num_kv_heads, head_dim,
+                            dev);
   }
   if (splits < 1) return PKV_ERR_CUDA;
   const size_t need = pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
@@ -183,10 +187,14 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
   a.scale_log2 = softmax_scale * k_scale * kLog2e;
   a.v_scale = v_scale;
   a.causal = causal ? 1 : 0;
+  a.window = window;
   a.num_splits = splits;
-  // the tensor-core softmax takes the row max before scaling: positive scales only
-  const bool tc_prefill =
-      prefill_supported(head_dim, bf16, num_q_heads / num_kv_heads) && softmax_scale > 0.f;
+  // the tensor-core softmax takes the row max before scaling: positive scales
+  // only.  Windows shorter than its 128-key tile run on the CUDA-core tiles:
+  // a tensor-core tile would be mostly masked, and rows averaging so few keys
+  // have outputs large enough for its bf16 P rounding to show.
+  const bool tc_prefill = prefill_supported(head_dim, bf16, num_q_heads / num_kv_heads) &&
+                          softmax_scale > 0.f && (window == 0 || window >= kTcMinWindow);
   // E4M3 caches: decode rows take the register-q tiles, longer requests the
   // CUDA-core tiles of the same kernel
   a.long_rows = tc_prefill ? 0 : (et == ElemType::kE4m3 ? (max_query_len > kDecodeMaxQ) : 1);
@@ -334,8 +342,26 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
   return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
                    max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
                    num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, 1.f, 1.f,
-                   causal, num_splits, workspace, workspace_bytes, error_flag, num_blocks,
+                   causal, 0, num_splits, workspace, workspace_bytes, error_flag, num_blocks,
                    dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32, stream);
+}
+
+pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const void* v_cache,
+                                       void* out, float* lse_out,
+                                       const int32_t* query_start_loc, const int32_t* seq_lens,
+                                       const int32_t* block_table, int max_blocks_per_seq,
+                                       int num_seqs, int64_t num_tokens, int max_query_len,
+                                       int max_seq_len, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float softmax_scale,
+                                       int causal, int window, int num_splits, void* workspace,
+                                       size_t workspace_bytes, int32_t* error_flag,
+                                       int64_t num_blocks, pkv_dtype dtype, void* stream) {
+  if (!valid_dtype(dtype) || window < 0) return PKV_ERR_INVALID_ARG;
+  return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                   max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                   num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, 1.f, 1.f,
+                   causal, window, num_splits, workspace, workspace_bytes, error_flag,
+                   num_blocks, dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32, stream);
 }
 
 pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const void* v_cache,
@@ -351,7 +377,7 @@ pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const v
   return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
                    max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
                    num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, k_scale,
-                   v_scale, causal, num_splits, workspace, workspace_bytes, error_flag,
+                   v_scale, causal, 0, num_splits, workspace, workspace_bytes, error_flag,
                    num_blocks, ElemType::kE4m3, stream);
 }
 

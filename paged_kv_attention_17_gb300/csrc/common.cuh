@@ -46,6 +46,7 @@ struct AttnArgs {
   float scale_log2;       // softmax_scale * log2(e) (* k_scale for E4M3 caches): log2-domain scores
   float v_scale;          // output multiplier: v_scale for E4M3 caches, else 1
   int causal;
+  int window;             // > 0: row at position p sees keys j > p - window only
   int num_splits;         // >= 1
   int long_rows;          // decode kernel also runs requests with q_len > kDecodeMaxQ
   float* ws_o;            // [S][num_seqs][kDecodeMaxQ][hq][D]

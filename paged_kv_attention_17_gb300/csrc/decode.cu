@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   // their registers for the generic path
   constexpr bool kSpec = SPEC && R == 4;
   // whether this CTA may speculate (same answer on every thread)
-  const bool spec_possible = kSpec && a.num_splits > 1 && blockIdx.y == 0;
+  const bool spec_possible = kSpec && a.num_splits > 1 && blockIdx.y == 0 && a.window == 0;
   constexpr int kPWarpFloats = kBlock * R * 2;        // p_s floats per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
   int32_t e_hint = 0;                  // producer lane w: hinted entry of warp w's first block
   bool hint_ok = false;
-  if (producer && z == 0) {
+  if (producer && z == 0 && a.window == 0) {
     // ---- L2 warm-up while the previous kernel finishes: the K/V blocks this
     //      CTA will most likely read (the split range a context of
     //      max_seq_len keys gives, cut at the request's length and at
@@ -416,10 +416,14 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     drain_spec();
     return;
   }
-  int b0 = 0, b1 = nblk;
+  // sliding window: the tile's first row sees keys from key_lo on, later rows
+  // from further on; blocks below key_lo are never read
+  const int key_lo = a.window > 0 ? max(0, L - n + rho0 / group - a.window + 1) : 0;
+  const int blk_lo = min(key_lo / kBlock, nblk);
+  int b0 = blk_lo, b1 = nblk;
   if (split_mode) {
-    const int per = (nblk + a.num_splits - 1) / a.num_splits;
-    b0 = min(s * per, nblk);
+    const int per = (nblk - blk_lo + a.num_splits - 1) / a.num_splits;
+    b0 = blk_lo + min(s * per, nblk - blk_lo);
     b1 = min(b0 + per, nblk);
   }
   if (b0 >= b1) {
@@ -481,12 +485,16 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   f32x2 qr[kFast ? 4 : 1][kFast ? 4 * kFastChunks : 1];
   f32x2 acc2[kFast ? C::kDPL : 1][2];                  // [column][row pair (0,1) | (2,3)]
   float m_mine = -INFINITY, l_mine = 0.f;
-  int lim_mine = 0;
-  // causal limit of each row: keys < lim[rho] are visible
-  int lim[R];
+  int lim_mine = 0, lo_mine = 0;
+  // visible keys of each row: lo[rho] <= key < lim[rho] (causal limit, and the
+  // sliding window's start, which is <= 0 without a window)
+  const int wlo = a.window > 0 ? L - n - a.window + 1 : -(1 << 30);   // window start of row i: wlo + i
+  int lim[R], lo[R];
 #pragma unroll
-  for (int rho = 0; rho < R; ++rho)
+  for (int rho = 0; rho < R; ++rho) {
     lim[rho] = min(key_end, a.causal ? (L - n + (rho0 + rho) / group + 1) : L);
+    lo[rho] = wlo + (rho0 + rho) / group;
+  }
 
   if (producer) {
     // ---- TMA producer: lane w feeds consumer warp w (blocks b0 + w + kWarps*j).
@@ -607,6 +615,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < C::kDPL; ++c) acc2[c][0] = acc2[c][1] = 0ull;
       lim_mine = min(key_end, a.causal ? (L - n + (rho0 + my_r) / group + 1) : L);
+      lo_mine = wlo + (rho0 + my_r) / group;
     } else {
       // ---- stage q rows (pre-scaled into the log2 domain), consumer warps only ----
 #pragma unroll
@@ -719,8 +728,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
           s2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
         }
         // ---- online softmax of row my_r (the 8 lanes holding it share m) ----
-        const float x0 = key0 + kk0 < lim_mine ? s2[0] : -INFINITY;
-        const float x1 = key0 + kk0 + 1 < lim_mine ? s2[1] : -INFINITY;
+        const float x0 = key0 + kk0 < lim_mine && key0 + kk0 >= lo_mine ? s2[0] : -INFINITY;
+        const float x1 =
+            key0 + kk0 + 1 < lim_mine && key0 + kk0 + 1 >= lo_mine ? s2[1] : -INFINITY;
         float mx = fmaxf(x0, x1);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -840,7 +850,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       for (int rho = 0; rho < R; ++rho) sv[rho] += __shfl_xor_sync(0xffffffffu, sv[rho], 16);
 #pragma unroll
       for (int rho = 0; rho < R; ++rho) {
-        sv[rho] = key < lim[rho] ? sv[rho] : -INFINITY;
+        sv[rho] = key < lim[rho] && key >= lo[rho] ? sv[rho] : -INFINITY;
         mx[rho] = sv[rho];
       }
 #pragma unroll
@@ -1099,8 +1109,11 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
                                    cudaStream_t stream) {
   switch (R) {
     case 4:
-      return a.num_splits > 1 ? launch_decode_t<T, D, 4, true>(a, kmap, vmap, row_tiles, pdl, stream)
-                              : launch_decode_t<T, D, 4, false>(a, kmap, vmap, row_tiles, pdl, stream);
+      // speculative first blocks only for split launches without a window
+      // (their hinted block range ignores it)
+      return a.num_splits > 1 && a.window == 0
+                 ? launch_decode_t<T, D, 4, true>(a, kmap, vmap, row_tiles, pdl, stream)
+                 : launch_decode_t<T, D, 4, false>(a, kmap, vmap, row_tiles, pdl, stream);
     case 8: return launch_decode_t<T, D, 8, false>(a, kmap, vmap, row_tiles, pdl, stream);
     default: return launch_decode_t<T, D, 16, false>(a, kmap, vmap, row_tiles, pdl, stream);
   }

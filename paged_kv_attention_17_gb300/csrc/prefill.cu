@@ -271,7 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
     return;
   }
-  const int ntk = (kv_len + kKeys - 1) / kKeys;
+  // sliding window: key tiles wholly below the first row's window start are
+  // skipped; kt below counts the remaining tiles from kt_base
+  const int kt_base =
+      a.window > 0 ? max(0, L - n + i0 - a.window + 1) / kKeys : 0;
+  const int ntk = (kv_len + kKeys - 1) / kKeys - kt_base;
 
   // ---- barriers and TMEM ----
   if (threadIdx.x == 0) {
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kt = 0;
     for (; kt < ntk; ++kt) {
       const int st = kt % kStages;
-      const int blk = kt * (kKeys / kBlock) + (lane & 7);
+      const int blk = (kt_base + kt) * (kKeys / kBlock) + (lane & 7);
       int32_t ent = -1;
       if (lane < kKeys / kBlock && blk < nblk_ctx) {
         ent = __ldg(table + blk);
@@ -445,6 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_eff = min(i_r, n - 1);                   // padding rows mirror the last row
     const int lim = a.causal ? (L - n + i_eff + 1) : L;  // keys < lim are visible
     const int lim_min = a.causal ? min(L - n + i0 + 1, L) : L;   // smallest lim of the tile
+    // window start of the row (keys >= lo are visible) and the tile's largest
+    const int lo = a.window > 0 ? L - n + i_eff - a.window + 1 : 0;
+    const int lo_max = a.window > 0 ? L - n + min(i0 + kQRows, n) - 1 - a.window + 1 : 0;
     const uint32_t lane_base = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t t_s = lane_base + t * kKeys, t_o = lane_base + 2 * kKeys + t * 128;
     const float sc = a.scale_log2;
@@ -475,10 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[96 + i] = __uint_as_float(r3[i]);
         }
       }
-      const int key0 = kt * kKeys;
-      if (key0 + kKeys > lim_min) {                      // a tile crossing the causal edge
+      const int key0 = (kt_base + kt) * kKeys;
+      if (key0 + kKeys > lim_min || key0 < lo_max) {     // a tile crossing a mask edge
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) s[i] = (key0 + i < lim) ? s[i] : -INFINITY;
+        for (int i = 0; i < kKeys; ++i) s[i] = (key0 + i < lim && key0 + i >= lo) ? s[i] : -INFINITY;
       }
       float mx8[8];                                      // 8 independent max chains
 #pragma unroll
