@@ -24,6 +24,10 @@ Modules, each citing the passage it follows:
   log-sum-exp merge (sections "Never materialise the TxT matrix" and
   "Prefill has a full grid; decode at batch 1 has almost none").
 
+* ``cascade`` - attention of requests sharing a block-aligned prefix: the
+  plain result over shared ++ own blocks, and its two-level form (prefix
+  partial over all rows + per-request suffix partial, merged by log-sum-exp)
+  that a cascade kernel computes.
 * ``fp8`` - E4M3 codes of an 8-bit KV cache with per-tensor scales (the
   reading taken for the FP8 KV cache the "Model execution" page names; pinned
   in ``tests/test_oracle_fp8.py``).
@@ -34,4 +38,4 @@ contiguous equivalent, closed forms (uniform weights -> prefix mean, one key ->
 v, head-constant V -> GQA mapping) and paging/split invariance.
 """
 
-from . import brute, flatten, merge, ref  # noqa: F401
+from . import brute, cascade, flatten, merge, ref  # noqa: F401

@@ -67,6 +67,7 @@ class Workload:
     replicas: list[list[Request]] = field(default_factory=list)
     kv_dtype: str | None = None     # None: caches in `dtype`; "e4m3": 8-bit codes + scales
     window: int = 0                 # > 0: sliding window of that many positions
+    shared_blocks: int = 0          # leading blocks every request's table shares
     k_scale: float = 1.0
     v_scale: float = 1.0
 
@@ -152,6 +153,34 @@ def build(name: str, dtype: str, hq: int, hkv: int, d: int,
                     softmax_scale=float(scale if scale is not None else 1.0 / np.sqrt(d)),
                     causal=causal, replicas=reps, kv_dtype=kv_dtype, k_scale=float(k_scale),
                     v_scale=float(v_scale), window=int(window))
+
+
+def build_cascade(name: str, dtype: str, hq: int, hkv: int, d: int, shared_blocks: int,
+                  shape: list[tuple[int, int]], seed: int = 0, spare_blocks: int = 3,
+                  rng: np.random.Generator | None = None) -> Workload:
+    """Requests that share a prefix of ``shared_blocks`` blocks: each (c, s)
+    pair is a request with c cached keys of its own after the prefix and s new
+    tokens; its table is the shared blocks followed by its own."""
+    rng = rng if rng is not None else np.random.Generator(np.random.PCG64(seed))
+    own = [_blocks_needed(c + s, BLOCK_SIZE) for c, s in shape]
+    num_blocks = shared_blocks + sum(own) + spare_blocks
+    perm = rng.permutation(num_blocks)
+    shared = [int(b) for b in perm[:shared_blocks]]
+    reqs, start = [], shared_blocks
+    P = shared_blocks * BLOCK_SIZE
+    for (c, s), nb in zip(shape, own):
+        reqs.append(Request(P + c, s, shared + [int(b) for b in perm[start:start + nb]]))
+        start += nb
+    n = sum(s for _, s in shape)
+    pool_shape = (num_blocks, BLOCK_SIZE, hkv, d)
+    k_pool, v_pool = _values(rng, pool_shape, dtype), _values(rng, pool_shape, dtype)
+    q = _values(rng, (n, hq, d), dtype)
+    k_new = _values(rng, (n, hkv, d), dtype)
+    v_new = _values(rng, (n, hkv, d), dtype)
+    return Workload(name=name, dtype=dtype, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                    num_blocks=num_blocks, requests=reqs, q=q, k_new=k_new, v_new=v_new,
+                    k_pool=k_pool, v_pool=v_pool, softmax_scale=float(1.0 / np.sqrt(d)),
+                    replicas=[reqs], shared_blocks=shared_blocks)
 
 
 # ---------------------------------------------------------------------------
