@@ -42,6 +42,9 @@ WORKLOAD_TEXT = {
     "batched_decode_64": "64 decodes, context U[512,4096], GQA 32/8, head_dim 128, bf16",
     "mixed_chunked": "flat batch: 2048-token prefill chunk + 3-token tail on 1000 + 62 decodes "
                      "U[256,2048], GQA 32/8, head_dim 128, bf16",
+    "cascade_64x4k": "64 decodes sharing a 4096-token prefix (256 blocks), U[0,511] own cached "
+                     "keys + 1 new token each, GQA 32/8, head_dim 128, bf16; shared-prefix "
+                     "(cascade) attention, 4 replicas of 84 MB",
     "decode_8k_e4m3": "decode_8k over an 8-bit E4M3 KV cache (k_scale = v_scale = 0.5; q, new "
                       "K/V and out bf16): 512-block table from a shuffled 8192-block pool",
 }
@@ -226,6 +229,75 @@ def _device_replicas(w, device):
     return common, reps
 
 
+def _cascade_tensors(w, reps, device):
+    """Shared table, own-key tables and lengths of each replica of a cascade."""
+    import numpy as np
+    import torch
+    P = w.shared_blocks * w.block_size
+    for rep in reps:
+        reqs = rep["requests"]
+        own = [r.blocks[w.shared_blocks:] for r in reqs]
+        width = max(max(len(b) for b in own), 1)
+        table = np.zeros((len(own), width), dtype=np.int32)
+        for i, b in enumerate(own):
+            table[i, :len(b)] = b
+        lens = [r.computed + r.scheduled - P for r in reqs]
+        rep["shared_table"] = torch.tensor(reqs[0].blocks[:w.shared_blocks], dtype=torch.int32,
+                                           device=device)
+        rep["suffix_table"] = torch.from_numpy(table).to(device)
+        rep["suffix_lens"] = torch.tensor(lens, dtype=torch.int32, device=device)
+        rep["max_suffix_len"] = max(lens)
+
+
+def run_e2e_cascade(args, w, reps, common, csplits, cws, flag, bytes_step):
+    """Per step: pinned host -> device copies of Q, new K/V and the metadata
+    (slot mapping, query_start_loc, own-key lengths and tables, shared table),
+    pkv_write + pkv_cascade_attention, device -> host copy of the output."""
+    import torch
+
+    import paged_kv_attention_17_gb300 as pkv
+    keys = ("qsl", "slot_mapping", "suffix_lens", "suffix_table", "shared_table")
+    host = {k: common[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+    hreps = [{k: r[k].cpu().pin_memory() for k in keys} for r in reps]
+    dev = {k: torch.empty_like(common[k]) for k in ("q", "k_new", "v_new")}
+    dmeta = {k: torch.empty_like(reps[0][k]) for k in keys}
+    out = torch.empty_like(common["q"])
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def one(i):
+        hr, rep = hreps[i % len(hreps)], reps[i % len(reps)]
+        for k in dev:
+            dev[k].copy_(host[k], non_blocking=True)
+        for k in dmeta:
+            dmeta[k].copy_(hr[k], non_blocking=True)
+        pkv.pkv_write(dev["k_new"], dev["v_new"], dmeta["slot_mapping"], common["k_cache"],
+                      common["v_cache"], error_flag=flag)
+        pkv.pkv_cascade_attention(dev["q"], common["k_cache"], common["v_cache"], out,
+                                  dmeta["qsl"], dmeta["suffix_lens"], dmeta["suffix_table"],
+                                  dmeta["shared_table"], rep["meta"]["max_query_len"],
+                                  rep["max_suffix_len"], w.softmax_scale, prefix_splits=csplits,
+                                  workspace=cws, error_flag=flag)
+        hout.copy_(out, non_blocking=True)
+
+    k = min(args.steps, 500)
+    for i in range(min(20, k)):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(k):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / k
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        sum(t.numel() * t.element_size() for t in hreps[0].values())
+    d2h = hout.numel() * hout.element_size()
+    return {"value": round((bytes_step / 1e9) / (ms / 1e3), 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
+            "ms_per_step": round(ms, 6), "mode": "eager API calls, pinned host buffers"}
+
+
 def _launches_per_step(splits, meta):
     n = 2                                             # write + decode
     if splits > 1:
@@ -282,7 +354,7 @@ def run_gpu(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     peaks, peak_src = load_peaks()
     name = args.workload
-    reps_wanted = {"decode_8k": 8, "decode_8k_e4m3": 16}.get(name, 1)
+    reps_wanted = {"decode_8k": 8, "decode_8k_e4m3": 16, "cascade_64x4k": 4}.get(name, 1)
     w = workloads.NAMED[name](replicas=reps_wanted) if name != "tiny_mixed_f32" else workloads.NAMED[name]()
     common, reps = _device_replicas(w, device)
     e4m3 = w.kv_dtype == "e4m3"
@@ -296,6 +368,14 @@ def run_gpu(args, rank, world, local_rank):
     out = torch.empty_like(common["q"])
     flag = torch.zeros(1, dtype=torch.int32, device=device)
 
+    cascade = w.shared_blocks > 0
+    if cascade:
+        _cascade_tensors(w, reps, device)
+        csplits = pkv.pkv_cascade_splits(w.num_tokens, w.shared_blocks, hq, hkv, d,
+                                         common["q"].dtype, local_rank)
+        cws = torch.empty(pkv.pkv_cascade_workspace_bytes(w.num_tokens, hq, d, csplits),
+                          dtype=torch.uint8, device=device)
+
     def write(rep):
         if e4m3:
             pkv.pkv_write_e4m3(common["k_new"], common["v_new"], rep["slot_mapping"],
@@ -307,6 +387,13 @@ def run_gpu(args, rank, world, local_rank):
 
     def attend(rep):
         m = rep["meta"]
+        if cascade:
+            pkv.pkv_cascade_attention(
+                common["q"], common["k_cache"], common["v_cache"], out, rep["qsl"],
+                rep["suffix_lens"], rep["suffix_table"], rep["shared_table"], m["max_query_len"],
+                rep["max_suffix_len"], w.softmax_scale, prefix_splits=csplits, workspace=cws,
+                error_flag=flag)
+            return
         if e4m3:
             pkv.pkv_attention_varlen_e4m3(
                 common["q"], common["k_cache"], common["v_cache"], out, rep["qsl"],
@@ -416,7 +503,42 @@ def run_gpu(args, rank, world, local_rank):
     a1.record()
     torch.cuda.synchronize()
     att_ms = a0.elapsed_time(a1) / calls
-    if decode_like:
+    cascade_info = None
+    if cascade:
+        # the same batch through the plain call (full tables), and the bytes a
+        # cascade must read from HBM: the shared prefix once, every own part
+        def plain(i):
+            rep = reps[i % len(reps)]
+            mm = rep["meta"]
+            pkv.pkv_attention_varlen(common["q"], common["k_cache"], common["v_cache"], out,
+                                     rep["qsl"], rep["seq_lens"], rep["block_table"],
+                                     mm["max_query_len"], mm["max_seq_len"], w.softmax_scale,
+                                     num_splits=splits, workspace=workspace, error_flag=flag)
+        for i in range(20):
+            plain(i)
+        torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record()
+        for i in range(nat):
+            plain(i)
+        p1.record()
+        torch.cuda.synchronize()
+        plain_ms = p0.elapsed_time(p1) / nat
+        P = w.shared_blocks * w.block_size
+        unique = (P + sum(r.computed + r.scheduled - P for r in w.requests)) * hkv * d * 2 * esize
+        cascade_info = {"prefix_splits": csplits, "plain_call_ms": round(plain_ms, 6),
+                        "cascade_call_ms": round(att_ms, 6),
+                        "speedup_vs_plain": round(plain_ms / att_ms, 3),
+                        "unique_kv_bytes": unique,
+                        "logical_kv_bytes": bytes_step}
+    if decode_like and cascade:
+        # roofline on the bytes a cascade has to move (prefix once + own parts)
+        achieved = (cascade_info["unique_kv_bytes"] / 1e9) / (att_ms / 1e3)
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4)}
+        kernel_file = "decode.cu"
+    elif decode_like:
         achieved = (bytes_step / 1e9) / (att_ms / 1e3)
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -432,12 +554,18 @@ def run_gpu(args, rank, world, local_rank):
     roof["traffic"] = tr["bytes"] if tr else None
     roof["kernel"] = ("pkv_attention_varlen call (split-KV decode kernel + LSE combine), "
                       f"{splits} splits" if decode_like else "pkv_attention_varlen call (prefill)")
+    if cascade:
+        roof["kernel"] = (f"pkv_cascade_attention call (prefix pass, {csplits} splits; own-key "
+                          "pass; merge)")
     roof["peak_source"] = peak_src
     roof["ms_per_launch"] = round(att_ms, 6)
 
     # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, flops_step,
-                  decode_like)
+    if cascade:
+        e2e = run_e2e_cascade(args, w, reps, common, csplits, cws, flag, bytes_step)
+    else:
+        e2e = run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step,
+                      flops_step, decode_like)
 
     result = {
         "metric": METRIC, "value": round(value, 2),
@@ -453,11 +581,13 @@ def run_gpu(args, rank, world, local_rank):
                           "inputs larger than L2"),
                    "cuda_graph": use_graph, "parallelism": f"replicas x{world}"},
         "roofline": roof, "e2e": e2e,
-        "gpu_launches": _launches_per_step(splits, m0) * args.steps,
+        "gpu_launches": (4 if cascade else _launches_per_step(splits, m0)) * args.steps,
         "ms_per_step_p10_p50_p90": pct,
     }
     if name == "mixed_chunked":
         result["mixed_roofline"] = mixed_roofline(w, hq, hkv, d, esize, ms_step, peaks)
+    if cascade_info is not None:
+        result["cascade"] = cascade_info
     if clk is not None:
         result["clocks"] = clk
     return result, w

@@ -273,6 +273,77 @@ pkv_status pkv_attention_varlen_noalloc(const void* q, const void* k_cache, cons
                                         int causal, int num_splits, int32_t* error_flag,
                                         int64_t num_blocks, pkv_dtype dtype, void* stream);
 
+/*
+ * Shared-prefix (cascade) attention.
+ *
+ * "Anatomy of a serving engine", section "Capacity belongs to the KV cache
+ * manager": paged blocks let requests share the blocks of a common prefix.
+ * Here every request of the batch starts with the same shared_blocks blocks
+ * (P = 16 * shared_blocks keys, named by shared_block_table) followed by its
+ * own suffix_lens[r] keys (suffix_block_table row r); its context is
+ * L = P + suffix_lens[r] and its n new tokens are the last n of them, all in
+ * its own part (n <= suffix_lens[r], else PKV_FLAG_BAD_LENGTHS).  The result
+ * is that of pkv_attention_varlen (causal) with the table shared ++ own.
+ * It is computed as the key axis split in two ("Inside the engine ...",
+ * section "Prefill has a full grid; decode at batch 1 has almost none": a
+ * split of the keys changes nothing about the result): every row of the
+ * batch over the prefix at once (all prefix keys are visible to every new
+ * row; the prefix is read from HBM once for all requests, split
+ * prefix_splits ways over the key axis), each request over its own keys,
+ * and a log-sum-exp merge of the prefix_splits + 1 partials per row.  The
+ * prefix pass runs on the tensor cores for bf16, head_dim 128 and an even GQA
+ * group that divides 128 (each 128-row tile holds 128 / group tokens with
+ * their whole group, so one K/V tile feeds every head of the KV head) and a
+ * positive softmax_scale, else on the split-KV kernel's CUDA-core tiles; the
+ * own-key pass and the merge always run on CUDA cores.
+ */
+
+/* pkv_cascade_splits - prefix splits for num_tokens rows over shared_blocks
+ * blocks.  Tensor-core prefix pass (bf16, head_dim 128, even GQA group
+ * dividing 128): U = num_kv_heads x ceil(group x num_tokens / 256) row tiles,
+ * T = floor(7 x SMs / 8), min(max(1, floor(T / U)), ceil(shared_blocks / 8),
+ * 63) - each split at least one 128-key tile.  CUDA-core pass (otherwise):
+ * U = num_kv_heads x ceil(group x num_tokens / 16), T as for pkv_num_splits,
+ * min(max(1, floor(T / U)), shared_blocks / 8, 63).  0 when shared_blocks ==
+ * 0; -1 for invalid arguments or device. */
+int pkv_cascade_splits(int64_t num_tokens, int shared_blocks, int num_q_heads, int num_kv_heads,
+                       int head_dim, pkv_dtype dtype, int device);
+
+/* pkv_cascade_workspace_bytes - device workspace pkv_cascade_attention needs:
+ * fp32 partial outputs [prefix_splits + 1][num_tokens][num_q_heads][head_dim]
+ * and their log-sum-exps, each 256-byte aligned. */
+size_t pkv_cascade_workspace_bytes(int64_t num_tokens, int num_q_heads, int head_dim,
+                                   int prefix_splits);
+
+/*
+ * pkv_cascade_attention - attention of a batch sharing a block-aligned prefix.
+ *
+ *   q, out, lse_out, query_start_loc, num_seqs, num_tokens, max_query_len,
+ *   heads, head_dim, block_size, softmax_scale, error_flag, num_blocks,
+ *   dtype, stream: as pkv_attention_varlen.
+ *   suffix_lens         device int32 [num_seqs]: keys after the prefix.
+ *   suffix_block_table  device int32 [num_seqs, max_blocks_per_seq]: the
+ *                       blocks of those keys.
+ *   shared_block_table  device int32 [shared_blocks] (NULL when 0 blocks).
+ *   max_suffix_len      host, >= every suffix_lens[r].
+ *   prefix_splits       0 = pkv_cascade_splits(...); else 1..63.
+ *   workspace           device, >= pkv_cascade_workspace_bytes(num_tokens,
+ *                       num_q_heads, head_dim, splits), 256-byte aligned
+ *                       (splits = 0 when shared_blocks == 0).
+ * Rows of out past query_start_loc[num_seqs] are not written (the prefix
+ * pass reads every q row below num_tokens).
+ */
+pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void* v_cache,
+                                 void* out, float* lse_out, const int32_t* query_start_loc,
+                                 const int32_t* suffix_lens, const int32_t* suffix_block_table,
+                                 int max_blocks_per_seq, const int32_t* shared_block_table,
+                                 int shared_blocks, int num_seqs, int64_t num_tokens,
+                                 int max_query_len, int max_suffix_len, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 float softmax_scale, int prefix_splits, void* workspace,
+                                 size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+                                 pkv_dtype dtype, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* pkv_status_string(pkv_status status);
 

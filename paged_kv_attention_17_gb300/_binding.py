@@ -24,7 +24,8 @@ FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_num_splits", "pkv_workspace_bytes",
            "pkv_attention_varlen", "pkv_attention_varlen_window", "pkv_attention_varlen_e4m3",
-           "pkv_attention_varlen_noalloc", "pkv_status_string")
+           "pkv_attention_varlen_noalloc", "pkv_cascade_splits", "pkv_cascade_workspace_bytes",
+           "pkv_cascade_attention", "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -68,6 +69,14 @@ def lib() -> ctypes.CDLL:
                                                    i32, i32, i32, i32, i32, i32, ctypes.c_float,
                                                    i32, i32, vp, i64, i32, vp]
         L.pkv_attention_varlen_noalloc.restype = i32
+        L.pkv_cascade_splits.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+        L.pkv_cascade_splits.restype = i32
+        L.pkv_cascade_workspace_bytes.argtypes = [i64, i32, i32, i32]
+        L.pkv_cascade_workspace_bytes.restype = sz
+        L.pkv_cascade_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i64,
+                                            i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
+                                            i64, i32, vp]
+        L.pkv_cascade_attention.restype = i32
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -238,4 +247,50 @@ def pkv_attention_varlen_noalloc(q, k_cache, v_cache, out, query_start_loc, seq_
         float(softmax_scale), 1 if causal else 0, int(num_splits), _ptr(error_flag), int(nb),
         _dtype_code(q.dtype), _stream(stream))
     _check("pkv_attention_varlen_noalloc", code)
+    return out
+
+
+def pkv_cascade_splits(num_tokens, shared_blocks, num_q_heads, num_kv_heads, head_dim,
+                       dtype=torch.bfloat16, device=None) -> int:
+    dev = torch.cuda.current_device() if device is None else int(device)
+    return int(lib().pkv_cascade_splits(int(num_tokens), int(shared_blocks), int(num_q_heads),
+                                        int(num_kv_heads), int(head_dim), _dtype_code(dtype),
+                                        dev))
+
+
+def pkv_cascade_workspace_bytes(num_tokens, num_q_heads, head_dim, prefix_splits) -> int:
+    return int(lib().pkv_cascade_workspace_bytes(int(num_tokens), int(num_q_heads),
+                                                 int(head_dim), int(prefix_splits)))
+
+
+def pkv_cascade_attention(q, k_cache, v_cache, out, query_start_loc, suffix_lens,
+                          suffix_block_table, shared_block_table, max_query_len, max_suffix_len,
+                          softmax_scale, prefix_splits=0, workspace=None, lse_out=None,
+                          error_flag=None, stream=None):
+    """Attention of a batch whose requests share the blocks of
+    ``shared_block_table`` (int32 [shared_blocks]) as a prefix, each followed
+    by its own ``suffix_lens[r]`` keys in ``suffix_block_table`` row r.
+    ``workspace`` (uint8, >= pkv_cascade_workspace_bytes) is allocated here
+    if None."""
+    n_tok, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    num_seqs = int(suffix_lens.numel())
+    shared = int(shared_block_table.numel()) if shared_block_table is not None else 0
+    splits = int(prefix_splits)
+    if shared == 0:
+        splits = 0
+    elif splits == 0 and n_tok > 0:
+        splits = pkv_cascade_splits(n_tok, shared, hq, hkv, d, q.dtype, q.device.index)
+    need = pkv_cascade_workspace_bytes(n_tok, hq, d, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    code = lib().pkv_cascade_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
+        _ptr(suffix_lens), _ptr(suffix_block_table), int(suffix_block_table.shape[1]),
+        _ptr(shared_block_table) if shared else None, shared, num_seqs, int(n_tok),
+        int(max_query_len), int(max_suffix_len), int(hq), int(hkv), int(d), int(bs),
+        float(softmax_scale), splits, _ptr(workspace), int(ws_bytes), _ptr(error_flag), int(nb),
+        _dtype_code(q.dtype), _stream(stream))
+    _check("pkv_cascade_attention", code)
     return out

@@ -23,6 +23,7 @@ cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStr
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
 int decode_ctas_per_sm(int head_dim);
 bool prefill_supported(int head_dim, bool bf16, int group);
+bool prefill_packed_supported(int head_dim, bool bf16, int group);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t stream);
 }  // namespace pkv
@@ -33,6 +34,7 @@ namespace {
 
 constexpr int kMinBlocksPerSplit = 8;    // 128 keys
 constexpr int kTcMinWindow = 128;        // shortest window the tensor-core prefill takes
+constexpr int kCascadeRows = 16;         // rows per tile of the cascade prefix pass
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -102,14 +104,17 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_slots, int
 }
 
 // 3-D map over q viewed as [num_tokens, num_q_heads, head_dim]: a box is 128
-// tokens of one head, 64 columns wide (128 bytes, 128B swizzle).
-bool encode_q_map(CUtensorMap* map, const void* q, int64_t num_tokens, int hq, int d) {
+// tokens of one head (or, with heads_per_box = a GQA group, 128 / group tokens
+// of the group's heads), 64 columns wide (128 bytes, 128B swizzle).
+bool encode_q_map(CUtensorMap* map, const void* q, int64_t num_tokens, int hq, int d,
+                  int heads_per_box = 1) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hq),
                         static_cast<cuuint64_t>(num_tokens)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hq) * d * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(heads_per_box),
+                       static_cast<cuuint32_t>(128 / heads_per_box)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -379,6 +384,170 @@ pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const v
                    num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, k_scale,
                    v_scale, causal, 0, num_splits, workspace, workspace_bytes, error_flag,
                    num_blocks, ElemType::kE4m3, stream);
+}
+
+int pkv_cascade_splits(int64_t num_tokens, int shared_blocks, int num_q_heads, int num_kv_heads,
+                       int head_dim, pkv_dtype dtype, int device) {
+  if (num_tokens < 1 || shared_blocks < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+      num_q_heads % num_kv_heads != 0 || !valid_dtype(dtype))
+    return -1;
+  if (shared_blocks == 0) return 0;
+  const int sms = device_sms(device);
+  if (sms <= 0) return -1;
+  const int group = num_q_heads / num_kv_heads;
+  // tensor-core prefix pass: 256 (token, head) rows per CTA, splits of whole
+  // 128-key tiles; CUDA-core pass: 16-row tiles, splits of >= 8 blocks
+  const bool tc = prefill_packed_supported(head_dim, dtype == PKV_BF16, group);
+  const int rows = tc ? 256 : kCascadeRows;
+  const int64_t tiles = static_cast<int64_t>(num_kv_heads) * ((group * num_tokens + rows - 1) / rows);
+  const int64_t target =
+      static_cast<int64_t>(sms) * (tc ? 1 : decode_ctas_per_sm(head_dim)) * 7 / 8;
+  int64_t s = target / tiles;
+  int64_t by_len = tc ? (shared_blocks + 7) / 8 : shared_blocks / kMinBlocksPerSplit;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplits - 1) s = kMaxSplits - 1;        // + the own-key partial <= kMaxSplits
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
+size_t pkv_cascade_workspace_bytes(int64_t num_tokens, int num_q_heads, int head_dim,
+                                   int prefix_splits) {
+  if (num_tokens < 1 || num_q_heads < 1 || head_dim < 1 || prefix_splits < 0) return 0;
+  const size_t rows = static_cast<size_t>(prefix_splits + 1) * num_tokens * num_q_heads;
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void* v_cache,
+                                 void* out, float* lse_out, const int32_t* query_start_loc,
+                                 const int32_t* suffix_lens, const int32_t* suffix_block_table,
+                                 int max_blocks_per_seq, const int32_t* shared_block_table,
+                                 int shared_blocks, int num_seqs, int64_t num_tokens,
+                                 int max_query_len, int max_suffix_len, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 float softmax_scale, int prefix_splits, void* workspace,
+                                 size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+                                 pkv_dtype dtype, void* stream) {
+  if (!valid_dtype(dtype) || num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
+      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || shared_blocks < 0 ||
+      prefix_splits < 0 || prefix_splits > kMaxSplits - 1 || num_blocks < 1 ||
+      max_suffix_len < 0 || max_query_len < 0 || !std::isfinite(softmax_scale))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != kBlock || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
+  if (max_query_len < 1 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !out || !query_start_loc || !suffix_lens ||
+      !suffix_block_table || (shared_blocks > 0 && !shared_block_table))
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(query_start_loc, 4) || !aligned(suffix_lens, 4) ||
+      !aligned(suffix_block_table, 4) || (shared_block_table && !aligned(shared_block_table, 4)) ||
+      (lse_out && !aligned(lse_out, 4)) || (error_flag && !aligned(error_flag, 4)))
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65535 || num_tokens > 0x7FFFFFFFll) return PKV_ERR_UNSUPPORTED;
+  const int64_t num_slots = num_blocks * kBlock;
+  if (num_slots > 0x7FFFFFFFll || static_cast<int64_t>(shared_blocks) * kBlock > 0x7FFFFFFFll)
+    return PKV_ERR_UNSUPPORTED;
+  int S = prefix_splits;
+  if (shared_blocks == 0) {
+    S = 0;
+  } else if (S == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    S = pkv_cascade_splits(num_tokens, shared_blocks, num_q_heads, num_kv_heads, head_dim, dtype,
+                           dev);
+    if (S < 1) return PKV_ERR_CUDA;
+  }
+  const size_t need = pkv_cascade_workspace_bytes(num_tokens, num_q_heads, head_dim, S);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return PKV_ERR_WORKSPACE;
+  const ElemType et = dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32;
+  const size_t rows = static_cast<size_t>(S + 1) * num_tokens * num_q_heads;
+
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.out = out;
+  a.lse_out = lse_out;
+  a.qsl = query_start_loc;
+  a.num_seqs = num_seqs;
+  a.num_tokens = num_tokens;
+  a.hq = num_q_heads;
+  a.hkv = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.scale_log2 = softmax_scale * kLog2e;
+  a.v_scale = 1.f;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                      align256(rows * head_dim * sizeof(float)));
+  a.flag = error_flag;
+  a.num_blocks = num_blocks;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  CUtensorMap kmap, vmap;
+  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, false) ||
+      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, false))
+    return PKV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  // tensor cores for the prefix pass (bf16, head_dim 128, a GQA group that
+  // divides 128 rows, positive scale); the CUDA-core tiles otherwise
+  const bool tc = prefill_packed_supported(head_dim, dtype == PKV_BF16,
+                                           num_q_heads / num_kv_heads) &&
+                  softmax_scale > 0.f;
+  if (S > 0) {
+    // 1. every row over the shared prefix, split S ways: partials 0..S-1
+    AttnArgs p = a;
+    p.block_table = shared_block_table;
+    p.max_blocks_per_seq = shared_blocks;
+    p.num_seqs = 1;
+    p.max_query_len = static_cast<int>(num_tokens);
+    p.max_seq_len = shared_blocks * kBlock;
+    p.causal = 0;
+    p.num_splits = S;
+    p.long_rows = 1;
+    p.cascade = 1;
+    p.prefix_len = shared_blocks * kBlock;
+    if (tc) {
+      CUtensorMap qmap, kmap_sw, vmap_sw;
+      if (!encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, p.group) ||
+          !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
+          !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
+        return PKV_ERR_CUDA;
+      e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
+    } else {
+      e = launch_decode(p, kmap, vmap, et, head_dim, /*pdl=*/true, st);
+    }
+  }
+  if (e == cudaSuccess) {
+    // 2. each request over its own keys (causal): partial S
+    AttnArgs u = a;
+    u.seq_lens = suffix_lens;
+    u.block_table = suffix_block_table;
+    u.max_blocks_per_seq = max_blocks_per_seq;
+    u.num_seqs = num_seqs;
+    u.max_query_len = max_query_len;
+    u.max_seq_len = max_suffix_len;
+    u.causal = 1;
+    u.num_splits = 1;
+    u.long_rows = max_query_len > kDecodeMaxQ ? 1 : 0;
+    u.cascade = 2;
+    u.cascade_slot = S;
+    e = launch_decode(u, kmap, vmap, et, head_dim, /*pdl=*/true, st);
+  }
+  if (e == cudaSuccess) {
+    // 3. merge the S + 1 partials of every row
+    AttnArgs c = a;
+    c.num_splits = S + 1;
+    c.cascade = 3;
+    e = launch_combine(c, et, head_dim, st);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
 }
 
 }  // extern "C"

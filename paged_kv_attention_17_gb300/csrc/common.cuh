@@ -55,6 +55,14 @@ struct AttnArgs {
   int64_t num_blocks;
   const void* k_cache;    // cache bases, for L2 prefetch hints
   const void* v_cache;
+  // Shared-prefix (cascade) passes.  1: every row of the batch as one request
+  // over the prefix_len shared keys (non-causal), split partials to the
+  // workspace; 2: each request over its own keys, its result written as
+  // partial cascade_slot; 3: merge of num_splits partials per row.  Partials
+  // are indexed [slot][token][q head] in these passes.  0: a plain call.
+  int cascade;
+  int prefix_len;
+  int cascade_slot;
 };
 
 // ---------------------------------------------------------------------------

@@ -194,6 +194,14 @@ __device__ __forceinline__ int64_t ws_row(const AttnArgs& a, int s, int r, int i
   return ((static_cast<int64_t>(s) * a.num_seqs + r) * kDecodeMaxQ + i) * a.hq + h;
 }
 
+// Workspace row of a partial: by (split, request, decode row) in a plain call,
+// by (slot, flat token t) in the cascade passes.
+__device__ __forceinline__ int64_t part_row(const AttnArgs& a, int s, int r, int64_t t, int i,
+                                            int h) {
+  return a.cascade ? (static_cast<int64_t>(s) * a.num_tokens + t) * a.hq + h
+                   : ws_row(a, s, r, i, h);
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -251,7 +259,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   // their registers for the generic path
   constexpr bool kSpec = SPEC && R == 4;
   // whether this CTA may speculate (same answer on every thread)
-  const bool spec_possible = kSpec && a.num_splits > 1 && blockIdx.y == 0 && a.window == 0;
+  const bool spec_possible =
+      kSpec && a.num_splits > 1 && blockIdx.y == 0 && a.window == 0 && a.cascade == 0;
   constexpr int kPWarpFloats = kBlock * R * 2;        // p_s floats per warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -288,7 +297,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
   int32_t e_hint = 0;                  // producer lane w: hinted entry of warp w's first block
   bool hint_ok = false;
-  if (producer && z == 0 && a.window == 0) {
+  if (producer && z == 0 && a.window == 0 && a.cascade == 0) {
     // ---- L2 warm-up while the previous kernel finishes: the K/V blocks this
     //      CTA will most likely read (the split range a context of
     //      max_seq_len keys gives, cut at the request's length and at
@@ -378,19 +387,23 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     if (spec_v0) spec_e0 = ld_early(table + bb);
     if (spec_v1) spec_e1 = ld_early(table + bb + C::kWarps);
   }
-  const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
+  // cascade prefix pass: one request holding every row of the batch, over the
+  // prefix_len shared keys
+  const bool prefix_pass = a.cascade == 1;
+  const int q0 = prefix_pass ? 0 : __ldg(a.qsl + r);
+  const int q1 = prefix_pass ? static_cast<int>(a.num_tokens) : __ldg(a.qsl + r + 1);
   const int n = q1 - q0;
-  const int L = __ldg(a.seq_lens + r);
+  const int L = prefix_pass ? a.prefix_len : __ldg(a.seq_lens + r);
   if (n == 0) {
     drain_spec();
     return;
   }
-  if (n < 0 || q0 < 0 || q1 > a.num_tokens || n > L || n > a.max_query_len) {
+  if (n < 0 || q0 < 0 || q1 > a.num_tokens || (n > L && !prefix_pass) || n > a.max_query_len) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && z == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
     drain_spec();
     return;
   }
-  const bool decode_class = n <= kDecodeMaxQ;
+  const bool decode_class = n <= kDecodeMaxQ || prefix_pass;
   if (!decode_class && !a.long_rows) {                // the prefill kernel owns it
     drain_spec();
     return;
@@ -430,7 +443,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     // empty split: partial (o = 0, lse = -inf) so the combine weighs it 0
     for (int rho = warp; rho < nrows && warp < C::kWarps; rho += C::kWarps) {
       const int rr = rho0 + rho;
-      const int64_t w = ws_row(a, s, r, rr / group, g * group + rr % group);
+      const int64_t w = part_row(a, s, r, q0 + rr / group, rr / group, g * group + rr % group);
 #pragma unroll
       for (int e = 0; e < C::kDPL; ++e) a.ws_o[w * D + lane * C::kDPL + e] = 0.f;
       if (lane == 0) a.ws_lse[w] = -INFINITY;
@@ -970,8 +983,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     const int rr = rho0 + rho;
     const int i = rr / group;
     const int h = g * group + rr % group;
-    if (split_mode) {
-      const int64_t w = ws_row(a, s, r, i, h);
+    if (split_mode || a.cascade != 0) {
+      // a split partial, or a cascade partial (prefix split s, or the own-key
+      // slot of a request)
+      const int64_t w = part_row(a, a.cascade == 2 ? a.cascade_slot : s, r, q0 + i, i, h);
 #pragma unroll
       for (int e = 0; e < C::kDPL; ++e) a.ws_o[w * D + lane * C::kDPL + e] = o[e] * inv;
       if (lane == 0) a.ws_lse[w] = lse2;
@@ -1064,6 +1079,43 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
     a.lse_out[t * a.hq + h] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
 }
 
+// Cascade merge: row (token t, q head h) combines the num_splits partials
+// [slot][t][h] (prefix splits, then the request's own keys) by the same
+// log-sum-exp rule.  One warp per row, lanes over columns; every partial's
+// loads are issued before any is used.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) cascade_combine_kernel(const AttnArgs a) {
+  constexpr int kDPL = D / 32;
+  pdl_launch_dependents();
+  pdl_wait_primary();
+  const int lane = threadIdx.x & 31;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  // rows past query_start_loc[num_seqs] (padding) have no own-key partial
+  if (item >= a.num_tokens * a.hq || item / a.hq >= __ldg(a.qsl + a.num_seqs)) return;
+  const int S = a.num_splits;                          // <= kMaxSplits = 64
+  const int64_t stride = a.num_tokens * a.hq;          // rows per slot
+  const float l0 = lane < S ? a.ws_lse[lane * stride + item] : -INFINITY;
+  const float l1 = lane + 32 < S ? a.ws_lse[(lane + 32) * stride + item] : -INFINITY;
+  const float M = warp_max(fmaxf(l0, l1));
+  const float w0 = M == -INFINITY ? 0.f : ex2(l0 - M);
+  const float w1 = M == -INFINITY ? 0.f : ex2(l1 - M);
+  const float wsum = warp_sum(w0 + w1);
+  float o[kDPL];
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) o[e] = 0.f;
+  for (int sp = 0; sp < S; ++sp) {
+    const float f = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+    const float* src = a.ws_o + (sp * stride + item) * D + lane * kDPL;
+#pragma unroll
+    for (int e = 0; e < kDPL; ++e) o[e] = fmaf(f, src[e], o[e]);
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) store_elem<T>(a.out, item * D + lane * kDPL + e, o[e] * inv);
+  if (a.lse_out != nullptr && lane == 0)
+    a.lse_out[item] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
+}
+
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
@@ -1111,7 +1163,7 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
     case 4:
       // speculative first blocks only for split launches without a window
       // (their hinted block range ignores it)
-      return a.num_splits > 1 && a.window == 0
+      return a.num_splits > 1 && a.window == 0 && a.cascade == 0
                  ? launch_decode_t<T, D, 4, true>(a, kmap, vmap, row_tiles, pdl, stream)
                  : launch_decode_t<T, D, 4, false>(a, kmap, vmap, row_tiles, pdl, stream);
     case 8: return launch_decode_t<T, D, 8, false>(a, kmap, vmap, row_tiles, pdl, stream);
@@ -1179,7 +1231,10 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 
 // The combine writes out in the query's type: bf16 for bf16 and E4M3 caches.
 cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStream_t stream) {
-  const int64_t items = static_cast<int64_t>(a.num_seqs) * combine_rows(a.max_query_len) * a.hq;
+  const int64_t items = a.cascade == 3
+                            ? (a.num_tokens * a.hq + 3) / 4   // four rows per CTA
+                            : static_cast<int64_t>(a.num_seqs) * combine_rows(a.max_query_len) * a.hq;
+  if (items < 1 || items > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(items));
   cfg.blockDim = dim3(128);
@@ -1189,6 +1244,13 @@ cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.cascade == 3) {
+    if (et != ElemType::kF32)
+      return head_dim == 128 ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 128>, a)
+                             : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 64>, a);
+    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<float, 128>, a)
+                           : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<float, 64>, a);
+  }
   if (et != ElemType::kF32) {
     return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128>, a)
                            : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64>, a);

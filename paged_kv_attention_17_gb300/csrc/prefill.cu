@@ -25,6 +25,11 @@
 //     tcgen05.mma in a ping-pong order - P0 V(k), S0(k+1), P1 V(k), S1(k+1) - so
 //     one head's softmax overlaps the other head's MMAs; P.V takes P straight
 //     from TMEM as the A operand, V from shared memory (MN-major).
+// Shared-prefix (cascade) mode: the CTA's 256 rows are (token, query head)
+// pairs of one KV head - 256 / group tokens of the batch, each with its whole
+// GQA group, loaded by one TMA box per 128 rows - over one split of the
+// shared prefix's keys, unmasked (every row sits after the prefix); rows
+// write fp32 partials (o, log2-domain lse) to the workspace for the merge.
 // The running max is a lagged reference: a row moves it (and rescales its O
 // accumulator and l) only when a tile's max exceeds it by more than 8 log2
 // units, so every p = 2^(s - reference) stays at most 2^8 - far from overflow
@@ -212,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* misc = reinterpret_cast<int*>(smem + kOffMisc);   // [0] request, [1] tile, [2] tmem
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h0 = 2 * blockIdx.y;                         // query heads h0, h0 + 1 (same KV head)
+  const bool packed = a.cascade == 1;                    // shared-prefix mode
+  const int h0 = packed ? 0 : 2 * blockIdx.y;            // query heads h0, h0 + 1 (same KV head)
   const int tglob = blockIdx.x;
 
   pdl_wait_primary();
@@ -220,7 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- which (request, query tile) this CTA owns: warp 0 scans the long
   //      requests' tile counts (ceil(n / 128) for n > the decode bound) ----
-  if (warp == 0) {
+  if (packed) {
+    if (threadIdx.x == 0) {
+      misc[0] = 0;
+      misc[1] = tglob;
+    }
+  } else if (warp == 0) {
     int base = 0, found_r = -1, found_t = 0;
     for (int r0 = 0; r0 < a.num_seqs && found_r < 0; r0 += 32) {
       const int r = r0 + lane;
@@ -255,14 +266,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = misc[0];
   if (r < 0) return;                                     // past the last tile
   const int tile = misc[1];
-  const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
+  const int q0 = packed ? 0 : __ldg(a.qsl + r);
+  const int q1 = packed ? static_cast<int>(a.num_tokens) : __ldg(a.qsl + r + 1);
   const int n = q1 - q0;
-  const int L = __ldg(a.seq_lens + r);
-  if (q0 < 0 || q1 > a.num_tokens || n > L || n > a.max_query_len) {
+  const int L = packed ? a.prefix_len : __ldg(a.seq_lens + r);
+  if (q0 < 0 || q1 > a.num_tokens || (n > L && !packed) || n > a.max_query_len) {
     if (threadIdx.x == 0 && h0 == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
     return;
   }
-  const int g = h0 / a.group;
+  const int g = packed ? static_cast<int>(blockIdx.y) % a.hkv : h0 / a.group;
+  const int split = packed ? static_cast<int>(blockIdx.y) / a.hkv : 0;
+  const int tok_per_tile = kQRows / a.group;             // packed: tokens per 128-row tile
   const int i0 = tile * kQRows;
   const int i_hi = min(i0 + kQRows, n) - 1;              // last real row of the tile
   const int kv_len = a.causal ? (L - n + i_hi + 1) : L;
@@ -273,9 +287,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // sliding window: key tiles wholly below the first row's window start are
   // skipped; kt below counts the remaining tiles from kt_base
-  const int kt_base =
+  int kt_base =
       a.window > 0 ? max(0, L - n + i0 - a.window + 1) / kKeys : 0;
-  const int ntk = (kv_len + kKeys - 1) / kKeys - kt_base;
+  int ntk = (kv_len + kKeys - 1) / kKeys - kt_base;
+  if (packed) {
+    // this CTA's split of the prefix's key tiles
+    const int per = (ntk + a.num_splits - 1) / a.num_splits;
+    kt_base = min(split * per, ntk);
+    ntk = min(per, ntk - kt_base);
+    if (ntk <= 0) {
+      // an empty split: partial o = 0, lse = -inf for every row it owns
+      for (int rr = threadIdx.x; rr < 2 * kQRows; rr += kThreads) {
+        const int64_t rho = static_cast<int64_t>(tile) * 2 * kQRows + rr;
+        const int64_t tk = rho / a.group;
+        if (tk >= a.num_tokens) continue;
+        const int64_t w = (static_cast<int64_t>(split) * a.num_tokens + tk) * a.hq +
+                          g * a.group + rho % a.group;
+        for (int c = 0; c < 128; ++c) a.ws_o[w * 128 + c] = 0.f;
+        a.ws_lse[w] = -INFINITY;
+      }
+      return;
+    }
+  }
 
   // ---- barriers and TMEM ----
   if (threadIdx.x == 0) {
@@ -317,9 +350,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar_q, 4 * kHalf);
       const uint64_t pol_q = l2_policy_evict_first();
       for (int t = 0; t < 2; ++t)
-        for (int hh = 0; hh < 2; ++hh)
-          tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64, h0 + t,
-                      q0 + i0, pol_q);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (packed)   // 128 rows = tok_per_tile tokens x the GQA group of KV head g
+            tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64, g * a.group,
+                        (2 * tile + t) * tok_per_tile, pol_q);
+          else
+            tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64, h0 + t,
+                        q0 + i0, pol_q);
+        }
     }
     int kt = 0;
     for (; kt < ntk; ++kt) {
@@ -570,6 +608,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (packed) {
+        // row (token, head) of the 256-row pair: fp32 partial and log2 lse
+        const int64_t rho = (2 * static_cast<int64_t>(tile) + t) * kQRows + row;
+        const int64_t tk = rho / a.group;
+        const int64_t w = (static_cast<int64_t>(split) * a.num_tokens + tk) * a.hq +
+                          g * a.group + rho % a.group;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(t_o + c * 32, v);
+          if (tk < a.num_tokens) {
+            float4* dst = reinterpret_cast<float4*>(a.ws_o + w * 128 + c * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(v[4 * q] * inv, v[4 * q + 1] * inv, v[4 * q + 2] * inv,
+                                   v[4 * q + 3] * inv);
+          }
+        }
+        if (tk < a.num_tokens) a.ws_lse[w] = l > 0.f ? m + lg2f_(l) : -INFINITY;
+      } else {
       const bool store = i_r < n;
       __nv_bfloat16* orow =
           static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(q0 + i_r) * a.hq + h) * 128;
@@ -592,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (store && a.lse_out != nullptr)
         a.lse_out[static_cast<int64_t>(q0 + i_r) * a.hq + h] =
             l > 0.f ? (m + lg2f_(l)) * kLn2 : -INFINITY;
+      }
     }
     if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
   }
@@ -611,6 +670,11 @@ bool prefill_supported(int head_dim, bool bf16, int group) {
   return bf16 && head_dim == 128 && group % 2 == 0;
 }
 
+// Shared-prefix mode needs whole GQA groups in a 128-row tile.
+bool prefill_packed_supported(int head_dim, bool bf16, int group) {
+  return prefill_supported(head_dim, bf16, group) && kQRows % group == 0;
+}
+
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                            const CUtensorMap& vmap, cudaStream_t stream) {
   static unsigned done = 0;
@@ -624,13 +688,17 @@ cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUt
     if (dev < 32) done |= 1u << dev;
   }
   // upper bound on the long requests' query tiles: sum ceil(n / 128) <=
-  // ceil(N / 128) + (number of long requests)
+  // ceil(N / 128) + (number of long requests); shared-prefix mode: pairs of
+  // 128-row (token, head) tiles per KV head, times the prefix splits
   const int64_t long_reqs = std::min<int64_t>(a.num_seqs, a.num_tokens / (kDecodeMaxQ + 1));
-  const int64_t tiles = (a.num_tokens + kQRows - 1) / kQRows + long_reqs;
+  const int64_t tiles = a.cascade == 1
+                            ? (a.num_tokens * a.group + 2 * kQRows - 1) / (2 * kQRows)
+                            : (a.num_tokens + kQRows - 1) / kQRows + long_reqs;
+  const int64_t ys = a.cascade == 1 ? static_cast<int64_t>(a.hkv) * a.num_splits : a.hq / 2;
   if (tiles <= 0) return cudaSuccess;
-  if (tiles > 0x7FFFFFFF || a.hq / 2 > 65535) return cudaErrorInvalidConfiguration;
+  if (tiles > 0x7FFFFFFF || ys > 65535) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(a.hq / 2));
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(ys));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;

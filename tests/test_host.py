@@ -181,6 +181,52 @@ def test_write_e4m3_host_validation(pkv):
     assert L.pkv_write_e4m3(vp(16), vp(16), vp(16), 3, vp(16), vp(24), *ok) == 1
 
 
+def _cascade_call(pkv, **over):
+    L = pkv.lib()
+    args = dict(q=16, k=16, v=16, out=16, lse=0, qsl=16, sl=16, bt=16, mbps=4, shared=16,
+                shared_blocks=3, num_seqs=2, num_tokens=2, max_q=1, max_s=40, hq=8, hkv=2, d=128,
+                bs=16, scale=0.1, splits=2, ws=0, ws_bytes=0, flag=0, num_blocks=10, dtype=1,
+                stream=0)
+    args.update(over)
+    vp = lambda x: ctypes.c_void_p(x) if x else None
+    return L.pkv_cascade_attention(
+        vp(args["q"]), vp(args["k"]), vp(args["v"]), vp(args["out"]), vp(args["lse"]),
+        vp(args["qsl"]), vp(args["sl"]), vp(args["bt"]), args["mbps"], vp(args["shared"]),
+        args["shared_blocks"], args["num_seqs"], args["num_tokens"], args["max_q"], args["max_s"],
+        args["hq"], args["hkv"], args["d"], args["bs"], args["scale"], args["splits"],
+        vp(args["ws"]), args["ws_bytes"], vp(args["flag"]), args["num_blocks"], args["dtype"],
+        vp(args["stream"]))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(), 3),                       # no workspace for 2 prefix splits + own part
+    (dict(ws=4096, ws_bytes=64), 3),
+    (dict(splits=64), 1),              # at most 63 prefix splits
+    (dict(splits=-1), 1),
+    (dict(shared_blocks=-1), 1),
+    (dict(shared=0), 1),               # shared blocks named but no table
+    (dict(hq=6, hkv=4), 1),
+    (dict(d=96), 2),
+    (dict(bs=32), 2),
+    (dict(dtype=7), 1),
+    (dict(q=24), 1),
+    (dict(num_tokens=0), 0),
+])
+def test_cascade_host_validation(pkv, over, code):
+    assert _cascade_call(pkv, **over) == code
+
+
+def test_cascade_workspace_and_split_rule(pkv):
+    rows = 3 * 5 * 8
+    want = -(-(rows * 128 * 4) // 256) * 256 + -(-(rows * 4) // 256) * 256
+    assert pkv.pkv_cascade_workspace_bytes(5, 8, 128, 2) == want
+    L = pkv.lib()
+    assert L.pkv_cascade_splits(5, 0, 8, 2, 128, 1, 0) == 0   # no prefix: no prefix pass
+    assert L.pkv_cascade_splits(0, 4, 8, 2, 128, 1, 0) == -1
+    assert L.pkv_cascade_splits(5, 4, 6, 4, 128, 1, 0) == -1
+    assert L.pkv_cascade_splits(5, 4, 8, 2, 128, 7, 0) == -1  # unknown dtype
+
+
 def test_num_splits_rejects_bad_args(pkv):
     assert pkv.lib().pkv_num_splits(0, 1, 100, 32, 8, 128, 0) == 0
     assert pkv.lib().pkv_num_splits(1, 1, 100, 30, 8, 128, 0) == 0

@@ -157,20 +157,26 @@ def build(name: str, dtype: str, hq: int, hkv: int, d: int,
 
 def build_cascade(name: str, dtype: str, hq: int, hkv: int, d: int, shared_blocks: int,
                   shape: list[tuple[int, int]], seed: int = 0, spare_blocks: int = 3,
-                  rng: np.random.Generator | None = None) -> Workload:
+                  rng: np.random.Generator | None = None, replicas: int = 1) -> Workload:
     """Requests that share a prefix of ``shared_blocks`` blocks: each (c, s)
     pair is a request with c cached keys of its own after the prefix and s new
-    tokens; its table is the shared blocks followed by its own."""
+    tokens; its table is the shared blocks followed by its own.  Replicas
+    repeat the batch on disjoint blocks (a prefix of their own each)."""
     rng = rng if rng is not None else np.random.Generator(np.random.PCG64(seed))
     own = [_blocks_needed(c + s, BLOCK_SIZE) for c, s in shape]
-    num_blocks = shared_blocks + sum(own) + spare_blocks
+    per_rep = shared_blocks + sum(own)
+    num_blocks = per_rep * replicas + spare_blocks
     perm = rng.permutation(num_blocks)
-    shared = [int(b) for b in perm[:shared_blocks]]
-    reqs, start = [], shared_blocks
     P = shared_blocks * BLOCK_SIZE
-    for (c, s), nb in zip(shape, own):
-        reqs.append(Request(P + c, s, shared + [int(b) for b in perm[start:start + nb]]))
-        start += nb
+    reps, start = [], 0
+    for _ in range(replicas):
+        shared = [int(b) for b in perm[start:start + shared_blocks]]
+        start += shared_blocks
+        reqs = []
+        for (c, s), nb in zip(shape, own):
+            reqs.append(Request(P + c, s, shared + [int(b) for b in perm[start:start + nb]]))
+            start += nb
+        reps.append(reqs)
     n = sum(s for _, s in shape)
     pool_shape = (num_blocks, BLOCK_SIZE, hkv, d)
     k_pool, v_pool = _values(rng, pool_shape, dtype), _values(rng, pool_shape, dtype)
@@ -178,9 +184,18 @@ def build_cascade(name: str, dtype: str, hq: int, hkv: int, d: int, shared_block
     k_new = _values(rng, (n, hkv, d), dtype)
     v_new = _values(rng, (n, hkv, d), dtype)
     return Workload(name=name, dtype=dtype, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
-                    num_blocks=num_blocks, requests=reqs, q=q, k_new=k_new, v_new=v_new,
+                    num_blocks=num_blocks, requests=reps[0], q=q, k_new=k_new, v_new=v_new,
                     k_pool=k_pool, v_pool=v_pool, softmax_scale=float(1.0 / np.sqrt(d)),
-                    replicas=[reqs], shared_blocks=shared_blocks)
+                    replicas=reps, shared_blocks=shared_blocks)
+
+
+def cascade_64x4k(seed: int = 0, replicas: int = 1) -> Workload:
+    """bf16, GQA 32/8, D = 128: 64 decodes sharing a 4096-token prefix (256
+    blocks), each with U[0, 511] cached keys of its own and one new token."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    own = rng.integers(0, 512, size=64)
+    return build_cascade("cascade_64x4k", "bf16", 32, 8, 128, 256, [(int(c), 1) for c in own],
+                         rng=rng, replicas=replicas)
 
 
 # ---------------------------------------------------------------------------
@@ -242,6 +257,7 @@ NAMED = {
     "mixed_chunked": mixed_chunked,
     "prefill_8k": prefill_8k,
     "decode_8k_e4m3": decode_8k_e4m3,
+    "cascade_64x4k": cascade_64x4k,
 }
 
 
