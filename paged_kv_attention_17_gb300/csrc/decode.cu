@@ -1009,8 +1009,10 @@ __host__ __device__ __forceinline__ int combine_rows(int max_query_len) {
 // Log-sum-exp merge of the split partials: for each (request, decode row,
 // q head), M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s.
 // One CTA of 4 warps per row: warp w takes splits s = w, w + 4, ...; all of a
-// warp's partial loads are issued before any is used.
-template <typename T, int D>
+// warp's partial loads are issued before any is used.  CASCADE: rows are
+// (token, q head) of the batch and the partials the shared-prefix splits
+// followed by each request's own-key partial.
+template <typename T, int D, bool CASCADE>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   constexpr int kDPL = D / 32;
   __shared__ float red[4][D + 1];
@@ -1022,31 +1024,41 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   const int64_t item = blockIdx.x;
   const int h = static_cast<int>(item % a.hq);
   const int64_t ri = item / a.hq;
-  const int qrows = combine_rows(a.max_query_len);
-  const int i = static_cast<int>(ri % qrows);
-  const int r = static_cast<int>(ri / qrows);
+  const int qrows = CASCADE ? 1 : combine_rows(a.max_query_len);
+  const int i = CASCADE ? 0 : static_cast<int>(ri % qrows);
+  const int r = CASCADE ? 0 : static_cast<int>(ri / qrows);
   if (r >= a.num_seqs) return;
   const int S = a.num_splits;                          // <= kMaxSplits = 64
+  // workspace row of partial s: by (request, decode row), or by token
+  auto prow = [&](int sp) -> int64_t {
+    return CASCADE ? (static_cast<int64_t>(sp) * a.num_tokens + ri) * a.hq + h
+                   : ws_row(a, sp, r, i, h);
+  };
   // Partials are loaded before the row is known to exist (rows of requests
   // that are not decode-class hold stale data and are simply not stored), so
   // the metadata and workspace loads are in flight together.
-  const int q0 = __ldg(a.qsl + r), q1 = __ldg(a.qsl + r + 1);
-  const int L = __ldg(a.seq_lens + r);
-  const float l0 = lane < S ? a.ws_lse[ws_row(a, lane, r, i, h)] : -INFINITY;
-  const float l1 = lane + 32 < S ? a.ws_lse[ws_row(a, lane + 32, r, i, h)] : -INFINITY;
+  const int q0 = CASCADE ? static_cast<int>(ri) : __ldg(a.qsl + r);
+  const int q1 = CASCADE ? __ldg(a.qsl + a.num_seqs) : __ldg(a.qsl + r + 1);
+  const int L = CASCADE ? 1 : __ldg(a.seq_lens + r);
+  const float l0 = lane < S ? a.ws_lse[prow(lane)] : -INFINITY;
+  const float l1 = lane + 32 < S ? a.ws_lse[prow(lane + 32)] : -INFINITY;
   constexpr int kMaxPer = kMaxSplits / 4;
   float part[kMaxPer][kDPL];
 #pragma unroll
   for (int u = 0; u < kMaxPer; ++u) {
     const int sp = warp + 4 * u;
     if (sp < S) {
-      const float* src = a.ws_o + ws_row(a, sp, r, i, h) * D + lane * kDPL;
+      const float* src = a.ws_o + prow(sp) * D + lane * kDPL;
 #pragma unroll
       for (int e = 0; e < kDPL; ++e) part[u][e] = src[e];
     }
   }
-  const int n = q1 - q0;
-  if (n <= 0 || n > kDecodeMaxQ || i >= n || q0 < 0 || q1 > a.num_tokens || n > L) return;
+  if (CASCADE) {
+    if (q0 >= q1) return;                              // padding rows: no own-key partial
+  } else {
+    const int n = q1 - q0;
+    if (n <= 0 || n > kDecodeMaxQ || i >= n || q0 < 0 || q1 > a.num_tokens || n > L) return;
+  }
   float M = warp_max(fmaxf(l0, l1));
   const float w0 = M == -INFINITY ? 0.f : ex2(l0 - M);
   const float w1 = M == -INFINITY ? 0.f : ex2(l1 - M);
@@ -1068,7 +1080,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   __syncthreads();
   if (warp != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const int64_t t = q0 + i;
+  const int64_t t = CASCADE ? ri : q0 + i;
 #pragma unroll
   for (int e = 0; e < kDPL; ++e) {
     const int col = lane * kDPL + e;
@@ -1077,43 +1089,6 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   }
   if (a.lse_out != nullptr && lane == 0)
     a.lse_out[t * a.hq + h] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
-}
-
-// Cascade merge: row (token t, q head h) combines the num_splits partials
-// [slot][t][h] (prefix splits, then the request's own keys) by the same
-// log-sum-exp rule.  One warp per row, lanes over columns; every partial's
-// loads are issued before any is used.
-template <typename T, int D>
-__global__ void __launch_bounds__(128) cascade_combine_kernel(const AttnArgs a) {
-  constexpr int kDPL = D / 32;
-  pdl_launch_dependents();
-  pdl_wait_primary();
-  const int lane = threadIdx.x & 31;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  // rows past query_start_loc[num_seqs] (padding) have no own-key partial
-  if (item >= a.num_tokens * a.hq || item / a.hq >= __ldg(a.qsl + a.num_seqs)) return;
-  const int S = a.num_splits;                          // <= kMaxSplits = 64
-  const int64_t stride = a.num_tokens * a.hq;          // rows per slot
-  const float l0 = lane < S ? a.ws_lse[lane * stride + item] : -INFINITY;
-  const float l1 = lane + 32 < S ? a.ws_lse[(lane + 32) * stride + item] : -INFINITY;
-  const float M = warp_max(fmaxf(l0, l1));
-  const float w0 = M == -INFINITY ? 0.f : ex2(l0 - M);
-  const float w1 = M == -INFINITY ? 0.f : ex2(l1 - M);
-  const float wsum = warp_sum(w0 + w1);
-  float o[kDPL];
-#pragma unroll
-  for (int e = 0; e < kDPL; ++e) o[e] = 0.f;
-  for (int sp = 0; sp < S; ++sp) {
-    const float f = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
-    const float* src = a.ws_o + (sp * stride + item) * D + lane * kDPL;
-#pragma unroll
-    for (int e = 0; e < kDPL; ++e) o[e] = fmaf(f, src[e], o[e]);
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-  for (int e = 0; e < kDPL; ++e) store_elem<T>(a.out, item * D + lane * kDPL + e, o[e] * inv);
-  if (a.lse_out != nullptr && lane == 0)
-    a.lse_out[item] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------
@@ -1232,7 +1207,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 // The combine writes out in the query's type: bf16 for bf16 and E4M3 caches.
 cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStream_t stream) {
   const int64_t items = a.cascade == 3
-                            ? (a.num_tokens * a.hq + 3) / 4   // four rows per CTA
+                            ? a.num_tokens * a.hq
                             : static_cast<int64_t>(a.num_seqs) * combine_rows(a.max_query_len) * a.hq;
   if (items < 1 || items > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -1246,17 +1221,17 @@ cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStr
   cfg.numAttrs = 1;
   if (a.cascade == 3) {
     if (et != ElemType::kF32)
-      return head_dim == 128 ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 128>, a)
-                             : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 64>, a);
-    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<float, 128>, a)
-                           : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<float, 64>, a);
+      return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128, true>, a)
+                             : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64, true>, a);
+    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 128, true>, a)
+                           : cudaLaunchKernelEx(&cfg, combine_kernel<float, 64, true>, a);
   }
   if (et != ElemType::kF32) {
-    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128>, a)
-                           : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64>, a);
+    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128, false>, a)
+                           : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64, false>, a);
   }
-  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 128>, a)
-                         : cudaLaunchKernelEx(&cfg, combine_kernel<float, 64>, a);
+  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 128, false>, a)
+                         : cudaLaunchKernelEx(&cfg, combine_kernel<float, 64, false>, a);
 }
 
 }  // namespace pkv
