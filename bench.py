@@ -45,6 +45,8 @@ WORKLOAD_TEXT = {
     "cascade_64x4k": "64 decodes sharing a 4096-token prefix (256 blocks), U[0,511] own cached "
                      "keys + 1 new token each, GQA 32/8, head_dim 128, bf16; shared-prefix "
                      "(cascade) attention, 4 replicas of 84 MB",
+    "batched_decode_64_e4m3": "batched_decode_64 over an 8-bit E4M3 KV cache (k_scale = "
+                              "v_scale = 0.5; q, new K/V and out bf16)",
     "decode_8k_e4m3": "decode_8k over an 8-bit E4M3 KV cache (k_scale = v_scale = 0.5; q, new "
                       "K/V and out bf16): 512-block table from a shuffled 8192-block pool",
 }

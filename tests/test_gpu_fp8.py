@@ -154,6 +154,16 @@ def test_decode_8k_full_size_bench_configuration():
     _check_lse(lse, lse_ref)
 
 
+def test_batched_decode_64_full_size():
+    w = workloads.batched_decode_64_e4m3()
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref)
+    _check_lse(lse, lse_ref)
+
+
 def test_matches_the_bf16_path_on_the_dequantised_cache():
     # the same step through the bf16 kernels on a cache holding scale * value
     # (exact in bf16: 4 significant bits times a power of two).  Decode rows

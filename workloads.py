@@ -240,6 +240,14 @@ def prefill_8k(seed: int = 0, replicas: int = 1) -> Workload:
     return build("prefill_8k", "bf16", 32, 8, 128, [(0, 8192)], seed=seed, replicas=replicas)
 
 
+def batched_decode_64_e4m3(seed: int = 0, replicas: int = 1) -> Workload:
+    """batched_decode_64 over an 8-bit E4M3 cache (k_scale = v_scale = 0.5)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = rng.integers(512, 4096 + 1, size=64)
+    return build("batched_decode_64_e4m3", "bf16", 32, 8, 128, [(int(c) - 1, 1) for c in ctx],
+                 replicas=replicas, rng=rng, kv_dtype="e4m3", k_scale=0.5, v_scale=0.5)
+
+
 def decode_8k_e4m3(seed: int = 0, replicas: int = 1) -> Workload:
     """decode_8k over an 8-bit E4M3 cache (codes of magnitude 1/8 .. 3.75,
     k_scale = v_scale = 0.5): half the cache bytes per key, so the shuffled
@@ -257,6 +265,7 @@ NAMED = {
     "mixed_chunked": mixed_chunked,
     "prefill_8k": prefill_8k,
     "decode_8k_e4m3": decode_8k_e4m3,
+    "batched_decode_64_e4m3": batched_decode_64_e4m3,
     "cascade_64x4k": cascade_64x4k,
 }
 
