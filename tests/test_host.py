@@ -120,6 +120,8 @@ def _attn_call(pkv, **over):
     (dict(scale=float("nan")), 1),
     (dict(num_tokens=0), 0),           # empty batch: no-op
     (dict(num_seqs=0), 0),
+    (dict(num_seqs=65536), 2),         # beyond the request grid
+    (dict(num_blocks=1 << 27), 2),     # 2^31 slots: beyond int32 TMA coordinates
 ])
 def test_attention_host_validation(pkv, over, code):
     assert _attn_call(pkv, **over) == code
