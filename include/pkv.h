@@ -33,7 +33,16 @@
  *     slot = block_id * block_size + offset.
  *   - Supported: block_size 16; head_dim 64 or 128; num_q_heads a multiple of
  *     num_kv_heads; dtype PKV_F32 or PKV_BF16 (same dtype for Q, K, V and
- *     the output).  Arithmetic is fp32 with fp32 accumulation.
+ *     the output), or an 8-bit E4M3 cache with bf16 Q and output through the
+ *     _e4m3 entry points.  Arithmetic is fp32 with fp32 accumulation (the
+ *     tensor-core prefill rounds P to bf16 for its P.V product).
+ *
+ * Entry points: pkv_write / pkv_write_e4m3 (slot-mapped write), pkv_num_splits
+ * and pkv_workspace_bytes (split-KV sizing), pkv_attention_varlen and its
+ * variants _window (sliding window), _e4m3 (8-bit cache) and _noalloc (no
+ * caller workspace), pkv_cascade_splits / pkv_cascade_workspace_bytes /
+ * pkv_cascade_attention (requests sharing a block-aligned prefix), and
+ * pkv_status_string.
  */
 #ifndef PKV_H
 #define PKV_H
