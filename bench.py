@@ -408,8 +408,24 @@ def run_gpu(args, rank, world, local_rank):
                                  m["max_seq_len"], w.softmax_scale, causal=w.causal,
                                  num_splits=splits, workspace=workspace, error_flag=flag)
 
+    # decode-class steps over a bf16/fp32 cache: the write rides in the decode
+    # kernel (pkv_write_attention_varlen)
+    fused = m0["max_query_len"] <= 4 and not e4m3 and not cascade
+
+    def fused_step(rep):
+        m = rep["meta"]
+        pkv.pkv_write_attention_varlen(common["k_new"], common["v_new"], rep["slot_mapping"],
+                                       common["q"], common["k_cache"], common["v_cache"], out,
+                                       rep["qsl"], rep["seq_lens"], rep["block_table"],
+                                       m["max_query_len"], m["max_seq_len"], w.softmax_scale,
+                                       causal=w.causal, num_splits=splits, workspace=workspace,
+                                       error_flag=flag)
+
     def step(i):
         rep = reps[i % len(reps)]
+        if fused:
+            fused_step(rep)
+            return
         write(rep)
         attend(rep)
 
@@ -577,13 +593,16 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic: seeded N(0,1) PCG64(0), cast to bf16 (RNE)" + (
             "; cache codes drawn as E4M3 bit fields (exponent 4..8)" if e4m3 else ""),
         "config": {"workload": f"{name}: {WORKLOAD_TEXT[name]}", "num_splits": splits,
+                   "step": ("pkv_write_attention_varlen (write fused into the decode kernel)"
+                            if fused else "pkv_write + attention call"),
                    "kv_bytes_per_step": bytes_step, "flops_per_step": flops_step,
                    "l2": (f"cold: steps rotate over {len(reps)} disjoint 512-block tables of a "
                           "268 MB pool" if name.startswith("decode_8k") else
                           "inputs larger than L2"),
                    "cuda_graph": use_graph, "parallelism": f"replicas x{world}"},
         "roofline": roof, "e2e": e2e,
-        "gpu_launches": (4 if cascade else _launches_per_step(splits, m0)) * args.steps,
+        "gpu_launches": (4 if cascade else _launches_per_step(splits, m0) - (1 if fused else 0))
+                        * args.steps,
         "ms_per_step_p10_p50_p90": pct,
     }
     if name == "mixed_chunked":

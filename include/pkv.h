@@ -201,6 +201,32 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
                                 int64_t num_blocks, pkv_dtype dtype, void* stream);
 
 /*
+ * pkv_write_attention_varlen - pkv_write then pkv_attention_varlen, as one
+ * call.
+ *
+ * The same two steps ("Model execution", section "Flattening a step": the
+ * new tokens' K/V go to their slots, then attention reads the cache).  When
+ * every request is decode-class (max_query_len <= PKV_DECODE_MAX_QLEN) the
+ * write rides in the decode kernel: each CTA stores the new-token rows it is
+ * about to read (a bounded barrier orders the stores before its TMA loads of
+ * them), so the step is one launch fewer.  Otherwise pkv_write runs first.
+ *   k_new, v_new, slot_mapping: as pkv_write (q's dtype).  The other
+ *   arguments as pkv_attention_varlen.  On the fused path only the tokens of
+ *   rows below query_start_loc[num_seqs] are stored (padding rows carry slot
+ *   -1 anyway); a slot past the cache is skipped and flagged
+ *   PKV_FLAG_BAD_SLOT.  The cache contents after the call are those of the
+ *   two separate calls.
+ */
+pkv_status pkv_write_attention_varlen(
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
+    void* k_cache, void* v_cache, void* out, float* lse_out, const int32_t* query_start_loc,
+    const int32_t* seq_lens, const int32_t* block_table, int max_blocks_per_seq, int num_seqs,
+    int64_t num_tokens, int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, float softmax_scale, int causal, int num_splits,
+    void* workspace, size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+    pkv_dtype dtype, void* stream);
+
+/*
  * pkv_attention_varlen_window - pkv_attention_varlen with a sliding window.
  *
  * "Anatomy of a serving engine", section "Where it breaks": sliding-window

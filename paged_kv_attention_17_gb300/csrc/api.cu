@@ -134,7 +134,9 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
                             int head_dim, int block_size, float softmax_scale, float k_scale,
                             float v_scale, int causal, int window, int num_splits,
                             void* workspace, size_t workspace_bytes, int32_t* error_flag,
-                            int64_t num_blocks, ElemType et, void* stream) {
+                            int64_t num_blocks, ElemType et, void* stream,
+                            const void* fuse_k_new = nullptr, const void* fuse_v_new = nullptr,
+                            const int64_t* fuse_slots = nullptr) {
   // ---- host-checkable arguments ----
   if (window < 0 || num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
       num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_splits < 0 ||
@@ -213,6 +215,14 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
   a.num_blocks = num_blocks;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
+  if (fuse_slots != nullptr) {
+    // the step's new K/V are stored by the decode kernel (every request is
+    // decode-class, checked by the caller)
+    a.fuse_write = 1;
+    a.k_new = fuse_k_new;
+    a.v_new = fuse_v_new;
+    a.slots = fuse_slots;
+  }
 
   CUtensorMap kmap, vmap;
   if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, false) ||
@@ -349,6 +359,39 @@ pkv_status pkv_attention_varlen(const void* q, const void* k_cache, const void* 
                    num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, 1.f, 1.f,
                    causal, 0, num_splits, workspace, workspace_bytes, error_flag, num_blocks,
                    dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32, stream);
+}
+
+pkv_status pkv_write_attention_varlen(
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
+    void* k_cache, void* v_cache, void* out, float* lse_out, const int32_t* query_start_loc,
+    const int32_t* seq_lens, const int32_t* block_table, int max_blocks_per_seq, int num_seqs,
+    int64_t num_tokens, int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, float softmax_scale, int causal, int num_splits,
+    void* workspace, size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+    pkv_dtype dtype, void* stream) {
+  if (!valid_dtype(dtype)) return PKV_ERR_INVALID_ARG;
+  if (num_tokens > 0 && num_seqs > 0) {
+    if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
+      return PKV_ERR_INVALID_ARG;
+  }
+  const ElemType et = dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32;
+  if (max_query_len <= kDecodeMaxQ) {
+    // every request decode-class: the write rides in the decode kernel
+    return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                     max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                     num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, 1.f, 1.f,
+                     causal, 0, num_splits, workspace, workspace_bytes, error_flag, num_blocks,
+                     et, stream, k_new, v_new, slot_mapping);
+  }
+  pkv_status st = pkv_write(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache, num_blocks,
+                            block_size, num_kv_heads, head_dim, dtype, error_flag, stream);
+  if (st != PKV_OK) return st;
+  return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                   max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                   num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, 1.f, 1.f,
+                   causal, 0, num_splits, workspace, workspace_bytes, error_flag, num_blocks, et,
+                   stream);
 }
 
 pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const void* v_cache,

@@ -63,6 +63,12 @@ struct AttnArgs {
   int cascade;
   int prefix_len;
   int cascade_slot;
+  // Fused write (decode-class steps): each CTA stores the K/V rows (its KV
+  // head) of the new tokens whose positions it reads, before loading them.
+  int fuse_write;
+  const void* k_new;      // [num_tokens, hkv, D], the cache's element type
+  const void* v_new;
+  const int64_t* slots;   // slot_mapping
 };
 
 // ---------------------------------------------------------------------------

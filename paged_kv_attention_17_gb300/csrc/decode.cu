@@ -153,7 +153,9 @@ struct DecodeSmem {
   // kfull[], vfull[], empty[], then per consumer warp the barrier and the
   // verdict of its speculative first block
   static constexpr int kSpecOff = kBarOff + 3 * C::kStages * 8;
-  static constexpr int kBytes = kSpecOff + C::kWarps * 8 + C::kWarps * 4;
+  // then the barrier of the fused KV write
+  static constexpr int kWrOff = kSpecOff + C::kWarps * 8 + (C::kWarps * 4 + 7) / 8 * 8;
+  static constexpr int kBytes = kWrOff + 8;
   static constexpr int kAlloc = kBytes + 1024;            // slack to align the base to 1 KB
 };
 
@@ -204,6 +206,11 @@ __device__ __forceinline__ int64_t part_row(const AttnArgs& a, int s, int r, int
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// this thread's generic-proxy global stores before its later async-proxy (TMA) reads
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // V columns lane*kDPL .. +kDPL-1 of one cached row, as fp32 pairs.
@@ -272,6 +279,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   uint64_t* empty = vfull + C::kStages;                                 // stage released
   uint64_t* spec_bar = reinterpret_cast<uint64_t*>(smem + Sm::kSpecOff);
   int* spec_state = reinterpret_cast<int*>(spec_bar + C::kWarps);
+  uint64_t* wr_bar = reinterpret_cast<uint64_t*>(smem + Sm::kWrOff);   // fused write stored
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool producer = warp == C::kWarps;
@@ -289,6 +297,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       mbar_init(&kfull[i], 1);
       mbar_init(&vfull[i], 1);
       if (i < C::kWarps) mbar_init(&spec_bar[i], 1);
+      if (i == 0) mbar_init(wr_bar, 1);
       mbar_init(&empty[i], 1);
     }
     fence_mbar_init();
@@ -452,6 +461,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     return;
   }
   const int key_end = min(kv_len, b1 * kBlock);       // keys of this split: [b0*16, key_end)
+  // fused write: the new-token rows this CTA reads, positions [fw_lo, fw_hi)
+  // (head g); consumer warp 0 stores them, and the producer issues a block
+  // holding one only after that (wr_bar)
+  const int fw_lo = a.fuse_write ? max(L - n, b0 * kBlock) : 0;
+  const int fw_hi = a.fuse_write ? key_end : 0;
   const int nt = b1 - b0;                              // one block per stage
   const int my_tiles = nt > warp ? (nt - warp + C::kWarps - 1) / C::kWarps : 0;
 
@@ -522,9 +536,14 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       return jj < tiles ? ld_early(table + b0 + w + C::kWarps * jj) : 0;
     };
     const bool spec_ok = spec_b0 == b0;
+    // a speculative first block holding new-token rows of a fused write was
+    // loaded before they were stored: discard it
+    const int sb = b0 + w;
+    const bool spec_clash = fw_lo < fw_hi && sb * kBlock < fw_hi && (sb + 1) * kBlock > fw_lo;
     // verdict on the speculative first block: 0 none, 1 used as tile 0,
     // 2 wasted (stage 0's phases then run one ahead of its tiles)
-    const bool used = spec_issued && spec_ok && tiles > 0 && spec_v0 && spec_e0 == e_hint;
+    const bool used = spec_issued && spec_ok && tiles > 0 && spec_v0 && spec_e0 == e_hint &&
+                      !spec_clash;
     const int verdict = !spec_issued ? 0 : (used ? 1 : 2);
     if (verdict == 2) {
       // a wasted fill lands before the verdict is published (the consumer's
@@ -556,6 +575,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
         // a wasted speculative fill must land before stage 0 is filled again
         if (ready && jj == 0 && shift0)
           ready = mbar_ready(&kfull[st], 0) && mbar_ready(&vfull[st], 0);
+        // a block holding rows of the fused write only once they are stored
+        if (ready && fw_lo < fw_hi) {
+          const int bi = b0 + w + C::kWarps * jj;
+          if (bi * kBlock < fw_hi && (bi + 1) * kBlock > fw_lo) ready = mbar_ready(wr_bar, 0);
+        }
         if (ready) {
           int id = e_cur;
           if (id < 0 || id >= a.num_blocks) {
@@ -637,6 +661,36 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
         if (e < R * D) q_s[q_index<T, D>(e / D, e % D)] = static_cast<float>(qraw[u]) * a.scale_log2;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(C::kConsumerThreads) : "memory");
+    }
+    // ---- fused write (warp 0): the K/V rows of head g of the new tokens this
+    //      CTA reads; every CTA reading a row stores the same bytes first ----
+    if (fw_lo < fw_hi && warp == 0) {
+      constexpr int kChunks = C::kRowBytes / 16;             // 16-byte chunks of a row
+      const int p_first = L - n;
+      const int count = (fw_hi - fw_lo) * 2 * kChunks;
+      const int64_t num_slots = a.num_blocks * kBlock;
+      for (int c = lane; c < count; c += 32) {
+        const int64_t t = q0 + (fw_lo - p_first) + c / (2 * kChunks);
+        const int part = (c / kChunks) & 1;                  // 0: K, 1: V
+        const int ch = c % kChunks;
+        const int64_t slot = __ldg(a.slots + t);
+        if (slot < 0) continue;                              // padding: nothing stored
+        if (slot >= num_slots) {
+          raise_flag(a.flag, PKV_FLAG_BAD_SLOT);
+          continue;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(
+                               static_cast<const uint8_t*>(part ? a.v_new : a.k_new) +
+                               (t * a.hkv + g) * C::kRowBytes) + ch;
+        uint4* dst = reinterpret_cast<uint4*>(
+                         static_cast<uint8_t*>(const_cast<void*>(part ? a.v_cache : a.k_cache)) +
+                         (slot * a.hkv + g) * C::kRowBytes) + ch;
+        *dst = __ldg(src);
+      }
+      // the stores before the producer's TMA (async proxy) loads of them
+      fence_proxy_async_global();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(wr_bar);
     }
     // the producer's verdict on this warp's speculative first block
     int shift0 = 0;

@@ -12,8 +12,8 @@ buckets and keeps a static memory pool.
 one graph holding a whole decode step on static buffers:
 
 1. the copy of the step's packed inputs from pinned host memory to the device,
-2. ``pkv_write`` of the new tokens' K/V,
-3. ``pkv_attention_varlen`` (one query token per request),
+2.-3. ``pkv_write_attention_varlen``: the new tokens' K/V stored by the decode
+   kernel itself, then attention (one query token per request),
 
 (``pkv_write_e4m3`` and ``pkv_attention_varlen_e4m3`` over an 8-bit E4M3 cache),
 4. the copy of the output rows (and the error flag) back to pinned host memory.
@@ -207,13 +207,12 @@ class DecodeGraphRunner:
                                         num_splits=self.splits[b], workspace=self.workspace,
                                         error_flag=self.flag)
         else:
-            B.pkv_write(v["k_new"], v["v_new"], v["slot_mapping"], self.k_cache, self.v_cache,
-                        error_flag=self.flag)
-            B.pkv_attention_varlen(v["q"], self.k_cache, self.v_cache, out,
-                                   v["query_start_loc"], v["seq_lens"], v["block_table"], 1,
-                                   self.max_seq_len, self.scale, causal=True,
-                                   num_splits=self.splits[b], workspace=self.workspace,
-                                   error_flag=self.flag)
+            # one token per request: the write rides in the decode kernel
+            B.pkv_write_attention_varlen(v["k_new"], v["v_new"], v["slot_mapping"], v["q"],
+                                         self.k_cache, self.v_cache, out, v["query_start_loc"],
+                                         v["seq_lens"], v["block_table"], 1, self.max_seq_len,
+                                         self.scale, causal=True, num_splits=self.splits[b],
+                                         workspace=self.workspace, error_flag=self.flag)
         if not self.zero_copy:
             self.host_out[slot][:b].copy_(self.out[:b], non_blocking=True)
             self.host_flag[slot].copy_(self.flag, non_blocking=True)

@@ -46,6 +46,22 @@ def device_inputs(w, device="cuda", requests=None) -> dict:
     return d
 
 
+def run_fused_step(d, num_splits=0, with_lse=True, causal=None, flag=None):
+    """pkv_write_attention_varlen of the step.  Returns (out, lse, flag)."""
+    w, meta = d["w"], d["meta"]
+    dev = d["q"].device
+    if flag is None:
+        flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev) if with_lse else None
+    pkv.pkv_write_attention_varlen(d["k_new"], d["v_new"], d["slot_mapping"], d["q"],
+                                   d["k_cache"], d["v_cache"], out, d["qsl"], d["seq_lens"],
+                                   d["block_table"], meta["max_query_len"], meta["max_seq_len"],
+                                   w.softmax_scale, causal=w.causal if causal is None else causal,
+                                   num_splits=num_splits, lse_out=lse, error_flag=flag)
+    return out, lse, flag
+
+
 def run_step(d, num_splits=0, write=True, with_lse=True, causal=None, workspace=None,
              flag=None, out=None):
     """pkv_write of the new tokens, then pkv_attention_varlen (their E4M3 forms
