@@ -408,12 +408,20 @@ def run_gpu(args, rank, world, local_rank):
                                  m["max_seq_len"], w.softmax_scale, causal=w.causal,
                                  num_splits=splits, workspace=workspace, error_flag=flag)
 
-    # decode-class steps over a bf16/fp32 cache: the write rides in the decode
-    # kernel (pkv_write_attention_varlen)
-    fused = m0["max_query_len"] <= 4 and not e4m3 and not cascade
+    # decode-class steps: the write rides in the decode kernel
+    # (pkv_write_attention_varlen, and its E4M3 form)
+    fused = m0["max_query_len"] <= 4 and not cascade
 
     def fused_step(rep):
         m = rep["meta"]
+        if e4m3:
+            pkv.pkv_write_attention_varlen_e4m3(
+                common["k_new"], common["v_new"], rep["slot_mapping"], common["q"],
+                common["k_cache"], common["v_cache"], out, rep["qsl"], rep["seq_lens"],
+                rep["block_table"], m["max_query_len"], m["max_seq_len"], w.softmax_scale,
+                w.k_scale, w.v_scale, causal=w.causal, num_splits=splits, workspace=workspace,
+                error_flag=flag)
+            return
         pkv.pkv_write_attention_varlen(common["k_new"], common["v_new"], rep["slot_mapping"],
                                        common["q"], common["k_cache"], common["v_cache"], out,
                                        rep["qsl"], rep["seq_lens"], rep["block_table"],

@@ -280,6 +280,23 @@ pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const v
                                      int32_t* error_flag, int64_t num_blocks, void* stream);
 
 /*
+ * pkv_write_attention_varlen_e4m3 - pkv_write_e4m3 then
+ * pkv_attention_varlen_e4m3, as one call: the write rides in the decode
+ * kernel (quantising bf16 rows with k_scale / v_scale as pkv_write_e4m3
+ * does) when every request is decode-class, as for
+ * pkv_write_attention_varlen.  k_new, v_new: bf16 [num_tokens,
+ * num_kv_heads, head_dim].  Other arguments as pkv_attention_varlen_e4m3.
+ */
+pkv_status pkv_write_attention_varlen_e4m3(
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
+    void* k_cache, void* v_cache, void* out, float* lse_out, const int32_t* query_start_loc,
+    const int32_t* seq_lens, const int32_t* block_table, int max_blocks_per_seq, int num_seqs,
+    int64_t num_tokens, int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, float softmax_scale, float k_scale, float v_scale, int causal,
+    int num_splits, void* workspace, size_t workspace_bytes, int32_t* error_flag,
+    int64_t num_blocks, void* stream);
+
+/*
  * pkv_attention_varlen_noalloc - pkv_attention_varlen without a caller
  * workspace.
  *

@@ -24,7 +24,7 @@ FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
 # Every symbol include/pkv.h declares.
 EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_num_splits", "pkv_workspace_bytes",
            "pkv_attention_varlen", "pkv_write_attention_varlen", "pkv_attention_varlen_window",
-           "pkv_attention_varlen_e4m3",
+           "pkv_attention_varlen_e4m3", "pkv_write_attention_varlen_e4m3",
            "pkv_attention_varlen_noalloc", "pkv_cascade_splits", "pkv_cascade_workspace_bytes",
            "pkv_cascade_attention", "pkv_status_string")
 
@@ -62,6 +62,11 @@ def lib() -> ctypes.CDLL:
                                                  i32, i64, i32, i32, i32, i32, i32, i32, f32,
                                                  i32, i32, vp, sz, vp, i64, i32, vp]
         L.pkv_write_attention_varlen.restype = i32
+        L.pkv_write_attention_varlen_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                      i32, i32, i64, i32, i32, i32, i32, i32,
+                                                      i32, f32, f32, f32, i32, i32, vp, sz, vp,
+                                                      i64, vp]
+        L.pkv_write_attention_varlen_e4m3.restype = i32
         L.pkv_attention_varlen_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
                                                   i32, i32, i32, i32, i32, i32, f32, i32, i32,
                                                   i32, vp, sz, vp, i64, i32, vp]
@@ -228,6 +233,38 @@ def pkv_write_attention_varlen(k_new, v_new, slot_mapping, q, k_cache, v_cache, 
         _ptr(workspace), int(ws_bytes), _ptr(error_flag), int(nb), _dtype_code(q.dtype),
         _stream(stream))
     _check("pkv_write_attention_varlen", code)
+    return out
+
+
+def pkv_write_attention_varlen_e4m3(k_new, v_new, slot_mapping, q, k_cache, v_cache, out,
+                                    query_start_loc, seq_lens, block_table, max_query_len,
+                                    max_seq_len, softmax_scale, k_scale, v_scale, causal=True,
+                                    num_splits=0, workspace=None, lse_out=None, error_flag=None,
+                                    stream=None):
+    """pkv_write_e4m3 then pkv_attention_varlen_e4m3 in one call (the write
+    rides in the decode kernel for decode-class steps)."""
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 caches are uint8 tensors of codes")
+    if q.dtype != torch.bfloat16 or k_new.dtype != torch.bfloat16:
+        raise TypeError("q and the new K/V are bf16 for E4M3 caches")
+    n_tok, hq, d = q.shape
+    nb, bs, hkv, _ = k_cache.shape
+    num_seqs = int(seq_lens.numel())
+    splits = int(num_splits)
+    if splits == 0 and num_seqs > 0:
+        splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, hq, hkv, d, q.device.index)
+    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib().pkv_write_attention_varlen_e4m3(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(out), _ptr(lse_out), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table),
+        int(block_table.shape[1]), num_seqs, int(n_tok), int(max_query_len), int(max_seq_len),
+        int(hq), int(hkv), int(d), int(bs), float(softmax_scale), float(k_scale), float(v_scale),
+        1 if causal else 0, splits, _ptr(workspace), int(ws_bytes), _ptr(error_flag), int(nb),
+        _stream(stream))
+    _check("pkv_write_attention_varlen_e4m3", code)
     return out
 
 

@@ -137,6 +137,8 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
                             int64_t num_blocks, ElemType et, void* stream,
                             const void* fuse_k_new = nullptr, const void* fuse_v_new = nullptr,
                             const int64_t* fuse_slots = nullptr) {
+  // (fuse_*: the step's new K/V, stored by the decode kernel - bf16 rows
+  // quantised with k_scale / v_scale for an E4M3 cache)
   // ---- host-checkable arguments ----
   if (window < 0 || num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
       num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || num_splits < 0 ||
@@ -222,6 +224,8 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     a.k_new = fuse_k_new;
     a.v_new = fuse_v_new;
     a.slots = fuse_slots;
+    a.wk_scale = k_scale;
+    a.wv_scale = v_scale;
   }
 
   CUtensorMap kmap, vmap;
@@ -392,6 +396,38 @@ pkv_status pkv_write_attention_varlen(
                    num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, 1.f, 1.f,
                    causal, 0, num_splits, workspace, workspace_bytes, error_flag, num_blocks, et,
                    stream);
+}
+
+pkv_status pkv_write_attention_varlen_e4m3(
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
+    void* k_cache, void* v_cache, void* out, float* lse_out, const int32_t* query_start_loc,
+    const int32_t* seq_lens, const int32_t* block_table, int max_blocks_per_seq, int num_seqs,
+    int64_t num_tokens, int max_query_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, float softmax_scale, float k_scale, float v_scale, int causal,
+    int num_splits, void* workspace, size_t workspace_bytes, int32_t* error_flag,
+    int64_t num_blocks, void* stream) {
+  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_INVALID_ARG;
+  if (num_tokens > 0 && num_seqs > 0) {
+    if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(slot_mapping, 8))
+      return PKV_ERR_INVALID_ARG;
+  }
+  if (max_query_len <= kDecodeMaxQ) {
+    return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                     max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                     num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, k_scale,
+                     v_scale, causal, 0, num_splits, workspace, workspace_bytes, error_flag,
+                     num_blocks, ElemType::kE4m3, stream, k_new, v_new, slot_mapping);
+  }
+  pkv_status st = pkv_write_e4m3(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache,
+                                 num_blocks, block_size, num_kv_heads, head_dim, PKV_BF16,
+                                 k_scale, v_scale, error_flag, stream);
+  if (st != PKV_OK) return st;
+  return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                   max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                   num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, k_scale,
+                   v_scale, causal, 0, num_splits, workspace, workspace_bytes, error_flag,
+                   num_blocks, ElemType::kE4m3, stream);
 }
 
 pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const void* v_cache,

@@ -69,6 +69,7 @@ struct AttnArgs {
   const void* k_new;      // [num_tokens, hkv, D], the cache's element type
   const void* v_new;
   const int64_t* slots;   // slot_mapping
+  float wk_scale, wv_scale;  // E4M3 caches: the write stores codes of value / scale
 };
 
 // ---------------------------------------------------------------------------

@@ -665,7 +665,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     // ---- fused write (warp 0): the K/V rows of head g of the new tokens this
     //      CTA reads; every CTA reading a row stores the same bytes first ----
     if (fw_lo < fw_hi && warp == 0) {
-      constexpr int kChunks = C::kRowBytes / 16;             // 16-byte chunks of a row
+      // a chunk: 16 bytes of the new row (8 bf16 -> 8 codes for E4M3 caches)
+      constexpr int kChunks = kIsE4m3<T> ? D / 8 : C::kRowBytes / 16;
       const int p_first = L - n;
       const int count = (fw_hi - fw_lo) * 2 * kChunks;
       const int64_t num_slots = a.num_blocks * kBlock;
@@ -679,13 +680,27 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
           raise_flag(a.flag, PKV_FLAG_BAD_SLOT);
           continue;
         }
-        const uint4* src = reinterpret_cast<const uint4*>(
-                               static_cast<const uint8_t*>(part ? a.v_new : a.k_new) +
-                               (t * a.hkv + g) * C::kRowBytes) + ch;
-        uint4* dst = reinterpret_cast<uint4*>(
-                         static_cast<uint8_t*>(const_cast<void*>(part ? a.v_cache : a.k_cache)) +
-                         (slot * a.hkv + g) * C::kRowBytes) + ch;
-        *dst = __ldg(src);
+        uint8_t* cache = static_cast<uint8_t*>(const_cast<void*>(part ? a.v_cache : a.k_cache));
+        if constexpr (kIsE4m3<T>) {
+          // codes of value / scale: fp32 division, nearest code, saturating
+          const uint4 x = __ldg(reinterpret_cast<const uint4*>(
+                                    static_cast<const uint8_t*>(part ? a.v_new : a.k_new) +
+                                    (t * a.hkv + g) * D * 2) + ch);
+          const float sc = part ? a.wv_scale : a.wk_scale;
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t c2[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            c2[i] = float2_to_e4m3x2(__fdiv_rn(bf16_lo(w[i]), sc), __fdiv_rn(bf16_hi(w[i]), sc));
+          *(reinterpret_cast<uint2*>(cache + (slot * a.hkv + g) * C::kRowBytes) + ch) =
+              make_uint2(c2[0] | (c2[1] << 16), c2[2] | (c2[3] << 16));
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(
+                                 static_cast<const uint8_t*>(part ? a.v_new : a.k_new) +
+                                 (t * a.hkv + g) * C::kRowBytes) + ch;
+          *(reinterpret_cast<uint4*>(cache + (slot * a.hkv + g) * C::kRowBytes) + ch) =
+              __ldg(src);
+        }
       }
       // the stores before the producer's TMA (async proxy) loads of them
       fence_proxy_async_global();

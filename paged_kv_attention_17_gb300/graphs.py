@@ -15,7 +15,7 @@ one graph holding a whole decode step on static buffers:
 2.-3. ``pkv_write_attention_varlen``: the new tokens' K/V stored by the decode
    kernel itself, then attention (one query token per request),
 
-(``pkv_write_e4m3`` and ``pkv_attention_varlen_e4m3`` over an 8-bit E4M3 cache),
+(``pkv_write_attention_varlen_e4m3`` over an 8-bit E4M3 cache),
 4. the copy of the output rows (and the error flag) back to pinned host memory.
 
 With ``zero_copy`` the graph has no copy nodes: its kernels read the pinned
@@ -199,13 +199,12 @@ class DecodeGraphRunner:
             self.dev_in[:lay.nbytes].copy_(self.host_in[slot][:lay.nbytes], non_blocking=True)
         if self.e4m3:
             ks, vs = self.kv_scales
-            B.pkv_write_e4m3(v["k_new"], v["v_new"], v["slot_mapping"], self.k_cache,
-                             self.v_cache, ks, vs, error_flag=self.flag)
-            B.pkv_attention_varlen_e4m3(v["q"], self.k_cache, self.v_cache, out,
-                                        v["query_start_loc"], v["seq_lens"], v["block_table"], 1,
-                                        self.max_seq_len, self.scale, ks, vs, causal=True,
-                                        num_splits=self.splits[b], workspace=self.workspace,
-                                        error_flag=self.flag)
+            B.pkv_write_attention_varlen_e4m3(v["k_new"], v["v_new"], v["slot_mapping"], v["q"],
+                                              self.k_cache, self.v_cache, out,
+                                              v["query_start_loc"], v["seq_lens"],
+                                              v["block_table"], 1, self.max_seq_len, self.scale,
+                                              ks, vs, causal=True, num_splits=self.splits[b],
+                                              workspace=self.workspace, error_flag=self.flag)
         else:
             # one token per request: the write rides in the decode kernel
             B.pkv_write_attention_varlen(v["k_new"], v["v_new"], v["slot_mapping"], v["q"],

@@ -54,6 +54,13 @@ def run_fused_step(d, num_splits=0, with_lse=True, causal=None, flag=None):
         flag = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty_like(d["q"])
     lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev) if with_lse else None
+    if getattr(w, "kv_dtype", None) == "e4m3":
+        pkv.pkv_write_attention_varlen_e4m3(
+            d["k_new"], d["v_new"], d["slot_mapping"], d["q"], d["k_cache"], d["v_cache"], out,
+            d["qsl"], d["seq_lens"], d["block_table"], meta["max_query_len"], meta["max_seq_len"],
+            w.softmax_scale, w.k_scale, w.v_scale, causal=w.causal if causal is None else causal,
+            num_splits=num_splits, lse_out=lse, error_flag=flag)
+        return out, lse, flag
     pkv.pkv_write_attention_varlen(d["k_new"], d["v_new"], d["slot_mapping"], d["q"],
                                    d["k_cache"], d["v_cache"], out, d["qsl"], d["seq_lens"],
                                    d["block_table"], meta["max_query_len"], meta["max_seq_len"],

@@ -20,10 +20,14 @@ TOL = {"bf16": (1e-2, 1e-3), "f32": (1e-4, 1e-5)}
 
 
 def _cache_bits(t):
+    if t.dtype == torch.uint8:
+        return t.cpu().numpy()
     return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32).cpu().numpy()
 
 
 def _ref_bits(x, dtype):
+    if x.dtype == np.uint8:
+        return x
     return np.ascontiguousarray(x).view(np.int16 if dtype == "bf16" else np.int32)
 
 
@@ -106,3 +110,34 @@ def test_padding_slot_is_not_stored_and_bad_slot_is_flagged():
     dev["slot_mapping"] = slots
     _, _, flag = run_fused_step(dev)
     assert int(flag.item()) & 2
+
+
+@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("hq,hkv,d,qlen", [(32, 8, 128, 1), (32, 8, 128, 3), (16, 2, 64, 1),
+                                           (64, 8, 128, 2)])
+def test_e4m3_decode_batches(splits, hq, hkv, d, qlen):
+    # the write quantises in the decode kernel: codes bit-exact to the oracle's
+    rng = np.random.Generator(np.random.PCG64(hq * 5 + qlen + d))
+    ctx = rng.integers(0, 600, size=10)
+    shape = [(int(c), qlen) for c in ctx] + [(0, qlen), (15, qlen), (16, qlen)]
+    w = workloads.build("fused8", "bf16", hq, hkv, d, shape, rng=rng, kv_dtype="e4m3",
+                        k_scale=0.037, v_scale=1.9)
+    dev = device_inputs(w)
+    out, lse, flag = run_fused_step(dev, num_splits=splits)
+    _check(w, dev, out, lse, flag, "bf16")
+
+
+def test_e4m3_bit_identical_to_separate_calls():
+    rng = np.random.Generator(np.random.PCG64(93))
+    shape = [(int(c), int(n)) for c, n in zip(rng.integers(0, 900, size=12),
+                                              rng.integers(1, 5, size=12))]
+    w = workloads.build("fused8_eq", "bf16", 32, 8, 128, shape, rng=rng, kv_dtype="e4m3",
+                        k_scale=0.5, v_scale=0.25)
+    dev = device_inputs(w)
+    fused, _, _ = run_fused_step(dev, num_splits=3)
+    dev2 = device_inputs(w)
+    sep, _, _ = run_step(dev2, num_splits=3)
+    assert torch.equal(fused, sep)
+    assert torch.equal(dev["k_cache"], dev2["k_cache"]) and torch.equal(dev["v_cache"],
+                                                                        dev2["v_cache"])
+
