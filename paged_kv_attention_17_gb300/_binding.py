@@ -158,6 +158,21 @@ def pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, num_splits) -> int:
                                          int(num_splits)))
 
 
+def _splits_and_workspace(q, hkv, num_seqs, max_query_len, span, num_splits, workspace):
+    """The split count (pkv_num_splits for a context of ``span`` keys when
+    num_splits is 0) and a workspace for its partials: the caller's, or one
+    allocated with torch here when none is given and one is needed."""
+    _, hq, d = q.shape
+    splits = int(num_splits)
+    if splits == 0 and num_seqs > 0:
+        splits = pkv_num_splits(num_seqs, max_query_len, span, hq, hkv, d, q.device.index)
+    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return splits, workspace, ws_bytes
+
+
 def split_span(max_seq_len, window=0) -> int:
     """The context length the automatic split count is sized for: a window
     bounds the keys a decode row reads to window + PKV_DECODE_MAX_QLEN."""
@@ -180,14 +195,8 @@ def pkv_attention_varlen(q, k_cache, v_cache, out, query_start_loc, seq_lens, bl
     n_tok, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     num_seqs = int(seq_lens.numel())
-    splits = int(num_splits)
-    if splits == 0 and num_seqs > 0:
-        splits = pkv_num_splits(num_seqs, max_query_len, split_span(max_seq_len, window), hq, hkv,
-                                d, q.device.index)
-    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    splits, workspace, ws_bytes = _splits_and_workspace(
+        q, hkv, num_seqs, max_query_len, split_span(max_seq_len, window), num_splits, workspace)
     if window:
         code = lib().pkv_attention_varlen_window(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out),
@@ -218,13 +227,8 @@ def pkv_write_attention_varlen(k_new, v_new, slot_mapping, q, k_cache, v_cache, 
     n_tok, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     num_seqs = int(seq_lens.numel())
-    splits = int(num_splits)
-    if splits == 0 and num_seqs > 0:
-        splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, hq, hkv, d, q.device.index)
-    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    splits, workspace, ws_bytes = _splits_and_workspace(
+        q, hkv, num_seqs, max_query_len, max_seq_len, num_splits, workspace)
     code = lib().pkv_write_attention_varlen(
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(out), _ptr(lse_out), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table),
@@ -250,13 +254,8 @@ def pkv_write_attention_varlen_e4m3(k_new, v_new, slot_mapping, q, k_cache, v_ca
     n_tok, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     num_seqs = int(seq_lens.numel())
-    splits = int(num_splits)
-    if splits == 0 and num_seqs > 0:
-        splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, hq, hkv, d, q.device.index)
-    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    splits, workspace, ws_bytes = _splits_and_workspace(
+        q, hkv, num_seqs, max_query_len, max_seq_len, num_splits, workspace)
     code = lib().pkv_write_attention_varlen_e4m3(
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), _ptr(k_cache), _ptr(v_cache),
         _ptr(out), _ptr(lse_out), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table),
@@ -282,13 +281,8 @@ def pkv_attention_varlen_e4m3(q, k_cache, v_cache, out, query_start_loc, seq_len
     n_tok, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     num_seqs = int(seq_lens.numel())
-    splits = int(num_splits)
-    if splits == 0 and num_seqs > 0:
-        splits = pkv_num_splits(num_seqs, max_query_len, max_seq_len, hq, hkv, d, q.device.index)
-    need = pkv_workspace_bytes(num_seqs, hq, d, splits)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    splits, workspace, ws_bytes = _splits_and_workspace(
+        q, hkv, num_seqs, max_query_len, max_seq_len, num_splits, workspace)
     code = lib().pkv_attention_varlen_e4m3(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
         _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]), num_seqs, int(n_tok),
