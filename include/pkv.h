@@ -40,8 +40,10 @@
  * Entry points: pkv_write / pkv_write_e4m3 (slot-mapped write), pkv_num_splits
  * and pkv_workspace_bytes (split-KV sizing), pkv_attention_varlen and its
  * variants _window (sliding window), _e4m3 (8-bit cache) and _noalloc (no
- * caller workspace), pkv_cascade_splits / pkv_cascade_workspace_bytes /
- * pkv_cascade_attention (requests sharing a block-aligned prefix), and
+ * caller workspace), pkv_write_attention_varlen / _e4m3 (write and attend in
+ * one call, the write folded into the decode kernel for decode steps), pkv_cascade_splits / pkv_cascade_workspace_bytes /
+ * pkv_cascade_attention (requests sharing a block-aligned prefix),
+ * pkv_build_metadata (the step's flat-batch metadata, host only) and
  * pkv_status_string.
  */
 #ifndef PKV_H
@@ -395,6 +397,37 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
                                  float softmax_scale, int prefix_splits, void* workspace,
                                  size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
                                  pkv_dtype dtype, void* stream);
+
+/*
+ * pkv_build_metadata - the flat-batch metadata of one step, on the host.
+ *
+ * "Model execution", section "Flattening a step": the scheduled tokens of all
+ * requests form one flat batch; query_start_loc holds the cumulative token
+ * offsets, seq_lens the context after this step (computed + scheduled),
+ * block_table each request's physical blocks, and slot_mapping the slot
+ * block_id * block_size + offset of new token k of request r, which sits at
+ * position computed[r] + k.  Host memory only; no CUDA call.
+ *   computed, scheduled  host int32 [num_seqs], >= 0.
+ *   block_offsets        host int32 [num_seqs + 1], [0] = 0, nondecreasing:
+ *                        request r's blocks are block_ids[block_offsets[r] ..
+ *                        block_offsets[r + 1]), at least ceil((computed +
+ *                        scheduled) / block_size) of them, ids >= 0.
+ *   max_blocks_per_seq   width of block_table, >= every request's block count.
+ *   num_tokens           must equal the sum of scheduled.
+ *   Outputs (host, caller-allocated): query_start_loc int32 [num_seqs + 1],
+ *   seq_lens int32 [num_seqs], block_table int32 [num_seqs,
+ *   max_blocks_per_seq] (unused entries 0), slot_mapping int64 [num_tokens],
+ *   positions int64 [num_tokens] or NULL, max_query_len / max_seq_len host
+ *   int32 or NULL.
+ * Every argument is checked before anything is written; a violation returns
+ * PKV_ERR_INVALID_ARG and writes nothing.
+ */
+pkv_status pkv_build_metadata(int num_seqs, const int32_t* computed, const int32_t* scheduled,
+                              const int32_t* block_offsets, const int32_t* block_ids,
+                              int block_size, int max_blocks_per_seq, int64_t num_tokens,
+                              int32_t* query_start_loc, int32_t* seq_lens, int32_t* block_table,
+                              int64_t* slot_mapping, int64_t* positions, int32_t* max_query_len,
+                              int32_t* max_seq_len);
 
 /* Static, human-readable name of a status code. */
 const char* pkv_status_string(pkv_status status);

@@ -17,6 +17,7 @@ from . import graphs, metadata  # noqa: F401
 from ._binding import (EXPORTS, FLAG_BAD_BLOCK, FLAG_BAD_LENGTHS, FLAG_BAD_SLOT,  # noqa: F401
                        FLAG_TIMEOUT, PKV_DECODE_MAX_QLEN, PkvError, lib, pkv_attention_varlen,
                        pkv_attention_varlen_e4m3, pkv_attention_varlen_noalloc,
+                       pkv_build_metadata,
                        pkv_cascade_attention, pkv_cascade_splits, pkv_cascade_workspace_bytes,
                        pkv_num_splits, pkv_status_string, pkv_workspace_bytes, pkv_write,
                        pkv_write_attention_varlen, pkv_write_attention_varlen_e4m3,

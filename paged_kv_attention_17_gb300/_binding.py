@@ -26,7 +26,7 @@ EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_num_splits", "pkv_workspace_bytes
            "pkv_attention_varlen", "pkv_write_attention_varlen", "pkv_attention_varlen_window",
            "pkv_attention_varlen_e4m3", "pkv_write_attention_varlen_e4m3",
            "pkv_attention_varlen_noalloc", "pkv_cascade_splits", "pkv_cascade_workspace_bytes",
-           "pkv_cascade_attention", "pkv_status_string")
+           "pkv_cascade_attention", "pkv_build_metadata", "pkv_status_string")
 
 
 class PkvError(RuntimeError):
@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
                                             i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
                                             i64, i32, vp]
         L.pkv_cascade_attention.restype = i32
+        L.pkv_build_metadata.argtypes = [i32, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp, vp,
+                                         vp, vp]
+        L.pkv_build_metadata.restype = i32
         L.pkv_status_string.argtypes = [i32]
         L.pkv_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -358,3 +361,41 @@ def pkv_cascade_attention(q, k_cache, v_cache, out, query_start_loc, suffix_lens
         _dtype_code(q.dtype), _stream(stream))
     _check("pkv_cascade_attention", code)
     return out
+
+
+def pkv_build_metadata(computed, scheduled, block_ids_per_request, block_size=16,
+                       max_blocks_per_seq=None):
+    """The step's flat-batch metadata from the library's host builder:
+    ``computed`` / ``scheduled`` per request and each request's block ids.
+    Returns numpy arrays query_start_loc, seq_lens, block_table (int32),
+    slot_mapping, positions (int64) and the host scalars num_tokens,
+    max_query_len, max_seq_len."""
+    import numpy as np
+    n = len(computed)
+    c = np.ascontiguousarray(computed, dtype=np.int32)
+    s = np.ascontiguousarray(scheduled, dtype=np.int32)
+    counts = [len(b) for b in block_ids_per_request]
+    offsets = np.zeros(n + 1, dtype=np.int32)
+    np.cumsum(counts, out=offsets[1:])
+    ids = np.ascontiguousarray(np.concatenate([np.asarray(b, dtype=np.int32)
+                                               for b in block_ids_per_request])
+                               if n and offsets[-1] else np.zeros(1, dtype=np.int32))
+    width = int(max_blocks_per_seq or max(counts + [1]))
+    num_tokens = int(s.sum()) if n else 0
+    qsl = np.zeros(n + 1, dtype=np.int32)
+    seq_lens = np.zeros(max(n, 1), dtype=np.int32)
+    table = np.zeros((max(n, 1), width), dtype=np.int32)
+    slots = np.zeros(max(num_tokens, 1), dtype=np.int64)
+    pos = np.zeros(max(num_tokens, 1), dtype=np.int64)
+    mq, ms = ctypes.c_int32(0), ctypes.c_int32(0)
+    p = lambda a: ctypes.c_void_p(a.ctypes.data)  # noqa: E731
+    code = lib().pkv_build_metadata(n, p(c) if n else None, p(s) if n else None, p(offsets),
+                                    p(ids), int(block_size), width, num_tokens, p(qsl),
+                                    p(seq_lens), p(table), p(slots), p(pos),
+                                    ctypes.byref(mq), ctypes.byref(ms))
+    _check("pkv_build_metadata", code)
+    return {"query_start_loc": qsl, "seq_lens": seq_lens[:n], "block_table": table[:n],
+            "slot_mapping": slots[:num_tokens], "positions": pos[:num_tokens],
+            "num_tokens": num_tokens, "max_query_len": int(mq.value),
+            "max_seq_len": int(ms.value)}
+

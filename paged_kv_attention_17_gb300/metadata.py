@@ -58,3 +58,14 @@ def context_slot_mapping(requests, block_size: int = 16) -> np.ndarray:
         blocks = np.asarray(r.blocks, dtype=np.int64)
         out.append(blocks[pos // block_size] * block_size + pos % block_size)
     return np.concatenate(out) if out else np.zeros(0, dtype=np.int64)
+
+
+def build_native(requests, block_size: int = 16, max_blocks_per_seq: int | None = None) -> dict:
+    """``build`` through the library's host builder (``pkv_build_metadata``,
+    the same arrays for a C host)."""
+    from . import _binding
+    return _binding.pkv_build_metadata([r.computed for r in requests],
+                                       [r.scheduled for r in requests],
+                                       [list(r.blocks) for r in requests], block_size,
+                                       max_blocks_per_seq)
+
