@@ -433,3 +433,27 @@ def test_planted_upcast_error_is_caught(monkeypatch):
     orig = ref.upcast
     monkeypatch.setattr(ref, "upcast", lambda x, dt: orig(x, dt) * (1 + 1e-6))
     assert not _sdpa_pin_holds()
+
+
+def _window_pin_holds(window=7):
+    rng = np.random.default_rng(78)
+    reqs, kc, vc, q = _contiguous_case(rng, 4, 2, 8, [(20, 3), (0, 9), (40, 1)])
+    o, _ = _ref(q, kc, vc, reqs, 4, 2, 0.3, True, window=window)
+    want = _sdpa_window(q, kc, vc, reqs, 4, 2, 0.3, window)
+    return np.abs(o - want).max() < 1e-12
+
+
+def test_planted_window_off_by_one_is_caught(monkeypatch):
+    assert _window_pin_holds()
+    orig = ref.attention
+
+    def wider(*a, window=0, **kw):                # keeps j >= p - W: one key too many
+        return orig(*a, window=window + 1 if window else 0, **kw)
+    monkeypatch.setattr(ref, "attention", wider)
+    assert not _window_pin_holds()
+
+
+def test_planted_window_ignored_is_caught(monkeypatch):
+    orig = ref.attention
+    monkeypatch.setattr(ref, "attention", lambda *a, window=0, **kw: orig(*a, **kw))
+    assert not _window_pin_holds()

@@ -74,3 +74,19 @@ def test_zero_query_averages_prefix_and_suffix_values():
             assert np.allclose(o[t, 0], flat[slots[:vis], 0].mean(axis=0), atol=1e-13, rtol=0)
             assert abs(lse[t, 0] - math.log(vis)) < 1e-13
             t += 1
+
+
+def test_planted_causal_prefix_pass_is_caught(monkeypatch):
+    # a cascade that masked the prefix causally (as if each row sat inside it)
+    # must disagree with the plain result
+    from oracle import ref
+    w = _cascade_workload(13, 3, [(4, 1), (0, 2)])
+    meta, shared, suffix_table, suffix_lens = _parts(w)
+    kw = dict(num_q_heads=4, num_kv_heads=2, softmax_scale=w.softmax_scale, dtype="f32")
+    args = (w.q, w.k_pool, w.v_pool, meta["query_start_loc"], suffix_lens, suffix_table, shared)
+    o, _ = cascade.attention(*args, **kw)
+    orig = ref.attention
+    monkeypatch.setattr(ref, "attention",
+                        lambda *a, causal=True, **k: orig(*a, causal=True, **k))
+    o2, _ = cascade.two_level(*args, **kw)
+    assert np.abs(o - o2).max() > 1e-6

@@ -108,3 +108,33 @@ def test_fp8_zero_query_gives_the_mean_of_visible_v():
     o, _, _, vc, meta = ref.paged_step(w)
     V = 0.5 * fp8.decode(ref.gather(vc, meta["block_table"][0], 21, 16))
     assert np.abs(o[0, 0] - V[:, 0, :].mean(0)).max() < 1e-12
+
+
+def _decode_pin_holds():
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().double().numpy()
+    got = fp8.decode(codes)
+    return bool(np.array_equal(np.isnan(got), np.isnan(want)) and
+                np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)]))
+
+
+def test_decode_matches_torch_for_every_code():
+    assert _decode_pin_holds()
+
+
+def test_planted_exponent_bias_is_caught(monkeypatch):
+    orig = fp8.decode
+    monkeypatch.setattr(fp8, "decode", lambda c: orig(c) / 2.0)      # bias 8 instead of 7
+    assert not _decode_pin_holds()
+
+
+def test_planted_subnormal_scale_is_caught(monkeypatch):
+    orig = fp8.decode
+
+    def wrong(c):
+        c = np.asarray(c, dtype=np.uint8)
+        v = orig(c)
+        sub = ((c >> 3) & 0xF) == 0
+        return np.where(sub, v * 2.0, v)                                # m/8 * 2^-5
+    monkeypatch.setattr(fp8, "decode", wrong)
+    assert not _decode_pin_holds()
