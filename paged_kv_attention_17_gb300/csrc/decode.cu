@@ -48,6 +48,14 @@
 //   * Each warp keeps its own (m, l, acc); the warps are merged through shared
 //     memory at the end (same algebra as the split merge).
 //   * Bounded mbarrier waits: a stuck pipeline sets PKV_FLAG_TIMEOUT and exits.
+//   * Variants over the same pipeline: E4M3 caches (codes widened to fp32 in
+//     registers, k/v scales folded into the score scale and the epilogue);
+//     sliding windows (a tile's range starts at its first row's window, each
+//     row masks below its own); the cascade passes (every row of the batch
+//     over a shared prefix, or a request's own keys, written as fp32
+//     partials); and the fused write (consumer warp 0 stores the step's new
+//     K/V rows this CTA reads, and the producer loads a block holding one only
+//     after a barrier says they are stored).
 #include <type_traits>
 
 #include "common.cuh"
