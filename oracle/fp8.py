@@ -10,7 +10,8 @@ format.  The reading taken: E4M3 codes - 1 sign bit, 4 exponent bits with bias
 finite magnitude is 1.75 * 2^8 = 448; there are no infinities and the codes
 S.1111.111 are NaN - with one fp32 scale per cache tensor: a cached element
 stands for scale * value(code).  Encoding rounds to the nearest code, ties to
-the even mantissa, and saturates magnitudes beyond 448 to 448.
+the even mantissa, and saturates magnitudes beyond 448 to 448; infinities
+saturate the same way (the format has none).
 
 Written from that definition with exact float64 arithmetic; pinned in
 ``tests/test_oracle_fp8.py`` against PyTorch's float8_e4m3fn conversion
@@ -37,8 +38,9 @@ def decode(codes) -> np.ndarray:
 
 
 def encode(x) -> np.ndarray:
-    """Nearest E4M3 code of each value (ties to even, saturating at 448; NaN
-    to the NaN code).  Values are exact float64 (e.g. float32 inputs)."""
+    """Nearest E4M3 code of each value (ties to even, saturating at 448, +-inf
+    included; NaN to the NaN code).  Values are exact float64 (e.g. float32
+    inputs)."""
     x = np.asarray(x, dtype=np.float64)
     out = np.empty(x.shape, dtype=np.uint8)
     flat, res = x.ravel(), out.ravel()
@@ -48,7 +50,9 @@ def encode(x) -> np.ndarray:
             continue
         s = 0x80 if np.signbit(v) else 0
         a = abs(v)
-        if a >= 2.0 ** -6:                        # normal range
+        if np.isinf(a):                           # no infinities in E4M3: saturate
+            res[k] = s | 0x7E
+        elif a >= 2.0 ** -6:                      # normal range
             mant, e = np.frexp(a)                 # a = mant * 2^e, mant in [0.5, 1)
             e -= 1                                # a = (2 mant) * 2^e, 2 mant in [1, 2)
             q = np.round((2.0 * mant - 1.0) * 8.0)   # ties to even

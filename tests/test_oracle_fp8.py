@@ -44,6 +44,9 @@ def test_closed_forms():
     for v, c in cases.items():
         assert int(fp8.encode(np.array([v]))[0]) == c, (v, c)
     assert int(fp8.encode(np.array([np.nan]))[0]) == 0x7F
+    # the format has no infinity: +-inf saturate like any magnitude past 448
+    assert fp8.encode(np.array([np.inf, -np.inf])).tolist() == [0x7E, 0xFE]
+    assert fp8.quantize(np.array([np.inf, -np.inf], dtype=np.float32), 0.5).tolist() == [0x7E, 0xFE]
     assert fp8.decode([0x7E])[0] == 448.0 and fp8.decode([0x01])[0] == 2.0 ** -9
     assert np.isnan(fp8.decode([0x7F, 0xFF])).all()
 
