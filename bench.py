@@ -309,6 +309,19 @@ def _launches_per_step(splits, meta):
     return n
 
 
+def graph_sizes(k: int, group: int) -> list[int]:
+    """Graph lengths a run of k steps replays: k // group replays of a graph
+    of `group` steps, then one graph of the remaining k % group."""
+    full, rest = divmod(k, group)
+    return ([group] if full else []) + ([rest] if rest else [])
+
+
+def precapture_sizes(warmup: int, steps: int, group: int) -> list[int]:
+    """Every graph length the warm-up, the timed steps and the percentile
+    replays (graphs of `group` steps) use: captured before any timing."""
+    return sorted(set(graph_sizes(warmup, group) + graph_sizes(steps, group) + [group]))
+
+
 def step_percentiles(run_steps, per_rep, device, reps=60):
     """p10 / p50 / p90 of the per-step time over individually timed replays of
     `per_rep` steps each (outside the main timed region)."""
@@ -445,10 +458,13 @@ def run_gpu(args, rank, world, local_rank):
     G = len(reps)
     use_graph = m0["max_query_len"] <= 4               # decode steps: graph, as a server runs them
     graphs = {}
+    timed = {"active": False, "captures": 0}
 
     def graph_of(nsteps, body):
         if nsteps in graphs:
             return graphs[nsteps]
+        if timed["active"]:
+            timed["captures"] += 1                    # never expected: checked below
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
@@ -473,6 +489,13 @@ def run_gpu(args, rank, world, local_rank):
         if rest:
             graph_of(rest, step).replay()
 
+    # ---- every graph the warm-up and the timed steps replay is captured (and
+    #      replayed once) here, so the timed region holds replays only ----
+    if use_graph:
+        for n in precapture_sizes(args.warmup, args.steps, G):
+            graph_of(n, step).replay()
+        torch.cuda.synchronize()
+
     # ---- warm-up, then exactly K timed steps ----
     run_steps(args.warmup)
     torch.cuda.synchronize()
@@ -483,18 +506,22 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.mark(True)
+    timed["active"] = True
     start.record()
     run_steps(args.steps)
     end.record()
     torch.cuda.synchronize()
+    timed["active"] = False
     clocks.mark(False)
     barrier(world)
+    if timed["captures"]:
+        raise RuntimeError("a CUDA graph was captured inside the timed region")
     ms_total = reduce_max(start.elapsed_time(end), world, device)
     clk = clocks.stop() if rank == 0 else None
     if int(flag.item()) != 0:
         raise RuntimeError(f"device error flag {int(flag.item())}")
     ms_step = ms_total / args.steps
-    pct = step_percentiles(run_steps, G if use_graph else 8, device)
+    pct = step_percentiles(run_steps, G if use_graph else 4, device)
     bytes_step = kv_bytes(w.requests, hkv, d, esize)
     flops_step = causal_flops(w.requests, hq, d)
     decode_like = m0["max_query_len"] <= 4
@@ -502,7 +529,7 @@ def run_gpu(args, rank, world, local_rank):
     value = per_rank_value * world
 
     # ---- the dominant kernel alone: attention calls back to back, events around ----
-    nat = 400 if decode_like else 3
+    nat = 400 if decode_like else 20
     att_body = lambda i: attend(reps[i % len(reps)])  # noqa: E731
     if use_graph:
         ga = torch.cuda.CUDAGraph()
@@ -570,6 +597,20 @@ def run_gpu(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4)}
         kernel_file = "decode.cu"
+    elif any(r.scheduled <= 4 for r in w.requests):
+        # a mixed step (decode rows and long chunks in one call): bound by the
+        # slower of its classes, t* = max(decode KV bytes / HBM peak, chunk
+        # FLOPs / bf16 peak); reported in the binding class's unit as the rate
+        # that would finish t*'s work in the measured call time, so that
+        # frac = t* / call time
+        mr = mixed_roofline(w, hq, hkv, d, esize, att_ms, peaks)
+        if mr["bound"] == "hbm":
+            peak, unit = float(peaks["hbm_gbs"]), "GB/s"
+        else:
+            peak, unit = float(peaks["bf16_tflops"]), "TFLOP/s"
+        roof = {"bound": mr["bound"], "achieved": round(mr["frac"] * peak, 1), "peak": peak,
+                "unit": unit, "frac": mr["frac"], "t_star_ms": mr["t_star_ms"]}
+        kernel_file = "decode.cu" if mr["bound"] == "hbm" else "prefill.cu"
     else:
         achieved = (flops_step / 1e12) / (att_ms / 1e3)
         peak = float(peaks["bf16_tflops"])
@@ -580,6 +621,9 @@ def run_gpu(args, rank, world, local_rank):
     roof["traffic"] = tr["bytes"] if tr else None
     roof["kernel"] = ("pkv_attention_varlen call (split-KV decode kernel + LSE combine), "
                       f"{splits} splits" if decode_like else "pkv_attention_varlen call (prefill)")
+    if not decode_like and "t_star_ms" in roof:
+        roof["kernel"] = ("pkv_attention_varlen call over the mixed batch (decode rows + prefill "
+                          "chunk): frac = t* / call time")
     if cascade:
         roof["kernel"] = (f"pkv_cascade_attention call (prefix pass, {csplits} splits; own-key "
                           "pass; merge)")
@@ -728,14 +772,25 @@ def run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, 
             "ms_per_step": round(ms, 6), "mode": "eager API calls, pinned host buffers"}
 
 
-def run_secondary_prefill(local_rank):
-    """prefill_8k: TFLOP/s of the causal prefill step (write + attention)."""
+SECONDARY = ("batched_decode_64", "mixed_chunked", "prefill_8k")
+
+
+def run_secondary(name, local_rank, steps, warmup, cpu_seconds):
+    """One more workload of the headline run, timed the same way (its own
+    warm-up, timed steps, roofline, clocks, end-to-end figure and CPU oracle
+    baseline)."""
     import torch
-    args = parse_args(["--workload", "prefill_8k", "--steps", "5", "--warmup", "2"])
+    args = parse_args(["--workload", name, "--steps", str(steps), "--warmup", str(warmup)])
     res, _ = run_gpu(args, 0, 1, local_rank)
     torch.cuda.synchronize()
-    return {"workload": res["config"]["workload"], "value": res["value"], "unit": res["unit"],
-            "ms_per_step": res["ms_per_step"], "roofline": res["roofline"], "e2e": res["e2e"]}
+    keep = ("value", "unit", "steps", "warmup", "ms_per_step", "ms_per_step_p10_p50_p90",
+            "roofline", "e2e", "clocks", "mixed_roofline", "gpu_launches", "dtype")
+    out = {"workload": res["config"]["workload"], "num_splits": res["config"]["num_splits"],
+           "step": res["config"]["step"], "l2": res["config"]["l2"]}
+    out.update({k: res[k] for k in keep if k in res})
+    if cpu_seconds > 0:
+        out["cpu_baseline"] = cpu_baseline(name, cpu_seconds)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -869,7 +924,12 @@ def main(argv=None):
             return 0
         result, w = run_gpu(args, rank, world, local_rank)
         if rank == 0 and world == 1 and not args.no_secondary and args.workload == HEADLINE:
-            result["prefill"] = run_secondary_prefill(local_rank)
+            # the other configurations of the pages' workloads, each timed with
+            # at least 20 steps after at least 3 warm-up steps
+            cs = 0.0 if args.no_cpu_baseline else min(args.cpu_seconds, 8.0)
+            result["secondary"] = {
+                n: run_secondary(n, local_rank, max(args.steps, 20), max(args.warmup, 3), cs)
+                for n in SECONDARY}
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
             if args.workload in ("decode_8k", "batched_decode_64"):

@@ -184,7 +184,10 @@ size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_
  *   seq_lens          device int32 [num_seqs].
  *   block_table       device int32 [num_seqs, max_blocks_per_seq].
  *   max_query_len     host: >= every n (bounds the prefill grid).
- *   max_seq_len       host: >= every L (used by the split heuristic only).
+ *   max_seq_len       host: >= every L, <= 16 * max_blocks_per_seq (sizes the
+ *                     split heuristic and the pre-launch L2 warm-up; a larger
+ *                     value returns PKV_ERR_INVALID_ARG).  A seq_len beyond the
+ *                     table row is flagged on the device (PKV_FLAG_BAD_LENGTHS).
  *   num_splits        0 = pkv_num_splits(...); else 1..64.
  *   workspace         device, >= pkv_workspace_bytes(num_seqs, num_q_heads,
  *                     head_dim, splits) bytes, 256-byte aligned; may be NULL
@@ -314,8 +317,9 @@ pkv_status pkv_write_attention_varlen_e4m3(
  *   exceed 8 MiB returns PKV_ERR_WORKSPACE and enqueues nothing.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current): make it before any
- *   stream capture.  All calls on a device share the array, so calls whose
- *   kernels overlap on the GPU race; serialise them.
+ *   stream capture.  Host threads may make first calls concurrently (the
+ *   cached address is atomic).  All calls on a device share the array, so
+ *   calls whose kernels overlap on the GPU race; serialise them.
  */
 pkv_status pkv_attention_varlen_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                         void* out, float* lse_out,
@@ -379,7 +383,8 @@ size_t pkv_cascade_workspace_bytes(int64_t num_tokens, int num_q_heads, int head
  *   suffix_block_table  device int32 [num_seqs, max_blocks_per_seq]: the
  *                       blocks of those keys.
  *   shared_block_table  device int32 [shared_blocks] (NULL when 0 blocks).
- *   max_suffix_len      host, >= every suffix_lens[r].
+ *   max_suffix_len      host, >= every suffix_lens[r] and <= 16 *
+ *                       max_blocks_per_seq (else PKV_ERR_INVALID_ARG).
  *   prefix_splits       0 = pkv_cascade_splits(...); else 1..63.
  *   workspace           device, >= pkv_cascade_workspace_bytes(num_tokens,
  *                       num_q_heads, head_dim, splits), 256-byte aligned

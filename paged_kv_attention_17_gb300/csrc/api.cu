@@ -148,6 +148,10 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
   if (block_size != kBlock || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
   if (max_query_len < 1 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+  // a table row of max_blocks_per_seq blocks holds at most 16x that many keys:
+  // a larger bound on seq_lens cannot describe a valid batch
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * kBlock)
+    return PKV_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !out || !query_start_loc || !seq_lens || !block_table)
     return PKV_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
@@ -513,6 +517,8 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
   if (block_size != kBlock || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
   if (max_query_len < 1 || max_blocks_per_seq < 1) return PKV_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_suffix_len) > static_cast<int64_t>(max_blocks_per_seq) * kBlock)
+    return PKV_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !out || !query_start_loc || !suffix_lens ||
       !suffix_block_table || (shared_blocks > 0 && !shared_block_table))
     return PKV_ERR_INVALID_ARG;

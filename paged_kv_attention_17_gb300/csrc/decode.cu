@@ -332,9 +332,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     const int len_hint = min(max(__ldcg(a.seq_lens + r), 0), a.max_seq_len);
     const int n_hint = __ldcg(a.qsl + r + 1) - __ldcg(a.qsl + r);
     const bool runs_here = n_hint >= 1 && (n_hint <= kDecodeMaxQ || a.long_rows);
+    // (capped at nb_spec: never past the table row, whatever the hinted length)
     const int sb1 = !runs_here ? sb0
-                               : min(min(sb0 + per_spec, (len_hint + kBlock - 1) / kBlock),
-                                     sb0 + C::kPrefetchBlocks);
+                               : min(min(min(sb0 + per_spec, (len_hint + kBlock - 1) / kBlock),
+                                         sb0 + C::kPrefetchBlocks),
+                                     nb_spec);
     constexpr int kLines = C::kRowBytes / 128 > 0 ? C::kRowBytes / 128 : 1;  // lines per row
     const int64_t head_off = static_cast<int64_t>(g) * C::kRowBytes;
     const int64_t slot_bytes = static_cast<int64_t>(a.hkv) * C::kRowBytes;

@@ -18,6 +18,10 @@
 // the GPU (e.g. on two streams) race on it and must be serialised by the
 // caller.  Nothing in it has to start at zero: every partial the combine
 // kernel reads is written earlier in the same call by the decode kernel.
+// The per-device address cache is atomic, so host threads may make their
+// first calls on a device concurrently (each stores the same address).
+#include <atomic>
+
 #include "common.cuh"
 
 namespace {
@@ -26,7 +30,9 @@ constexpr size_t kStaticWorkspaceBytes = static_cast<size_t>(8) << 20;
 
 __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-void* g_workspace_ptr[64] = {nullptr};   // device address of the array, per device
+// device address of the array, per device (relaxed atomics: every thread that
+// resolves it stores the same value)
+std::atomic<void*> g_workspace_ptr[64];
 
 }  // namespace
 
@@ -63,17 +69,17 @@ extern "C" pkv_status pkv_attention_varlen_noalloc(
   // an explicit split count whose partials do not fit is rejected
   if (pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits) > kStaticWorkspaceBytes)
     return PKV_ERR_WORKSPACE;
-  if (g_workspace_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) {
+  void* ws = g_workspace_ptr[dev].load(std::memory_order_relaxed);
+  if (ws == nullptr) {
+    if (cudaGetSymbolAddress(&ws, g_static_workspace) != cudaSuccess || ws == nullptr) {
       cudaGetLastError();
       return PKV_ERR_CUDA;
     }
-    g_workspace_ptr[dev] = p;
+    g_workspace_ptr[dev].store(ws, std::memory_order_relaxed);
   }
   return pkv_attention_varlen(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens,
                               block_table, max_blocks_per_seq, num_seqs, num_tokens, max_query_len,
                               max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                              softmax_scale, causal, splits, g_workspace_ptr[dev],
+                              softmax_scale, causal, splits, ws,
                               kStaticWorkspaceBytes, error_flag, num_blocks, dtype, stream);
 }

@@ -122,6 +122,7 @@ def _attn_call(pkv, **over):
     (dict(num_seqs=0), 0),
     (dict(num_seqs=65536), 2),         # beyond the request grid
     (dict(num_blocks=1 << 27), 2),     # 2^31 slots: beyond int32 TMA coordinates
+    (dict(mbps=2, max_s=33), 1),       # a 2-block table row holds at most 32 keys
 ])
 def test_attention_host_validation(pkv, over, code):
     assert _attn_call(pkv, **over) == code
@@ -213,6 +214,7 @@ def _cascade_call(pkv, **over):
     (dict(dtype=7), 1),
     (dict(q=24), 1),
     (dict(num_tokens=0), 0),
+    (dict(mbps=2, max_s=33, ws=4096, ws_bytes=1 << 20), 1),   # own keys beyond the table row
 ])
 def test_cascade_host_validation(pkv, over, code):
     assert _cascade_call(pkv, **over) == code
