@@ -322,6 +322,15 @@ def precapture_sizes(warmup: int, steps: int, group: int) -> list[int]:
     return sorted(set(graph_sizes(warmup, group) + graph_sizes(steps, group) + [group]))
 
 
+def gpu_lead_in():
+    """Keep the GPU busy (a bounded spin of ~0.25 ms at full clock) while the
+    host enqueues the start event and the first steps, so the timed region
+    starts on a busy, clocked-up GPU instead of including the host's launch
+    latency and the clock ramp after an idle gap."""
+    import torch
+    torch.cuda._sleep(500_000)
+
+
 def step_percentiles(run_steps, per_rep, device, reps=60):
     """p10 / p50 / p90 of the per-step time over individually timed replays of
     `per_rep` steps each (outside the main timed region)."""
@@ -329,6 +338,7 @@ def step_percentiles(run_steps, per_rep, device, reps=60):
     times = []
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gpu_lead_in()
         a.record()
         run_steps(per_rep)
         b.record()
@@ -507,6 +517,7 @@ def run_gpu(args, rank, world, local_rank):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.mark(True)
     timed["active"] = True
+    gpu_lead_in()
     start.record()
     run_steps(args.steps)
     end.record()
@@ -544,6 +555,7 @@ def run_gpu(args, rank, world, local_rank):
             ga.replay()
     torch.cuda.synchronize()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_lead_in()
     a0.record()
     if use_graph:
         for _ in range(nat):
