@@ -21,7 +21,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
                           ElemType et, int head_dim, bool pdl, cudaStream_t stream);
 cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStream_t stream);
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
-int decode_ctas_per_sm(int head_dim);
+bool decode_swizzled(ElemType et, int head_dim);
 bool prefill_supported(int head_dim, bool bf16, int group);
 bool prefill_packed_supported(int head_dim, bool bf16, int group);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
@@ -232,19 +232,22 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     a.wv_scale = v_scale;
   }
 
+  // the decode kernel's tensor-core build takes 128B-swizzled boxes, the
+  // same maps the tensor-core prefill takes
+  const bool sw = decode_swizzled(et, head_dim);
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, false) ||
-      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, false))
+  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, sw) ||
+      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, sw))
     return PKV_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode(a, kmap, vmap, et, head_dim, /*pdl=*/true, st);
   if (e == cudaSuccess && splits > 1) e = launch_combine(a, et, head_dim, st);
   if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ) {
-    CUtensorMap qmap, kmap_sw, vmap_sw;
+    CUtensorMap qmap, kmap_sw = kmap, vmap_sw = vmap;
     if (num_tokens > 0x7FFFFFFFll || !encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim) ||
-        !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
-        !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
+        (!sw && (!encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
+                 !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))))
       return PKV_ERR_CUDA;
     e = launch_prefill(a, qmap, kmap_sw, vmap_sw, st);
   }
@@ -329,7 +332,11 @@ int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_h
   const int qd = max_query_len < kDecodeMaxQ ? (max_query_len < 1 ? 1 : max_query_len) : kDecodeMaxQ;
   const int R = decode_rows_per_tile(group, qd, false);
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((group * qd + R - 1) / R);
-  const int64_t capacity = static_cast<int64_t>(sms) * decode_ctas_per_sm(head_dim);
+  // one decode CTA per SM: the tensor-core build fits two, and the second
+  // slot is left to the next launch, whose CTAs warm L2 there before their
+  // dependency wait
+  (void)head_dim;
+  const int64_t capacity = sms;
   // As many splits as fit in 7/8 of the device in one wave (none when the
   // grid is already nearly full): every CTA's blocks in flight together, and the SMs
   // left over let the combine and the next launch's prologue become resident
@@ -484,7 +491,7 @@ int pkv_cascade_splits(int64_t num_tokens, int shared_blocks, int num_q_heads, i
   const int rows = tc ? 256 : kCascadeRows;
   const int64_t tiles = static_cast<int64_t>(num_kv_heads) * ((group * num_tokens + rows - 1) / rows);
   const int64_t target =
-      static_cast<int64_t>(sms) * (tc ? 1 : decode_ctas_per_sm(head_dim)) * 7 / 8;
+      static_cast<int64_t>(sms) * 7 / 8;
   int64_t s = target / tiles;
   int64_t by_len = tc ? (shared_blocks + 7) / 8 : shared_blocks / kMinBlocksPerSplit;
   if (s > by_len) s = by_len;
@@ -570,9 +577,10 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
   a.num_blocks = num_blocks;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
+  const bool sw = decode_swizzled(et, head_dim);
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, false) ||
-      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, false))
+  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, sw) ||
+      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, sw))
     return PKV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -595,10 +603,10 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
     p.cascade = 1;
     p.prefix_len = shared_blocks * kBlock;
     if (tc) {
-      CUtensorMap qmap, kmap_sw, vmap_sw;
+      CUtensorMap qmap, kmap_sw = kmap, vmap_sw = vmap;
       if (!encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, p.group) ||
-          !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
-          !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
+          (!sw && (!encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
+                   !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))))
         return PKV_ERR_CUDA;
       e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
     } else {

@@ -216,6 +216,18 @@ __device__ __forceinline__ int32_t ld_early(const int32_t* p) {
   return v;
 }
 
+// 32- and 64-bit read-only loads issued where they stand (volatile asm).
+__device__ __forceinline__ uint32_t ld_early_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_early_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 // Bring the 128-byte line holding p into L2 (a hint: no data is returned).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -14,48 +14,42 @@
 //   * One CTA = (split, kv head, row tile of one request).  The rows of a tile
 //     are the GQA group's query heads x the request's new tokens, so every K/V
 //     byte fetched from HBM feeds all query heads that share the kv head.
-//   * Warp-specialised CTA: consumer warps (11 for 4-row tiles, 7 otherwise)
-//     each own a private ring of shared-memory stages, one 16-token block of
-//     K and of V per stage, with "K full", "V full" and "empty" mbarriers per
-//     stage (one waiter each, so parity waits cannot alias).  Lane w of one
-//     producer warp feeds consumer warp w (blocks b0 + w, b0 + w + warps,
-//     ...): it fetches their block-table entries ahead of use, polls the
-//     warp's "empty" barriers and issues one TMA box per block for K and one
-//     for V as soon as a stage is released (K and V complete separate
-//     barriers, so a warp computes its scores while V lands).  Only the
-//     producer ever waits on the TMA unit's queue, whose per-operation cost
-//     is why a block takes two boxes and no more.
+//   * Every warp streams its own blocks (b0 + w, b0 + w + warps, ...) through
+//     its own ring of shared-memory stages, one 16-token block of K and of V
+//     per stage with a "K full" and a "V full" mbarrier each (one waiter, so
+//     parity waits cannot alias): it issues a block's TMA boxes from several
+//     lanes at once (the TMA unit serves boxes from many issuing threads in
+//     parallel, while one thread's boxes go one after another), computes its
+//     scores as soon as K lands, and refills the stage with its block P
+//     further on as soon as it has read it.  Block ids come from the table in
+//     windows of 32 tiles, one per lane, the next window loaded ahead.
+//   * Tensor-core build (bf16 caches, and E4M3 caches of head_dim 128): the
+//     tile's rows are the M dimension of mma.sync m16n8k16 for both Q.K^T
+//     and P.V (K and V read from 128B-swizzled stages by ldmatrix, or as E4M3
+//     codes widened to f16 in registers), with a lagged reference max per row;
+//     four warps and a 96 KB ring, so two CTAs fit on an SM.
+//   * CUDA-core build (fp32 caches, E4M3 at head_dim 64): a register-q path
+//     for one token of a 4-head group (each lane dots a 16-dim slice of the
+//     four q rows with packed fp32 FMAs, a transpose-reduce over 8 lanes) and
+//     a generic path (lanes own keys, q staged in shared memory).
 //   * Before the programmatic-dependent-launch wait (while the previous
 //     kernel finishes) the CTA sets up its barriers, prefetches the tensor
 //     maps and warms L2 with the K/V blocks it will most likely read; every
 //     input it then uses is read after the wait.
-//   * In split launches each consumer warp's first block is loaded right
-//     after the wait from the block id read before it, and kept only if the
-//     metadata and table read after the wait confirm it; otherwise that fill
-//     is discarded (its stage's phases then run one ahead, and the warp is
-//     told so only once the discarded fill has landed).
-//   * Generic path: a warp takes one 16-key block per stage; lanes j and
-//     j + 16 dot the two halves of key j's row against q in shared memory
-//     (each lane's chunk order is rotated by its key, so the reads do not
-//     conflict), one shuffle adds the halves, the row max is a shuffle tree,
-//     exp2 works in the log2 domain, then lanes own D/32 output columns for
-//     P.V.
-//   * Register-q path (bf16, 4-row tiles, the decode hot case): each lane
-//     holds a 16-dim slice of the four q rows in registers (loaded straight
-//     from global memory, no CTA-wide barrier), dots 4 keys with packed fp32
-//     FMAs and a transpose-reduce over the 8 slice lanes leaves it 2 scores
-//     of one row; P.V pairs rows in each packed FMA.
+//   * In split launches each warp's first block is loaded right after the
+//     wait from the block id read before it, and kept only if the metadata
+//     and table read after the wait confirm it; otherwise the warp lets that
+//     fill land and its stage's phases run one ahead.
 //   * Each warp keeps its own (m, l, acc); the warps are merged through shared
 //     memory at the end (same algebra as the split merge).
 //   * Bounded mbarrier waits: a stuck pipeline sets PKV_FLAG_TIMEOUT and exits.
-//   * Variants over the same pipeline: E4M3 caches (codes widened to fp32 in
-//     registers, k/v scales folded into the score scale and the epilogue);
-//     sliding windows (a tile's range starts at its first row's window, each
-//     row masks below its own); the cascade passes (every row of the batch
-//     over a shared prefix, or a request's own keys, written as fp32
-//     partials); and the fused write (consumer warp 0 stores the step's new
-//     K/V rows this CTA reads, and the producer loads a block holding one only
-//     after a barrier says they are stored).
+//   * Variants over the same pipeline: E4M3 caches (k/v scales folded into
+//     the score scale and the epilogue); sliding windows (a tile's range
+//     starts at its first row's window, each row masks below its own); the
+//     cascade passes (every row of the batch over a shared prefix, or a
+//     request's own keys, written as fp32 partials); and the fused write
+//     (warp 0 stores the step's new K/V rows this CTA reads, and a block
+//     holding one is loaded only after a barrier says they are stored).
 #include <type_traits>
 
 #include "common.cuh"
@@ -117,47 +111,161 @@ __device__ __forceinline__ void mul2(f32x2& acc, f32x2 a) {
 }
 __device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pack2(bf16_lo(w), bf16_hi(w)); }
 
+// ---- warp-level tensor-core helpers (mma.sync m16n8k16, ldmatrix) ----
+// D += A.B for a 16x16 A (four .b32 registers: rows g and g+8, k 2q..2q+1 and
+// 2q+8..2q+9 for lane 4g+q) and a 16x8 B (two registers: k 2q..2q+1 and
+// 2q+8..2q+9, column g); D rows g (d0, d1) and g+8 (d2, d3), columns 2q, 2q+1.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float& d0, float& d1, float& d2, float& d3,
+                                         uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// Four 8x8 16-bit matrices from shared memory: lane l gives the address of
+// row l % 8 of matrix l / 8; register i receives matrix i (plain: row l / 4,
+// columns 2(l % 4), +1; .trans: the transposed matrix's).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+// Transpose of an 8x8 16-bit matrix held one .b32 (row l / 4, columns
+// 2 (l % 4), +1) per lane: lane l receives the same slots of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// two E4M3 codes (low 16 bits, element 0 in the low byte) -> f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 c, u;\n\tmov.b32 {c, u}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h2)
+      : "r"(two_codes));
+  return h2;
+}
+// (lo, hi) -> bf16x2 / f16x2, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  float f;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}"
+      : "=f"(f)
+      : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  float f;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}"
+      : "=f"(f)
+      : "r"(w));
+  return f;
+}
+
+// Tensor-core (mma.sync m16n8k16) build of the decode kernel: bf16 caches
+// (head_dim 64 or 128) and E4M3 caches of head_dim 128.  The GQA group's
+// rows (up to 16 per tile) are the M dimension of both contractions, so one
+// K/V tile feeds every query head of its kv head through the tensor cores
+// and a 16-key block costs a warp about a hundred instructions instead of
+// several hundred of CUDA-core FMAs.  fp32 caches and E4M3 at head_dim 64
+// keep the CUDA-core build.
+template <typename T, int D>
+constexpr bool kMmaBuild = (sizeof(T) == 2 && (D == 64 || D == 128)) || (kIsE4m3<T> && D == 128);
+
 template <typename T, int D, int R = 4>
 struct DecodeCfg {
+  static constexpr bool kMma = kMmaBuild<T, D>;
   static constexpr int kRowBytes = D * static_cast<int>(sizeof(T));
   static constexpr int kHalfChunks = kRowBytes / 32;      // 16-byte chunks per half key row
-  // K and V each arrive as one unswizzled TMA box per block (16 rows of the
-  // head's kRowBytes): the register-q path has the 8 lanes of a quarter-warp
-  // read 8 consecutive 16-byte chunks of one key row, the generic path
-  // rotates each lane's chunk order by its key, so neither conflicts on
-  // shared-memory banks.
+  // CUDA-core build: K and V each arrive as one unswizzled TMA box per block
+  // (16 rows of the head's kRowBytes); the register-q path has the 8 lanes of
+  // a quarter-warp read 8 consecutive 16-byte chunks of one key row, the
+  // generic path rotates each lane's chunk order by its key, so neither
+  // conflicts on shared-memory banks.  Tensor-core build: each 128-byte
+  // column slice of a row is its own box in the 128B-swizzled layout, so the
+  // ldmatrix row reads of 8 consecutive keys hit 8 distinct bank groups.
+  static constexpr int kBoxes = kMma ? kRowBytes / 128 : 1;
+  static constexpr int kBoxBytes = kBlock * kRowBytes / kBoxes;
   static constexpr int kStageBytes = 2 * kBlock * kRowBytes;   // one block of K and of V
-  // Consumer (compute) warps per CTA.  With the producer warp the CTA has 12
-  // warps (three per SM sub-partition, 168 registers each) for 4-row tiles,
-  // whose register-q path fits that budget; wider tiles keep 255 registers
-  // with 7 + 1 warps.
-  static constexpr int kWarps = R == 4 ? 11 : 7;
-  // A 192 KB ring per CTA (one CTA per SM): 3 blocks in flight per warp for
-  // 256-byte rows, so a 19-way split of an 8K context has every block in
-  // flight at once and longer contexts keep two prefetched per warp.
-  static constexpr int kStagesRaw = 196608 / (kWarps * kStageBytes);
+  // Consumer (compute) warps per CTA, plus one TMA producer warp.  CUDA-core
+  // build: 11 + 1 warps (three per SM sub-partition, 168 registers each) for
+  // 4-row tiles, whose register-q path fits that budget; wider tiles keep
+  // 255 registers with 7 + 1 warps; one CTA per SM.  Tensor-core build: 4 + 1
+  // warps and a 96 KB ring, so two CTAs fit on an SM and the next launch's
+  // CTAs become resident (and warm L2) while this one streams.
+  static constexpr int kWarps = kMma ? 4 : (R == 4 ? 11 : 7);
+  static constexpr int kRingBudget = kMma ? 98304 : 196608;
+  static constexpr int kStagesRaw = kRingBudget / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 6 ? 6 : kStagesRaw);
   static constexpr int kStages = kWarps * kStagesPerWarp;
-  // Blocks per CTA warmed into L2 before the dependent-launch wait: each
-  // consumer warp's first block.  Warming more floods the memory queues that
-  // the previous kernel's last loads (the split combine) wait in.
-  static constexpr int kPrefetchBlocks = kWarps;
+  static constexpr int kMinBlocksPerSm = kMma ? 2 : 1;
+  // Blocks per CTA warmed into L2 before the dependent-launch wait.  CUDA-core
+  // build: each consumer warp's first block (warming more floods the memory
+  // queues that the previous kernel's last loads wait in, with one CTA per
+  // SM).  Tensor-core build: a split launch's whole range up to this cap (its
+  // CTAs are resident beside the previous launch's), else the first ring fill.
+  static constexpr int kPrefetchBlocks = kMma ? 64 : kWarps;
   static constexpr int kConsumerThreads = kWarps * 32;
   static constexpr int kThreads = kConsumerThreads + 32;  // + one TMA producer warp
+  // producer lanes: one per (consumer warp, K or V, 128-byte box), so every
+  // TMA box of a block is issued by a thread of its own
+  static constexpr int kIssueLanes = kWarps * 2 * kBoxes;
+  static_assert(kIssueLanes <= 32, "one producer lane per box");
   static constexpr int kDPL = D / 32;                     // output columns per lane
   static constexpr int kPairs = kDPL / 2;
   static_assert((kHalfChunks & (kHalfChunks - 1)) == 0, "chunks per half row: power of two");
+  static_assert(!kMma || kRowBytes % 128 == 0, "tensor-core build: rows of whole 128-byte slices");
 };
 
 template <typename T, int D, int R>
 struct DecodeSmem {
   using C = DecodeCfg<T, D, R>;
   static constexpr int kStageArea = C::kStages * C::kStageBytes;
-  static constexpr int kMergeBytes = C::kWarps * R * (D + 2) * 4;
+  static constexpr int kMergeBytes = C::kWarps * R * (D + 3) * 4;   // m, l, l~, acc per row
   static constexpr int kRingBytes = kStageArea > kMergeBytes ? kStageArea : kMergeBytes;
+  // q rows and the P tile live in registers in the tensor-core build
   static constexpr int kQOff = kRingBytes;
-  static constexpr int kPOff = kQOff + R * D * 4;
-  static constexpr int kBarOff = kPOff + C::kWarps * kBlock * R * 8;
+  static constexpr int kPOff = kQOff + (C::kMma ? 0 : R * D * 4);
+  static constexpr int kBarOff = kPOff + (C::kMma ? 0 : C::kWarps * kBlock * R * 8);
   // kfull[], vfull[], empty[], then per consumer warp the barrier and the
   // verdict of its speculative first block
   static constexpr int kSpecOff = kBarOff + 3 * C::kStages * 8;
@@ -258,20 +366,21 @@ __device__ __forceinline__ void load_v_pairs(const uint8_t* vrow, int lane,
 // SPEC: build with the speculative first blocks (used for split launches of
 // 4-row tiles; unsplit launches run the build without, which measures faster)
 template <typename T, int D, int R, bool SPEC>
-__global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
+__global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, R>::kMinBlocksPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   using C = DecodeCfg<T, D, R>;
   using Sm = DecodeSmem<T, D, R>;
   constexpr int P = C::kStagesPerWarp;
-  // Register-q path for one token of a 4-query-head GQA group in bf16 (the
-  // decode hot case); every other shape takes the generic path below.
+  constexpr int W = C::kWarps;
+  // Register-q path for one token of a 4-query-head GQA group (CUDA-core
+  // build); every other CUDA-core shape takes the generic path below.
   using QT = typename QType<T>::type;                  // q / out element type
-  constexpr bool kFast = (sizeof(T) == 2 || kIsE4m3<T>) && R == 4;
+  constexpr bool kMma = C::kMma;                      // tensor-core build (see DecodeCfg)
+  constexpr bool kFast = !kMma && (sizeof(T) == 2 || kIsE4m3<T>) && R == 4;
   constexpr int kFastChunks = D / 64;                 // 16-byte q chunks per row and lane
   // speculative first blocks (below) for the 4-row tiles of split launches,
-  // where each CTA's first block is on the critical path; wider tiles keep
-  // their registers for the generic path
+  // where each CTA's first block is on the critical path
   constexpr bool kSpec = SPEC && R == 4;
   // whether this CTA may speculate (same answer on every thread)
   const bool spec_possible =
@@ -290,7 +399,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   uint64_t* wr_bar = reinterpret_cast<uint64_t*>(smem + Sm::kWrOff);   // fused write stored
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool producer = warp == C::kWarps;
+  const bool producer = warp == W;
+  // producer lane -> (consumer warp pw, box part pp: K boxes, then V boxes)
+  const int pw = lane / (2 * C::kBoxes), pp = lane % (2 * C::kBoxes);
+  const bool p_act = producer && lane < C::kIssueLanes;
   const int g = blockIdx.x % a.hkv;
   const int s = blockIdx.x / a.hkv;
   const int z = blockIdx.y;
@@ -304,49 +416,51 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&kfull[i], 1);
       mbar_init(&vfull[i], 1);
-      if (i < C::kWarps) mbar_init(&spec_bar[i], 1);
-      if (i == 0) mbar_init(wr_bar, 1);
       mbar_init(&empty[i], 1);
     }
+    for (int i = 0; i < W; ++i) mbar_init(&spec_bar[i], 1);
+    mbar_init(wr_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
   const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
-  int32_t e_hint = 0;                  // producer lane w: hinted entry of warp w's first block
+  // the split range a context of max_seq_len keys gives (the pre-launch hint)
+  const int nb_spec = min((a.max_seq_len + kBlock - 1) / kBlock, a.max_blocks_per_seq);
+  const int per_spec = a.num_splits > 1 ? (nb_spec + a.num_splits - 1) / a.num_splits : nb_spec;
+  const int spec_b0 = min(s * per_spec, nb_spec);
+  int32_t e_hint = 0;                  // producer lane: hinted entry of warp pw's first block
   bool hint_ok = false;
-  if (producer && z == 0 && a.window == 0 && a.cascade == 0) {
+  if (z == 0 && a.window == 0 && a.cascade == 0) {
     // ---- L2 warm-up while the previous kernel finishes: the K/V blocks this
-    //      CTA will most likely read (the split range a context of
-    //      max_seq_len keys gives, cut at the request's length and at
-    //      kPrefetchBlocks) are prefetched into L2.  The table and lengths
-    //      read here may still change before the wait, so they only steer
-    //      prefetches: every value used below is re-read after the wait, and
-    //      L2 stays coherent with the previous kernel's writes.  Only the
-    //      first row tile of a request this kernel will run warms L2 (the
-    //      others share its blocks or exit at once). ----
-    const int nb_spec = min((a.max_seq_len + kBlock - 1) / kBlock, a.max_blocks_per_seq);
-    const int per_spec = a.num_splits > 1 ? (nb_spec + a.num_splits - 1) / a.num_splits : nb_spec;
-    const int sb0 = min(s * per_spec, nb_spec);
+    //      CTA will most likely read (the hinted split range, cut at the
+    //      request's length, the table row and a cap), each warp its own
+    //      tiles.  The table and lengths read here may still change before the
+    //      wait, so they only steer prefetches: every value used below is
+    //      re-read after the wait, and L2 stays coherent with the previous
+    //      kernel's writes.  Only the first row tile of a request warms L2
+    //      (the others share its blocks or exit at once). ----
     // L2-only loads (ld.global.cg): nothing read before the wait may sit in L1,
     // where the read-only loads after the wait could find a stale copy
     const int len_hint = min(max(__ldcg(a.seq_lens + r), 0), a.max_seq_len);
     const int n_hint = __ldcg(a.qsl + r + 1) - __ldcg(a.qsl + r);
     const bool runs_here = n_hint >= 1 && (n_hint <= kDecodeMaxQ || a.long_rows);
-    // (capped at nb_spec: never past the table row, whatever the hinted length)
-    const int sb1 = !runs_here ? sb0
-                               : min(min(min(sb0 + per_spec, (len_hint + kBlock - 1) / kBlock),
-                                         sb0 + C::kPrefetchBlocks),
+    // tensor-core build without a split: the blocks of the first ring fill
+    const int pf_cap = kMma && a.num_splits == 1 ? C::kStages : C::kPrefetchBlocks;
+    const int sb1 = !runs_here ? spec_b0
+                               : min(min(min(spec_b0 + per_spec, (len_hint + kBlock - 1) / kBlock),
+                                         spec_b0 + pf_cap),
                                      nb_spec);
     constexpr int kLines = C::kRowBytes / 128 > 0 ? C::kRowBytes / 128 : 1;  // lines per row
     const int64_t head_off = static_cast<int64_t>(g) * C::kRowBytes;
     const int64_t slot_bytes = static_cast<int64_t>(a.hkv) * C::kRowBytes;
-    for (int base = sb0; base < sb1; base += 32) {
-      const int32_t e = base + lane < sb1 ? __ldcg(table + base + lane) : -1;
-      if (spec_possible && base == sb0 && lane < C::kWarps && base + lane < sb1) {
-        e_hint = e;
-        hint_ok = true;
-      }
-      for (int i = 0; i < 32 && base + i < sb1; ++i) {
+    if (p_act && spec_possible && spec_b0 + pw < sb1) {
+      e_hint = __ldcg(table + spec_b0 + pw);
+      hint_ok = true;
+    }
+    for (int j0 = 0; !producer && spec_b0 + warp + W * j0 < sb1; j0 += 32) {
+      const int bb = spec_b0 + warp + W * (j0 + lane);
+      const int32_t e = bb < sb1 ? __ldcg(table + bb) : -1;
+      for (int i = 0; i < 32 && spec_b0 + warp + W * (j0 + i) < sb1; ++i) {
         const int32_t id = __shfl_sync(0xffffffffu, e, i);
         if (id < 0 || id >= a.num_blocks) continue;
         for (int u = lane; u < kBlock * kLines; u += 32) {
@@ -359,53 +473,83 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     }
   }
 
-  // ---- request geometry (uniform over the CTA); inputs only after the wait ----
+  // where this request's rows start in q (an address hint, read L2-only)
+  const int q0_hint = kMma && !producer && a.cascade != 1 ? __ldcg(a.qsl + r) : 0;
+
+  // ---- inputs only after the wait ----
   pdl_wait_primary();
   pdl_launch_dependents();
-  // Speculative first block: producer lane w loads warp w's first block of the
-  // hinted split range into the warp's stage 0 at once - the K/V data is read
-  // after the wait, only the block id comes from the hint.  The block is kept
-  // (used) only if the metadata and table read below confirm that block id as
-  // the warp's first; otherwise the stage's first fill is wasted and the
-  // stage's phases shift by one.  An out-of-range hint loads rows -16..-1,
-  // which TMA fills with zeros without reading memory.
-  bool spec_issued = false;
-  if (producer && hint_ok) {
-    uint8_t* ks = smem + (lane * P) * C::kStageBytes;
-    uint8_t* vs = ks + kBlock * C::kRowBytes;
-    const int row = (e_hint >= 0 && e_hint < a.num_blocks) ? e_hint * kBlock : -kBlock;
-    const uint64_t pol0 = l2_policy_evict_first();
-    mbar_arrive_expect_tx(&kfull[lane * P], kBlock * C::kRowBytes);
-    tma_load_3d(ks, &kmap, &kfull[lane * P], 0, g, row, pol0);
-    mbar_arrive_expect_tx(&vfull[lane * P], kBlock * C::kRowBytes);
-    tma_load_3d(vs, &vmap, &vfull[lane * P], 0, g, row, pol0);
-    spec_issued = true;
-  }
-  // every exit from here on first lets a speculative load land (bounded)
-  auto drain_spec = [&]() {
-    if (spec_issued) {
-      mbar_wait(&kfull[lane * P], 0);
-      mbar_wait(&vfull[lane * P], 0);
+  // Tensor-core build: the q rows of this tile are loaded at once from the
+  // hinted start (token index kept inside q, so every load is in bounds),
+  // in flight together with the metadata; reloaded below if the metadata
+  // puts the rows elsewhere.  bf16 cache: k-step t covers dims 16t..16t+15 in
+  // order.  E4M3 cache (f16 MMAs): k-step t of lane kq covers dims
+  // 32kq + 4t .. +3, so that a lane's K codes for all k-steps are 32
+  // consecutive bytes of a key row (the dot product is indifferent to the
+  // order of its terms).
+  constexpr int kMT = kMma ? D / 16 : 1;               // k-steps of Q.K^T
+  constexpr bool kHi = R == 16;                        // M-rows 8..15 are tile rows
+  constexpr int kHR = kHi ? 2 : 1;                     // M-row halves this lane holds
+  const int g8 = lane >> 2, kq = lane & 3;
+  uint32_t qw[kHR][kMT][2];
+  auto load_q = [&](int q0v) {
+#pragma unroll
+    for (int hr = 0; hr < kHR; ++hr) {
+      const int rr = blockIdx.y * R + g8 + 8 * hr;
+      const int64_t tok = min(max(static_cast<int64_t>(q0v) + rr / a.group, int64_t{0}),
+                              a.num_tokens - 1);
+      const QT* qp = static_cast<const QT*>(a.q) + (tok * a.hq + g * a.group + rr % a.group) * D;
+#pragma unroll
+      for (int t = 0; t < kMT; ++t) {
+        if constexpr (kIsE4m3<T>) {
+          const uint2 v = ld_early_v2(qp + 32 * kq + 4 * t);
+          qw[hr][t][0] = v.x;
+          qw[hr][t][1] = v.y;
+        } else {
+          qw[hr][t][0] = ld_early_u32(qp + 16 * t + 2 * kq);
+          qw[hr][t][1] = ld_early_u32(qp + 16 * t + 8 + 2 * kq);
+        }
+      }
     }
   };
-  // The block-table entries of each consumer warp's first two blocks,
-  // fetched speculatively (producer lane w for warp w) for the split range a
-  // context of max_seq_len keys would give, in flight together with the
-  // metadata; kept if the real range starts at the same block, so the first
-  // K/V loads go out as soon as the metadata arrives.
-  int spec_b0 = -1;
-  int32_t spec_e0 = 0, spec_e1 = 0;
-  bool spec_v0 = false, spec_v1 = false;              // loaded (inside the bound)
-  if (producer && lane < C::kWarps) {
-    const int nb_spec = min((a.max_seq_len + kBlock - 1) / kBlock, a.max_blocks_per_seq);
-    const int per_spec = a.num_splits > 1 ? (nb_spec + a.num_splits - 1) / a.num_splits : nb_spec;
-    spec_b0 = min(s * per_spec, nb_spec);
-    const int bb = spec_b0 + lane;
-    spec_v0 = bb < nb_spec;
-    spec_v1 = bb + C::kWarps < nb_spec;
-    if (spec_v0) spec_e0 = ld_early(table + bb);
-    if (spec_v1) spec_e1 = ld_early(table + bb + C::kWarps);
+  if constexpr (kMma) {
+    if (!producer) load_q(q0_hint);
   }
+  // Producer lane (pw, pp) issues box pp of each block of consumer warp pw:
+  // TMA boxes from many issuing threads proceed in parallel, while one
+  // thread's boxes go one after another.  The first box of K (of V) posts its
+  // barrier's byte count.
+  const uint64_t pol = l2_policy_evict_first();
+  auto issue_box = [&](int st, int row) {
+    const int b = pp % C::kBoxes;
+    const bool v = pp >= C::kBoxes;
+    uint64_t* bar = v ? &vfull[st] : &kfull[st];
+    if (b == 0) mbar_arrive_expect_tx(bar, kBlock * C::kRowBytes);
+    tma_load_3d(smem + st * C::kStageBytes + (v ? kBlock * C::kRowBytes : 0) + b * C::kBoxBytes,
+                v ? &vmap : &kmap, bar, b * (128 / static_cast<int>(sizeof(T))), g, row, pol);
+  };
+  // Speculative first block: warp pw's first block of the hinted split range
+  // goes into its stage 0 at once - the K/V data is read after the wait,
+  // only the block id comes from the hint.  It is kept (used) only if the
+  // metadata and table read below confirm that block id as the warp's first;
+  // otherwise the fill is wasted and that stage's phases shift by one.  An
+  // out-of-range hint loads rows -16..-1, which TMA fills with zeros without
+  // reading memory.
+  const bool spec_issued = p_act && spec_possible && hint_ok;
+  if (spec_issued)
+    issue_box(pw * P, (e_hint >= 0 && e_hint < a.num_blocks) ? e_hint * kBlock : -kBlock);
+  // every exit from here on first lets a speculative load land (bounded)
+  auto drain_spec = [&]() {
+    if (spec_issued) mbar_wait(pp >= C::kBoxes ? &vfull[pw * P] : &kfull[pw * P], 0);
+  };
+  // The table entries of warp pw's first two blocks of the hinted split range,
+  // read now (after the wait), together with the metadata: the verdict on the
+  // speculative block and the first loads need no second round trip when the
+  // real range starts at the hinted block.
+  const bool spec_v0 = p_act && spec_b0 + pw < nb_spec;
+  const bool spec_v1 = p_act && spec_b0 + pw + W < nb_spec;
+  const int32_t spec_e0 = spec_v0 ? ld_early(table + spec_b0 + pw) : 0;
+  const int32_t spec_e1 = spec_v1 ? ld_early(table + spec_b0 + pw + W) : 0;
   // cascade prefix pass: one request holding every row of the batch, over the
   // prefix_len shared keys
   const bool prefix_pass = a.cascade == 1;
@@ -472,18 +616,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   }
   const int key_end = min(kv_len, b1 * kBlock);       // keys of this split: [b0*16, key_end)
   // fused write: the new-token rows this CTA reads, positions [fw_lo, fw_hi)
-  // (head g); consumer warp 0 stores them, and the producer issues a block
-  // holding one only after that (wr_bar)
+  // (head g); warp 0 stores them, and a block holding one is loaded only
+  // after that (wr_bar)
   const int fw_lo = a.fuse_write ? max(L - n, b0 * kBlock) : 0;
   const int fw_hi = a.fuse_write ? key_end : 0;
   const int nt = b1 - b0;                              // one block per stage
-  const int my_tiles = nt > warp ? (nt - warp + C::kWarps - 1) / C::kWarps : 0;
+  const int my_tiles = nt > warp ? (nt - warp + W - 1) / W : 0;
 
   // q elements this thread stages (generic path), loaded before the causal
   // limits are worked out so the loads are in flight meanwhile
-  constexpr int kQPer = kFast ? 1 : (R * D + C::kConsumerThreads - 1) / C::kConsumerThreads;
+  constexpr int kQPer = kFast || kMma ? 1 : (R * D + C::kConsumerThreads - 1) / C::kConsumerThreads;
   QT qraw[kQPer];
-  if constexpr (!kFast) {
+  if constexpr (!kFast && !kMma) {
 #pragma unroll
     for (int u = 0; u < kQPer; ++u) {
       const int e = threadIdx.x + u * C::kConsumerThreads;
@@ -533,78 +677,108 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     lo[rho] = wlo + (rho0 + rho) / group;
   }
 
+  // ---- tensor-core build state.  Both contractions are taken transposed,
+  //      S^T = K.Q^T and O^T = V^T.P^T, so the 16 keys of a block (and 16
+  //      dims of O) fill the M dimension and the tile's rows the N dimension
+  //      (8 per n-tile h; 16-row tiles have two): lane 4*g8 + kq holds the B
+  //      operand of Q^T for rows 8h + g8 per 16-dim k-step, and for rows
+  //      8h + 2kq + e (e = 0, 1) the running max (log2 domain, a lagged
+  //      reference: moved only when a block's max passes it by more than
+  //      kLag, so p <= 2^kLag), its partial sums of p (fp32: the row's mass,
+  //      for the LSE and the split weights) and of p as rounded into the
+  //      16-bit P operand (the accumulator's own normaliser, so the output is
+  //      an exact weighted average of V rows), and the O^T accumulator per
+  //      16-dim m-tile. ----
+  constexpr int kMD = kMma ? D / 16 : 1;               // m-tiles of O^T (16 dims each)
+  constexpr float kLag = 8.f;
+  uint32_t qa[kMT][2 * kHR];                           // [t][rows 8h + g8: k lo, k hi per h]
+  float oacc[kMD][kHR][4];                             // O^T: dims g8 (c0, c1), g8 + 8 (c2, c3)
+  float mm[kHR][2], ll[kHR][2], lr[kHR][2];
+  int mlim[kHR][2], mlo[kHR][2];
+  float score_scale = a.scale_log2;
+#pragma unroll
+  for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      mm[hr][e] = -INFINITY;
+      ll[hr][e] = 0.f;
+      lr[hr][e] = 0.f;
+      const int i_row = (rho0 + 8 * hr + 2 * kq + e) / group;   // token (padding rows too)
+      mlim[hr][e] = min(key_end, a.causal ? (L - n + i_row + 1) : L);
+      mlo[hr][e] = wlo + i_row;
+    }
+#pragma unroll
+  for (int mt = 0; mt < kMD; ++mt)
+#pragma unroll
+    for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) oacc[mt][hr][c] = 0.f;
+
   if (producer) {
-    // ---- TMA producer: lane w feeds consumer warp w (blocks b0 + w + kWarps*j).
-    //      It polls the "empty" barrier of the warp's next stage without
-    //      blocking and, once the stage is released, issues the block's K and V
-    //      loads; lanes whose stages are free issue together.  The compute
-    //      warps never stall behind the TMA unit's queue. ----
-    const uint64_t pol = l2_policy_evict_first();
-    const int w = lane;
-    const int tiles = (w < C::kWarps && nt > w) ? (nt - w + C::kWarps - 1) / C::kWarps : 0;
+    // ---- TMA producer: lane (pw, pp) issues box pp of every block of
+    //      consumer warp pw (blocks b0 + pw + W j).  It polls the "empty"
+    //      barrier of the warp's next stage without blocking and issues its
+    //      box as soon as the stage is released; the lanes of ready stages
+    //      issue together.  The compute warps never stall behind the TMA
+    //      unit. ----
+    const int tiles = (p_act && nt > pw) ? (nt - pw + W - 1) / W : 0;
     auto entry_of = [&](int jj) -> int32_t {
-      return jj < tiles ? ld_early(table + b0 + w + C::kWarps * jj) : 0;
+      return jj < tiles ? ld_early(table + b0 + pw + W * jj) : 0;
     };
-    const bool spec_ok = spec_b0 == b0;
     // a speculative first block holding new-token rows of a fused write was
     // loaded before they were stored: discard it
-    const int sb = b0 + w;
+    const int sb = b0 + pw;
     const bool spec_clash = fw_lo < fw_hi && sb * kBlock < fw_hi && (sb + 1) * kBlock > fw_lo;
+    const bool spec_ok = spec_b0 == b0;                 // the real range starts at the hint
+    int32_t e_cur = spec_ok && spec_v0 ? spec_e0 : entry_of(0);
+    int32_t e_next = spec_ok && spec_v1 ? spec_e1 : entry_of(1);
     // verdict on the speculative first block: 0 none, 1 used as tile 0,
     // 2 wasted (stage 0's phases then run one ahead of its tiles)
-    const bool used = spec_issued && spec_ok && tiles > 0 && spec_v0 && spec_e0 == e_hint &&
+    const bool used = spec_issued && spec_ok && spec_v0 && tiles > 0 && spec_e0 == e_hint &&
                       !spec_clash;
     const int verdict = !spec_issued ? 0 : (used ? 1 : 2);
     if (verdict == 2) {
       // a wasted fill lands before the verdict is published (the consumer's
       // parity waits on stage 0 rely on it), bounded like every wait
-      if (!mbar_wait(&kfull[w * P], 0) || !mbar_wait(&vfull[w * P], 0))
+      if (!mbar_wait(pp >= C::kBoxes ? &vfull[pw * P] : &kfull[pw * P], 0))
         raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     }
-    if (spec_possible && w < C::kWarps) {
-      spec_state[w] = verdict;
-      mbar_arrive(&spec_bar[w]);
+    __syncwarp();
+    if (spec_possible && p_act && pp == 0) {
+      spec_state[pw] = verdict;
+      mbar_arrive(&spec_bar[pw]);
     }
-    if (used && (e_hint < 0 || e_hint >= a.num_blocks)) raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
+    if (used && pp == 0 && (e_hint < 0 || e_hint >= a.num_blocks))
+      raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
     const int shift0 = verdict == 2;
-    int jj = used ? 1 : 0;
-    int32_t e_cur, e_next;
+    int jj = 0;
     if (used) {
-      e_cur = spec_ok && spec_v1 ? spec_e1 : entry_of(1);
+      jj = 1;
+      e_cur = e_next;
       e_next = entry_of(2);
-    } else {
-      e_cur = spec_ok && spec_v0 ? spec_e0 : entry_of(0);
-      e_next = spec_ok && spec_v1 ? spec_e1 : entry_of(1);
     }
     unsigned long long t_progress = 0;
     while (__any_sync(0xffffffffu, jj < tiles)) {
       bool ready = false;
       if (jj < tiles) {
-        const int st = w * P + jj % P;
+        const int st = pw * P + jj % P;
         ready = jj < P || mbar_ready(&empty[st], ((jj / P) - 1) & 1);
         // a wasted speculative fill must land before stage 0 is filled again
         if (ready && jj == 0 && shift0)
           ready = mbar_ready(&kfull[st], 0) && mbar_ready(&vfull[st], 0);
         // a block holding rows of the fused write only once they are stored
         if (ready && fw_lo < fw_hi) {
-          const int bi = b0 + w + C::kWarps * jj;
+          const int bi = b0 + pw + W * jj;
           if (bi * kBlock < fw_hi && (bi + 1) * kBlock > fw_lo) ready = mbar_ready(wr_bar, 0);
         }
         if (ready) {
           int id = e_cur;
           if (id < 0 || id >= a.num_blocks) {
-            raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
+            if (pp == 0) raise_flag(a.flag, PKV_FLAG_BAD_BLOCK);
             id = 0;
           }
-          uint8_t* ks = smem + st * C::kStageBytes;
-          uint8_t* vs = ks + kBlock * C::kRowBytes;
           if (jj >= P) fence_proxy_async_smem();   // the warp's reads of the stage before a refill
-          // K and V on their own barriers: all ready lanes' K boxes go out
-          // first, and a consumer starts its scores while V is landing
-          mbar_arrive_expect_tx(&kfull[st], kBlock * C::kRowBytes);
-          tma_load_3d(ks, &kmap, &kfull[st], 0, g, id * kBlock, pol);
-          mbar_arrive_expect_tx(&vfull[st], kBlock * C::kRowBytes);
-          tma_load_3d(vs, &vmap, &vfull[st], 0, g, id * kBlock, pol);
+          issue_box(st, id * kBlock);
           ++jj;
           e_cur = e_next;
           e_next = entry_of(jj + 1);
@@ -623,17 +797,60 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
         __nanosleep(32);
       }
     }
-    // every load this lane issued has landed before the merge reuses the ring
+    // every box this lane issued has landed before the merge reuses the ring
     // (a no-op unless a consumer gave up early); bounded like every wait
-    for (int q = 0; q < P; ++q) {
+    for (int q = 0; p_act && q < P; ++q) {
       const int c = (jj > q ? (jj - q + P - 1) / P : 0) + (q == 0 ? shift0 : 0);  // fills of stage q
-      if (c > 0 && (!mbar_wait(&kfull[w * P + q], (c - 1) & 1) ||
-                    !mbar_wait(&vfull[w * P + q], (c - 1) & 1)))
+      if (c > 0 && !mbar_wait(pp >= C::kBoxes ? &vfull[pw * P + q] : &kfull[pw * P + q], (c - 1) & 1))
         break;
     }
     __syncwarp();
   } else {
-    if constexpr (kFast) {
+    if constexpr (kMma) {
+      // ---- q as the A operand (loaded right after the wait): reloaded if
+      //      the metadata puts the rows elsewhere; rows past the tile's are
+      //      zero.  E4M3 cache: q is scaled by a power of two bringing max|q|
+      //      into [2^14, 2^15), where f16 holds every bf16 value exactly, and
+      //      the score scale takes the inverse. ----
+      if (q0 != (prefix_pass ? 0 : q0_hint)) load_q(q0);
+#pragma unroll
+      for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+        for (int t = 0; t < kMT; ++t)
+          if (g8 + 8 * hr >= nrows) qw[hr][t][0] = qw[hr][t][1] = 0u;
+      if constexpr (kIsE4m3<T>) {
+        float mx = 0.f;
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+          for (int t = 0; t < kMT; ++t)
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(qw[hr][t][u])), fabsf(bf16_hi(qw[hr][t][u]))));
+        mx = warp_max(mx);
+        int e = 0;
+        if (mx > 0.f && mx <= 3.0e38f) e = ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14;
+        e = max(-100, min(100, e));
+        const float qs = __int_as_float((127 - e) << 23);          // 2^-e
+        score_scale = a.scale_log2 * __int_as_float((127 + e) << 23);
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+          for (int t = 0; t < kMT; ++t)
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              qa[t][2 * hr + u] =
+                  pack_f16x2(bf16_lo(qw[hr][t][u]) * qs, bf16_hi(qw[hr][t][u]) * qs);
+      } else {
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+          for (int t = 0; t < kMT; ++t) {
+            qa[t][2 * hr] = qw[hr][t][0];
+            qa[t][2 * hr + 1] = qw[hr][t][1];
+          }
+      }
+    } else if constexpr (kFast) {
       // this lane's q slice of all four rows straight from global memory (no
       // CTA-wide staging), pre-scaled into the log2 domain
       uint4 qv[4][kFastChunks];
@@ -728,9 +945,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       // parity-1 wait for tile 0 cannot pass early
       shift0 = spec_state[warp] == 2 ? 1 : 0;
     }
-    int j = 0;
-    for (; j < my_tiles; ++j) {
-      const int blk = b0 + warp + C::kWarps * j;
+    for (int j = 0; j < my_tiles; ++j) {
+      const int blk = b0 + warp + W * j;
       const int st = warp * P + (j % P);
       const int ph = (j / P + (j % P == 0 ? shift0 : 0)) & 1;   // phase of this fill
       const bool got = mbar_wait(&kfull[st], ph);
@@ -743,7 +959,192 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
       const int key0 = blk * kBlock;
       const int nvalid = min(kBlock, key_end - key0);
 
-      if constexpr (kFast) {
+      if constexpr (kMma) {
+        constexpr bool kF16 = kIsE4m3<T>;              // f16 MMAs over widened E4M3 codes
+        const uint32_t ks_u = smem_u32(ks), vs_u = smem_u32(vs);
+        const int r8 = lane & 7, mi = lane >> 3;      // ldmatrix: row r8 of matrix mi
+        // ---- S^T = K.Q^T: rows of the accumulator are the block's keys (g8,
+        //      g8 + 8), columns the tile's rows; even and odd k-steps
+        //      accumulate separately (independent MMA chains), then add ----
+        float sc[2][kHR][4];                           // [k-step parity][n-tile][c]
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[u][hr][c] = 0.f;
+        auto mma_s = [&](int t, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+#pragma unroll
+          for (int hr = 0; hr < kHR; ++hr)
+            mma16816<kF16>(sc[t & 1][hr][0], sc[t & 1][hr][1], sc[t & 1][hr][2], sc[t & 1][hr][3],
+                           a0, a1, a2, a3, qa[t][2 * hr], qa[t][2 * hr + 1]);
+        };
+        if constexpr (kIsE4m3<T>) {
+          // lane's codes: key rows g8 and g8 + 8, bytes 32kq .. 32kq + 31
+          // (16-byte chunks 2kq, 2kq + 1, placed at chunk ^ (row % 8))
+          uint4 kc[2][2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              kc[j][h] = lds128(ks_u + (g8 + 8 * j) * 128 + (((2 * kq + h) ^ g8) << 4));
+#pragma unroll
+          for (int t = 0; t < kMT; ++t) {
+            auto word = [&](const uint4& c4) {
+              return (t & 3) == 0 ? c4.x : (t & 3) == 1 ? c4.y : (t & 3) == 2 ? c4.z : c4.w;
+            };
+            const uint32_t w0 = word(kc[0][t >> 2]), w1 = word(kc[1][t >> 2]);
+            mma_s(t, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
+                  e4m3x2_to_f16x2(w1 >> 16));
+          }
+        } else {
+          // matrix mi: keys 8 (mi & 1) .. +7, 16-byte chunk 2 (t % 4) + (mi >> 1)
+          // of 128-byte slice t / 4
+          const uint32_t krow = ks_u + (8 * (mi & 1) + r8) * 128;
+#pragma unroll
+          for (int t = 0; t < kMT; ++t) {
+            uint32_t ka[4];
+            ldsm_x4(ka, krow + (t >> 2) * C::kBoxBytes + (((2 * (t & 3) + (mi >> 1)) ^ r8) << 4));
+            mma_s(t, ka[0], ka[1], ka[2], ka[3]);
+          }
+        }
+        // ---- scores in the log2 domain, masked (keys past the split range,
+        //      the causal limit, the window start); lane holds keys g8 (c0,
+        //      c1) and g8 + 8 (c2, c3) of rows 8h + 2kq + e ----
+        const int kA = key0 + g8, kB = key0 + g8 + 8;
+        bool all_in = nvalid == kBlock;
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            all_in = all_in && key0 >= mlo[hr][e] && key0 + kBlock <= mlim[hr][e];
+        all_in = __all_sync(0xffffffffu, all_in);
+        float x[kHR][4];
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int e = c & 1, key = c < 2 ? kA : kB;
+            const float v = (sc[0][hr][c] + sc[1][hr][c]) * score_scale;
+            x[hr][c] = all_in || (key < mlim[hr][e] && key >= mlo[hr][e]) ? v : -INFINITY;
+          }
+        // ---- online softmax with a lagged reference max per row: a row's 16
+        //      keys sit on the 8 lanes of its kq ----
+        float bm[kHR][2];
+        bool need = false;
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float v = fmaxf(x[hr][e], x[hr][2 + e]);
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+            bm[hr][e] = v;
+            need = need || v > mm[hr][e] + kLag;
+          }
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const bool nd = bm[hr][e] > mm[hr][e] + kLag;
+              const float al = nd ? ex2(mm[hr][e] - bm[hr][e]) : 1.f;   // 0 when mm was -inf
+              mm[hr][e] = nd ? bm[hr][e] : mm[hr][e];
+              ll[hr][e] *= al;
+              lr[hr][e] *= al;
+#pragma unroll
+              for (int mt = 0; mt < kMD; ++mt) {
+                oacc[mt][hr][e] *= al;
+                oacc[mt][hr][2 + e] *= al;
+              }
+            }
+        }
+        // P^T (B operand of O^T += V^T.P^T) per n-tile: p of keys g8 | g8 + 8
+        // for rows 2kq, 2kq + 1 packed into 16-bit pairs, then transposed so
+        // each lane holds row g8's keys 2kq, 2kq+1 | 8+2kq, 9+2kq
+        uint32_t pb[kHR][2];
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr) {
+          float p[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float m = mm[hr][c & 1];
+            p[c] = ex2(x[hr][c] - (m == -INFINITY ? 0.f : m));
+          }
+          uint32_t pk[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            if constexpr (kF16) {
+              pk[j] = pack_f16x2(p[2 * j], p[2 * j + 1]);
+              lr[hr][0] += f16_lo(pk[j]);
+              lr[hr][1] += f16_hi(pk[j]);
+            } else {
+              pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+              lr[hr][0] += bf16_lo(pk[j]);
+              lr[hr][1] += bf16_hi(pk[j]);
+            }
+            ll[hr][0] += p[2 * j];
+            ll[hr][1] += p[2 * j + 1];
+            pb[hr][j] = movmatrix_t(pk[j]);
+          }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&vfull[st], ph))) {
+          if (lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+          break;
+        }
+        // ---- O^T += V^T.P^T over 16-dim m-tiles ----
+        auto mma_o = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+#pragma unroll
+          for (int hr = 0; hr < kHR; ++hr)
+            mma16816<kF16>(oacc[mt][hr][0], oacc[mt][hr][1], oacc[mt][hr][2], oacc[mt][hr][3], a0,
+                           a1, a2, a3, pb[hr][0], pb[hr][1]);
+        };
+        if constexpr (kIsE4m3<T>) {
+          // lane's codes: keys 2kq, 2kq+1, 2kq+8, 2kq+9, dims 16 g8 .. +15 (one
+          // 16-byte chunk each); m-tile mt takes its rows g8 and g8 + 8 as
+          // dims 16 g8 + 2 mt and 16 g8 + 2 mt + 1, so a byte shuffle pairs
+          // the two keys of each dim
+          uint4 vc[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kv = 2 * kq + (i & 1) + 8 * (i >> 1);
+            vc[i] = lds128(vs_u + kv * 128 + ((g8 ^ (kv & 7)) << 4));
+            // keys past the split range may hold anything (even NaN codes)
+            if (nvalid < kBlock && kv >= nvalid) vc[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            auto word = [&](const uint4& c4) {
+              return w == 0 ? c4.x : w == 1 ? c4.y : w == 2 ? c4.z : c4.w;
+            };
+            const uint32_t a0 = word(vc[0]), a1 = word(vc[1]), b0 = word(vc[2]), b1 = word(vc[3]);
+            const uint32_t alo = prmt(a0, a1, 0x5140), ahi = prmt(a0, a1, 0x7362);
+            const uint32_t blo = prmt(b0, b1, 0x5140), bhi = prmt(b0, b1, 0x7362);
+            mma_o(2 * w, e4m3x2_to_f16x2(alo), e4m3x2_to_f16x2(alo >> 16), e4m3x2_to_f16x2(blo),
+                  e4m3x2_to_f16x2(blo >> 16));
+            mma_o(2 * w + 1, e4m3x2_to_f16x2(ahi), e4m3x2_to_f16x2(ahi >> 16),
+                  e4m3x2_to_f16x2(bhi), e4m3x2_to_f16x2(bhi >> 16));
+          }
+        } else {
+          // matrix mi (.trans): keys 8 (mi >> 1) .. +7, chunk 2 (mt % 4) + (mi & 1)
+          // of 128-byte slice mt / 4
+          const uint32_t vrow = vs_u + (8 * (mi >> 1) + r8) * 128;
+          // keys past the split range may hold anything: zero their V
+          uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+          if (nvalid < kBlock) {
+            mk0 = (2 * kq < nvalid ? 0x0000ffffu : 0u) | (2 * kq + 1 < nvalid ? 0xffff0000u : 0u);
+            mk1 = (2 * kq + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * kq + 9 < nvalid ? 0xffff0000u : 0u);
+          }
+#pragma unroll
+          for (int mt = 0; mt < kMD; ++mt) {
+            uint32_t va[4];
+            ldsm_x4_t(va, vrow + (mt >> 2) * C::kBoxBytes +
+                              (((2 * (mt & 3) + (mi & 1)) ^ r8) << 4));
+            mma_o(mt, va[0] & mk0, va[1] & mk0, va[2] & mk1, va[3] & mk1);
+          }
+        }
+      } else if constexpr (kFast) {
         // ---- scores: partial dots of 4 keys x 4 rows over this lane's slice ----
         f32x2 part[4][4];
 #pragma unroll
@@ -1005,8 +1406,40 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   // ---- merge the warps' states (shared memory reused) ----
   __syncthreads();
   float* mw = reinterpret_cast<float*>(smem);
-  float* lw = mw + C::kWarps * R;
-  float* aw = lw + C::kWarps * R;
+  float* lw = mw + C::kWarps * R;                      // row mass (fp32 sum of p)
+  float* lrw = lw + C::kWarps * R;                     // the accumulator's normaliser
+  float* aw = lrw + C::kWarps * R;
+  if (kMma && !producer) {
+    // rows 8h + 2kq + e of this warp: l summed over the row's eight lanes;
+    // accumulator slot c of m-tile mt is dim 16 mt + g8 (+ 8 for c >= 2) for
+    // a bf16 cache, 16 g8 + 2 mt (+ 1 for c >= 2) for an E4M3 cache
+#pragma unroll
+    for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float lt = ll[hr][e], lrt = lr[hr][e];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          lt += __shfl_xor_sync(0xffffffffu, lt, o);
+          lrt += __shfl_xor_sync(0xffffffffu, lrt, o);
+        }
+        const int rho = 8 * hr + 2 * kq + e;
+        if (rho < R) {
+          if (g8 == 0) {
+            mw[warp * R + rho] = mm[hr][e];
+            lw[warp * R + rho] = lt;
+            lrw[warp * R + rho] = lrt;
+          }
+#pragma unroll
+          for (int mt = 0; mt < kMD; ++mt)
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi) {
+              const int dim = kIsE4m3<T> ? 16 * g8 + 2 * mt + hi : 16 * mt + g8 + 8 * hi;
+              aw[(warp * R + rho) * D + dim] = oacc[mt][hr][2 * hi + e];
+            }
+        }
+      }
+  }
   if (kFast && !producer) {
     float lt = l_mine + __shfl_xor_sync(0xffffffffu, l_mine, 1);
     lt += __shfl_xor_sync(0xffffffffu, lt, 8);
@@ -1026,7 +1459,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
   }
 #pragma unroll
   for (int rho = 0; rho < R; ++rho) {
-    if (!kFast && !producer && rho < nrows) {
+    if (!kFast && !kMma && !producer && rho < nrows) {
       const float lt = warp_sum(l[rho]);
       if (lane == 0) {
         mw[warp * R + rho] = m[rho];
@@ -1039,25 +1472,27 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, 1)
     }
   }
   __syncthreads();
-  for (int rho = warp; rho < nrows && !producer; rho += C::kWarps) {
+  for (int rho = warp; rho < nrows && !producer; rho += W) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kWarps; ++w) M = fmaxf(M, mw[w * R + rho]);
     float o[C::kDPL];
 #pragma unroll
     for (int e = 0; e < C::kDPL; ++e) o[e] = 0.f;
-    float lsum = 0.f;
+    float lsum = 0.f, lnorm = 0.f;   // row mass; the accumulator's normaliser
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < C::kWarps; ++w) {
         const float f = ex2(mw[w * R + rho] - M);
         lsum = fmaf(f, lw[w * R + rho], lsum);
+        if constexpr (kMma) lnorm = fmaf(f, lrw[w * R + rho], lnorm);
 #pragma unroll
         for (int e = 0; e < C::kDPL; ++e)
           o[e] = fmaf(f, aw[(w * R + rho) * D + lane * C::kDPL + e], o[e]);
       }
     }
-    const float inv = lsum > 0.f ? a.v_scale / lsum : 0.f;   // v_scale: E4M3 caches
+    if constexpr (!kMma) lnorm = lsum;
+    const float inv = lnorm > 0.f ? a.v_scale / lnorm : 0.f;   // v_scale: E4M3 caches
     const float lse2 = lsum > 0.f ? M + lg2(lsum) : -INFINITY;
     const int rr = rho0 + rho;
     const int i = rr / group;
@@ -1183,6 +1618,11 @@ static cudaError_t ensure_smem_attr() {
   if (dev < 32 && ((done >> dev) & 1u)) return cudaSuccess;
   e = cudaFuncSetAttribute(decode_kernel<T, D, R, SPEC>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::kAlloc);
+  // the tensor-core build runs two CTAs per SM: ask for the largest
+  // shared-memory carveout
+  if (e == cudaSuccess && DecodeCfg<T, D, R>::kMma)
+    e = cudaFuncSetAttribute(decode_kernel<T, D, R, SPEC>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e == cudaSuccess && dev < 32) done |= 1u << dev;
   return e;
 }
@@ -1225,34 +1665,13 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
   }
 }
 
-// Resident decode CTAs per SM for the bf16 single-token configuration (the
-// one the split heuristic sizes), from the occupancy calculator.
-int decode_ctas_per_sm(int head_dim) {
-  static int cache[2] = {0, 0};
-  const int k = head_dim == 128 ? 1 : 0;
-  if (cache[k] == 0) {
-    int n = 0;
-    cudaError_t e;
-    if (k) {
-      e = ensure_smem_attr<__nv_bfloat16, 128, 4>();
-      if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, decode_kernel<__nv_bfloat16, 128, 4, false>, DecodeCfg<__nv_bfloat16, 128>::kThreads,
-            DecodeSmem<__nv_bfloat16, 128, 4>::kAlloc);
-    } else {
-      e = ensure_smem_attr<__nv_bfloat16, 64, 4>();
-      if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, decode_kernel<__nv_bfloat16, 64, 4, false>, DecodeCfg<__nv_bfloat16, 64>::kThreads,
-            DecodeSmem<__nv_bfloat16, 64, 4>::kAlloc);
-    }
-    if (e != cudaSuccess || n < 1) {
-      cudaGetLastError();
-      return 1;
-    }
-    cache[k] = n;
-  }
-  return cache[k];
+// Whether the decode kernel for this cache type and head_dim takes its K/V
+// boxes in the 128B-swizzled layout (the tensor-core build) rather than as
+// whole unswizzled rows.
+bool decode_swizzled(ElemType et, int head_dim) {
+  if (et == ElemType::kBf16) return head_dim == 64 || head_dim == 128;
+  if (et == ElemType::kE4m3) return head_dim == 128;
+  return false;
 }
 
 // Rows per CTA tile: one token's GQA group rounded up to 4/8/16 rows, so a

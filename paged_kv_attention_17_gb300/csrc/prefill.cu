@@ -189,6 +189,35 @@ __device__ __forceinline__ float lg2f_(float x) {
   return y;
 }
 
+// Packed fp32 pairs (sm_100+: one instruction for two lanes of fp32 math) and
+// a three-input max, to thin out the softmax's instruction stream.
+__device__ __forceinline__ unsigned long long pair(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpair(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ unsigned long long fma_pair(unsigned long long a, unsigned long long b,
+                                                       unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add_pair(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -218,8 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool packed = a.cascade == 1;                    // shared-prefix mode
-  const int h0 = packed ? 0 : 2 * blockIdx.y;            // query heads h0, h0 + 1 (same KV head)
-  const int tglob = blockIdx.x;
+  // The grid is one-dimensional with the head pair (shared-prefix mode: the
+  // kv head and prefix split) varying fastest, so every head pair's heaviest
+  // query tiles are dispatched in the first waves (longest work first) and
+  // the CTAs reading the same K/V tiles run side by side.
+  const int ys = packed ? a.hkv * a.num_splits : a.hq / 2;
+  const int yidx = static_cast<int>(blockIdx.x % static_cast<unsigned>(ys));
+  const int h0 = packed ? 0 : 2 * yidx;                  // query heads h0, h0 + 1 (same KV head)
+  const int tglob = static_cast<int>(blockIdx.x / static_cast<unsigned>(ys));
 
   pdl_wait_primary();
   pdl_launch_dependents();
@@ -274,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && h0 == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
     return;
   }
-  const int g = packed ? static_cast<int>(blockIdx.y) % a.hkv : h0 / a.group;
-  const int split = packed ? static_cast<int>(blockIdx.y) / a.hkv : 0;
+  const int g = packed ? yidx % a.hkv : h0 / a.group;
+  const int split = packed ? yidx / a.hkv : 0;
   const int tok_per_tile = kQRows / a.group;             // packed: tokens per 128-row tile
   const int i0 = tile * kQRows;
   const int i_hi = min(i0 + kQRows, n) - 1;              // last real row of the tile
@@ -527,11 +562,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mx8[8];                                      // 8 independent max chains
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mx8[j] = s[j];
+      for (int j = 0; j < 8; ++j) mx8[j] = fmaxf(s[j], s[j + 8]);
 #pragma unroll
-      for (int i = 8; i < kKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], s[i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int i = 16; i < kKeys; i += 16)               // two new scores per max
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx8[j] = max3(mx8[j], s[i + j], s[i + 8 + j]);
+      const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]),
+                            fmaxf(mx8[6], mx8[7]));
       // Scores are unscaled here; m (scaled log2 domain) is the reference max
       // the accumulator and l are kept relative to.  It moves only when the
       // row max exceeds it by more than kRescaleSlack, so p <= 2^kRescaleSlack
@@ -540,14 +577,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float mnew = (mcand > m + kRescaleSlack) ? mcand : m;
       const float msafe = mnew == -INFINITY ? 0.f : mnew;
       const float alpha = ex2f_(m - msafe);
-      float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // 8 independent sums
+      // p = 2^(s sc - m): the scaling in packed pairs, 4 independent pair sums
+      const unsigned long long scp = pair(sc, sc), nmp = pair(-msafe, -msafe);
+      unsigned long long ps4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int i = 0; i < kKeys; ++i) {
-        s[i] = ex2f_(fmaf(s[i], sc, -msafe));
-        ps8[i & 7] += s[i];
+      for (int j = 0; j < kKeys / 2; ++j) {
+        const float2 x = unpair(fma_pair(pair(s[2 * j], s[2 * j + 1]), scp, nmp));
+        s[2 * j] = ex2f_(x.x);
+        s[2 * j + 1] = ex2f_(x.y);
+        ps4[j & 3] = add_pair(ps4[j & 3], pair(s[2 * j], s[2 * j + 1]));
       }
-      const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
-                         ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+      const float2 sa = unpair(add_pair(add_pair(ps4[0], ps4[1]), add_pair(ps4[2], ps4[3])));
+      const float psum = sa.x + sa.y;
       l = l * alpha + psum;
       m = mnew;
       // P row as bf16 pairs into the first 64 columns of this row's S (the
@@ -696,9 +737,9 @@ cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUt
                             : (a.num_tokens + kQRows - 1) / kQRows + long_reqs;
   const int64_t ys = a.cascade == 1 ? static_cast<int64_t>(a.hkv) * a.num_splits : a.hq / 2;
   if (tiles <= 0) return cudaSuccess;
-  if (tiles > 0x7FFFFFFF || ys > 65535) return cudaErrorInvalidConfiguration;
+  if (ys < 1 || tiles * ys > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(ys));
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles * ys));      // (tile, head pair), pair fastest
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;
