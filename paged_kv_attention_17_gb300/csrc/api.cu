@@ -22,6 +22,7 @@ cudaError_t launch_decode(const AttnArgs& a, const CUtensorMap& kmap, const CUte
 cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStream_t stream);
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
 bool decode_swizzled(ElemType et, int head_dim);
+int decode_ctas_per_sm(ElemType et, int head_dim);
 bool prefill_supported(int head_dim, bool bf16, int group);
 bool prefill_packed_supported(int head_dim, bool bf16, int group);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
@@ -126,6 +127,36 @@ bool valid_dtype(pkv_dtype dt) { return dt == PKV_F32 || dt == PKV_BF16; }
 
 bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
+// The split rule for a cache type: as many splits as fit in 7/8 of the
+// device's decode CTA slots in one wave (none when the grid is already nearly
+// full), every split keeping at least kMinBlocksPerSplit blocks.
+int split_rule(int num_seqs, int max_query_len, int max_seq_len, int num_q_heads,
+               int num_kv_heads, int head_dim, int device, ElemType et) {
+  if (num_seqs < 1 || max_seq_len < 0 || max_query_len < 0 || num_q_heads < 1 ||
+      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return 0;
+  const int sms = device_sms(device);
+  if (sms <= 0) return 0;
+  const int group = num_q_heads / num_kv_heads;
+  const int qd = max_query_len < kDecodeMaxQ ? (max_query_len < 1 ? 1 : max_query_len) : kDecodeMaxQ;
+  const int R = decode_rows_per_tile(group, qd, false);
+  const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((group * qd + R - 1) / R);
+  // decode CTA slots of the device (two per SM for the tensor-core build);
+  // 7/8 of them leave room for the combine and the next launch's prologue
+  // (decode at context 8192, 8 KV heads, bf16, 152 SMs: 16 splits take
+  // 14 us a call, 32 splits 10.8 us; a second wave at 40 splits 18 us)
+  const int64_t capacity = static_cast<int64_t>(sms) * decode_ctas_per_sm(et, head_dim);
+  const int64_t target = capacity * 7 / 8;
+  int64_t s = target / units;
+  if (s <= 1) return 1;
+  const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kBlock - 1) / kBlock;
+  int64_t by_len = nblk / kMinBlocksPerSplit;
+  if (by_len < 1) by_len = 1;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
 static pkv_status attention(const void* q, const void* k_cache, const void* v_cache, void* out,
                             float* lse_out, const int32_t* query_start_loc,
                             const int32_t* seq_lens, const int32_t* block_table,
@@ -172,8 +203,8 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     // a window bounds the keys a decode row reads: size the split by that span
     const int span = window > 0 && window < max_seq_len - kDecodeMaxQ
                          ? window + kDecodeMaxQ : max_seq_len;
-    splits = pkv_num_splits(num_seqs, max_query_len, span, num_q_heads, num_kv_heads, head_dim,
-                            dev);
+    splits = split_rule(num_seqs, max_query_len, span, num_q_heads, num_kv_heads, head_dim, dev,
+                        et);
   }
   if (splits < 1) return PKV_ERR_CUDA;
   const size_t need = pkv_workspace_bytes(num_seqs, num_q_heads, head_dim, splits);
@@ -323,34 +354,10 @@ pkv_status pkv_write_e4m3(const void* k_new, const void* v_new, const int64_t* s
 
 int pkv_num_splits(int num_seqs, int max_query_len, int max_seq_len, int num_q_heads,
                    int num_kv_heads, int head_dim, int device) {
-  if (num_seqs < 1 || max_seq_len < 0 || max_query_len < 0 || num_q_heads < 1 ||
-      num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
-    return 0;
-  const int sms = device_sms(device);
-  if (sms <= 0) return 0;
-  const int group = num_q_heads / num_kv_heads;
-  const int qd = max_query_len < kDecodeMaxQ ? (max_query_len < 1 ? 1 : max_query_len) : kDecodeMaxQ;
-  const int R = decode_rows_per_tile(group, qd, false);
-  const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads * ((group * qd + R - 1) / R);
-  // one decode CTA per SM: the tensor-core build fits two, and the second
-  // slot is left to the next launch, whose CTAs warm L2 there before their
-  // dependency wait
-  (void)head_dim;
-  const int64_t capacity = sms;
-  // As many splits as fit in 7/8 of the device in one wave (none when the
-  // grid is already nearly full): every CTA's blocks in flight together, and the SMs
-  // left over let the combine and the next launch's prologue become resident
-  // early under programmatic dependent launch (decode at context 8192, 8 KV
-  // heads, 152 SMs: 16 splits take 11.2 us a call, 19 splits 12.5 us).
-  const int64_t target = capacity * 7 / 8;
-  int64_t s = target / units;
-  if (s <= 1) return 1;
-  const int64_t nblk = (static_cast<int64_t>(max_seq_len) + kBlock - 1) / kBlock;
-  int64_t by_len = nblk / kMinBlocksPerSplit;
-  if (by_len < 1) by_len = 1;
-  if (s > by_len) s = by_len;
-  if (s > kMaxSplits) s = kMaxSplits;
-  return static_cast<int>(s < 1 ? 1 : s);
+  // the rule for bf16 and E4M3 caches (an fp32 cache's automatic count may be
+  // lower, so a workspace sized from this count always suffices)
+  return split_rule(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                    device, ElemType::kBf16);
 }
 
 size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_splits) {

@@ -229,10 +229,11 @@ struct DecodeCfg {
   // Consumer (compute) warps per CTA, plus one TMA producer warp.  CUDA-core
   // build: 11 + 1 warps (three per SM sub-partition, 168 registers each) for
   // 4-row tiles, whose register-q path fits that budget; wider tiles keep
-  // 255 registers with 7 + 1 warps; one CTA per SM.  Tensor-core build: 4 + 1
-  // warps and a 96 KB ring, so two CTAs fit on an SM and the next launch's
-  // CTAs become resident (and warm L2) while this one streams.
-  static constexpr int kWarps = kMma ? 4 : (R == 4 ? 11 : 7);
+  // 255 registers with 7 + 1 warps; one CTA per SM.  Tensor-core build: 6 + 1
+  // warps and a 96 KB ring (two or four stages per warp), so two CTAs fit on
+  // an SM and the next launch's CTAs become resident (and warm L2) while this
+  // one streams.
+  static constexpr int kWarps = kMma ? 6 : (R == 4 ? 11 : 7);
   static constexpr int kRingBudget = kMma ? 98304 : 196608;
   static constexpr int kStagesRaw = kRingBudget / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 6 ? 6 : kStagesRaw);
@@ -262,9 +263,12 @@ struct DecodeSmem {
   static constexpr int kStageArea = C::kStages * C::kStageBytes;
   static constexpr int kMergeBytes = C::kWarps * R * (D + 3) * 4;   // m, l, l~, acc per row
   static constexpr int kRingBytes = kStageArea > kMergeBytes ? kStageArea : kMergeBytes;
-  // q rows and the P tile live in registers in the tensor-core build
+  // CUDA-core build: q rows as fp32; tensor-core build: the tile's q rows as
+  // loaded (bf16), rows padded by 16 bytes so the fragment reads of 8 rows
+  // hit distinct banks
+  static constexpr int kQRowBytes = D * 2 + 16;
   static constexpr int kQOff = kRingBytes;
-  static constexpr int kPOff = kQOff + (C::kMma ? 0 : R * D * 4);
+  static constexpr int kPOff = kQOff + (C::kMma ? R * kQRowBytes : R * D * 4);
   static constexpr int kBarOff = kPOff + (C::kMma ? 0 : C::kWarps * kBlock * R * 8);
   // kfull[], vfull[], empty[], then per consumer warp the barrier and the
   // verdict of its speculative first block
@@ -479,36 +483,44 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   // ---- inputs only after the wait ----
   pdl_wait_primary();
   pdl_launch_dependents();
+  // The request's metadata and the table entries of the hinted split range
+  // are the first loads after the wait (everything after depends on them);
+  // the speculative q rows and K/V boxes go out behind them.
+  // cascade prefix pass: one request holding every row of the batch, over the
+  // prefix_len shared keys
+  const bool prefix_pass = a.cascade == 1;
+  const int md_q0 = prefix_pass ? 0 : ld_early(a.qsl + r);
+  const int md_q1 = prefix_pass ? static_cast<int>(a.num_tokens) : ld_early(a.qsl + r + 1);
+  const int md_L = prefix_pass ? a.prefix_len : ld_early(a.seq_lens + r);
+  // the table entries of warp pw's first two blocks of the hinted split range:
+  // the verdict on the speculative block and the first loads need no second
+  // round trip when the real range starts at the hinted block
+  const bool spec_v0 = p_act && spec_b0 + pw < nb_spec;
+  const bool spec_v1 = p_act && spec_b0 + pw + W < nb_spec;
+  const int32_t spec_e0 = spec_v0 ? ld_early(table + spec_b0 + pw) : 0;
+  const int32_t spec_e1 = spec_v1 ? ld_early(table + spec_b0 + pw + W) : 0;
   // Tensor-core build: the q rows of this tile are loaded at once from the
-  // hinted start (token index kept inside q, so every load is in bounds),
-  // in flight together with the metadata; reloaded below if the metadata
-  // puts the rows elsewhere.  bf16 cache: k-step t covers dims 16t..16t+15 in
-  // order.  E4M3 cache (f16 MMAs): k-step t of lane kq covers dims
-  // 32kq + 4t .. +3, so that a lane's K codes for all k-steps are 32
-  // consecutive bytes of a key row (the dot product is indifferent to the
-  // order of its terms).
+  // hinted start (token index kept inside q, so every load is in bounds) in
+  // 16-byte pieces by all consumer threads, in flight together with the
+  // metadata; reloaded below if the metadata puts the rows elsewhere, then
+  // staged in shared memory, where each lane picks its fragment words.
   constexpr int kMT = kMma ? D / 16 : 1;               // k-steps of Q.K^T
   constexpr bool kHi = R == 16;                        // M-rows 8..15 are tile rows
   constexpr int kHR = kHi ? 2 : 1;                     // M-row halves this lane holds
+  constexpr int kQChunks = R * D / 8;                  // 16-byte pieces of the tile's q rows
+  constexpr int kQLd = kMma ? (kQChunks + C::kConsumerThreads - 1) / C::kConsumerThreads : 1;
   const int g8 = lane >> 2, kq = lane & 3;
-  uint32_t qw[kHR][kMT][2];
+  uint4 qld[kQLd];
   auto load_q = [&](int q0v) {
 #pragma unroll
-    for (int hr = 0; hr < kHR; ++hr) {
-      const int rr = blockIdx.y * R + g8 + 8 * hr;
-      const int64_t tok = min(max(static_cast<int64_t>(q0v) + rr / a.group, int64_t{0}),
-                              a.num_tokens - 1);
-      const QT* qp = static_cast<const QT*>(a.q) + (tok * a.hq + g * a.group + rr % a.group) * D;
-#pragma unroll
-      for (int t = 0; t < kMT; ++t) {
-        if constexpr (kIsE4m3<T>) {
-          const uint2 v = ld_early_v2(qp + 32 * kq + 4 * t);
-          qw[hr][t][0] = v.x;
-          qw[hr][t][1] = v.y;
-        } else {
-          qw[hr][t][0] = ld_early_u32(qp + 16 * t + 2 * kq);
-          qw[hr][t][1] = ld_early_u32(qp + 16 * t + 8 + 2 * kq);
-        }
+    for (int u = 0; u < kQLd; ++u) {
+      const int idx = threadIdx.x + u * C::kConsumerThreads;
+      if (idx < kQChunks) {
+        const int rr = blockIdx.y * R + idx / (D / 8);
+        const int64_t tok = min(max(static_cast<int64_t>(q0v) + rr / a.group, int64_t{0}),
+                                a.num_tokens - 1);
+        qld[u] = ld_early_v4(static_cast<const QT*>(a.q) +
+                             (tok * a.hq + g * a.group + rr % a.group) * D + (idx % (D / 8)) * 8);
       }
     }
   };
@@ -542,21 +554,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   auto drain_spec = [&]() {
     if (spec_issued) mbar_wait(pp >= C::kBoxes ? &vfull[pw * P] : &kfull[pw * P], 0);
   };
-  // The table entries of warp pw's first two blocks of the hinted split range,
-  // read now (after the wait), together with the metadata: the verdict on the
-  // speculative block and the first loads need no second round trip when the
-  // real range starts at the hinted block.
-  const bool spec_v0 = p_act && spec_b0 + pw < nb_spec;
-  const bool spec_v1 = p_act && spec_b0 + pw + W < nb_spec;
-  const int32_t spec_e0 = spec_v0 ? ld_early(table + spec_b0 + pw) : 0;
-  const int32_t spec_e1 = spec_v1 ? ld_early(table + spec_b0 + pw + W) : 0;
-  // cascade prefix pass: one request holding every row of the batch, over the
-  // prefix_len shared keys
-  const bool prefix_pass = a.cascade == 1;
-  const int q0 = prefix_pass ? 0 : __ldg(a.qsl + r);
-  const int q1 = prefix_pass ? static_cast<int>(a.num_tokens) : __ldg(a.qsl + r + 1);
+  const int q0 = md_q0, q1 = md_q1;
   const int n = q1 - q0;
-  const int L = prefix_pass ? a.prefix_len : __ldg(a.seq_lens + r);
+  const int L = md_L;
   if (n == 0) {
     drain_spec();
     return;
@@ -807,17 +807,43 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
     __syncwarp();
   } else {
     if constexpr (kMma) {
-      // ---- q as the A operand (loaded right after the wait): reloaded if
-      //      the metadata puts the rows elsewhere; rows past the tile's are
-      //      zero.  E4M3 cache: q is scaled by a power of two bringing max|q|
-      //      into [2^14, 2^15), where f16 holds every bf16 value exactly, and
-      //      the score scale takes the inverse. ----
+      // ---- q (loaded right after the wait): reloaded if the metadata puts
+      //      the rows elsewhere, staged in shared memory, and each lane's B
+      //      operand words picked for rows 8h + g8 (zero past the tile's
+      //      rows).  E4M3 cache: q is scaled by a power of two bringing
+      //      max|q| into [2^14, 2^15), where f16 holds every bf16 value
+      //      exactly, and the score scale takes the inverse. ----
       if (q0 != (prefix_pass ? 0 : q0_hint)) load_q(q0);
+      uint8_t* qst = smem + Sm::kQOff;
 #pragma unroll
-      for (int hr = 0; hr < kHR; ++hr)
+      for (int u = 0; u < kQLd; ++u) {
+        const int idx = threadIdx.x + u * C::kConsumerThreads;
+        if (idx < kQChunks)
+          *reinterpret_cast<uint4*>(qst + (idx / (D / 8)) * Sm::kQRowBytes + (idx % (D / 8)) * 16) =
+              qld[u];
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(C::kConsumerThreads) : "memory");
+      uint32_t qw[kHR][kMT][2];
 #pragma unroll
-        for (int t = 0; t < kMT; ++t)
-          if (g8 + 8 * hr >= nrows) qw[hr][t][0] = qw[hr][t][1] = 0u;
+      for (int hr = 0; hr < kHR; ++hr) {
+        const int rho = g8 + 8 * hr;
+        const uint8_t* qrow = qst + rho * Sm::kQRowBytes;
+#pragma unroll
+        for (int t = 0; t < kMT; ++t) {
+          if (rho >= nrows) {
+            qw[hr][t][0] = qw[hr][t][1] = 0u;
+          } else if constexpr (kIsE4m3<T>) {
+            // dims 32kq + 4t .. +3
+            const uint2 v = *reinterpret_cast<const uint2*>(qrow + (32 * kq + 4 * t) * 2);
+            qw[hr][t][0] = v.x;
+            qw[hr][t][1] = v.y;
+          } else {
+            // dims 16t + 2kq, +1 and 16t + 8 + 2kq, +1
+            qw[hr][t][0] = *reinterpret_cast<const uint32_t*>(qrow + (16 * t + 2 * kq) * 2);
+            qw[hr][t][1] = *reinterpret_cast<const uint32_t*>(qrow + (16 * t + 8 + 2 * kq) * 2);
+          }
+        }
+      }
       if constexpr (kIsE4m3<T>) {
         float mx = 0.f;
 #pragma unroll
@@ -1663,6 +1689,14 @@ static cudaError_t launch_decode_d(const AttnArgs& a, const CUtensorMap& kmap,
     case 8: return launch_decode_t<T, D, 8, false>(a, kmap, vmap, row_tiles, pdl, stream);
     default: return launch_decode_t<T, D, 16, false>(a, kmap, vmap, row_tiles, pdl, stream);
   }
+}
+
+// Resident decode CTAs per SM the split rule plans for: two for the
+// tensor-core build, one for the CUDA-core build.
+int decode_ctas_per_sm(ElemType et, int head_dim) {
+  const bool mma = (et == ElemType::kBf16 && (head_dim == 64 || head_dim == 128)) ||
+                   (et == ElemType::kE4m3 && head_dim == 128);
+  return mma ? 2 : 1;
 }
 
 // Whether the decode kernel for this cache type and head_dim takes its K/V

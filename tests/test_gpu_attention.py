@@ -166,10 +166,11 @@ def test_split_count_changes_nothing_f32():
 
 
 def test_split_heuristic_rule():
-    # one wave of split CTAs over 7/8 of the SMs (one decode CTA per SM), at
-    # least 8 blocks per split, split off once the grid is nearly full
+    # one wave of split CTAs over 7/8 of the decode CTA slots (two per SM for
+    # the bf16 tensor-core build), at least 8 blocks per split, split off once
+    # the grid is nearly full
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    target = sms * 7 // 8
+    target = 2 * sms * 7 // 8
     # batch 1, 8 KV heads, GQA group 4 (one 4-row tile): U = 8
     assert pkv.pkv_num_splits(1, 1, 8192, 32, 8, 128) == min(64, max(1, target // 8))
     # a short context caps the split at 8 blocks (128 keys) per split
