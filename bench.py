@@ -681,8 +681,8 @@ def run_gpu(args, rank, world, local_rank):
 def run_e2e_graphs(args, w, reps, common, bytes_step):
     """Decode steps through the package's CUDA-graph runner: per step the
     packed inputs (Q, new K/V, metadata) are staged in pinned host memory and
-    one graph replay writes and attends, its kernels reading those inputs and
-    writing the output rows in pinned host memory over the host-device link."""
+    one graph replay copies them to the device (pkv_stage_inputs), writes and
+    attends, the output rows written into pinned host memory."""
     import torch
 
     from paged_kv_attention_17_gb300.graphs import DecodeGraphRunner
@@ -726,8 +726,9 @@ def run_e2e_graphs(args, w, reps, common, bytes_step):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
             "ms_per_step": round(ms, 6),
             "mode": "CUDA-graph runner: per step the packed inputs are staged in pinned host "
-                    "memory and one replay writes and attends, reading them and writing the "
-                    "output rows in pinned host memory over NVLink-C2C"}
+                    "memory; one replay copies them to the device with a library kernel over "
+                    "NVLink-C2C, then writes and attends, writing the output rows into pinned "
+                    "host memory"}
 
 
 def run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, flops_step,

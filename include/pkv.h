@@ -37,7 +37,8 @@
  *     _e4m3 entry points.  Arithmetic is fp32 with fp32 accumulation (the
  *     tensor-core prefill rounds P to bf16 for its P.V product).
  *
- * Entry points: pkv_write / pkv_write_e4m3 (slot-mapped write), pkv_num_splits
+ * Entry points: pkv_write / pkv_write_e4m3 (slot-mapped write), pkv_stage_inputs
+ * (a step's packed inputs copied to the device), pkv_num_splits
  * and pkv_workspace_bytes (split-KV sizing), pkv_attention_varlen and its
  * variants _window (sliding window), _e4m3 (8-bit cache) and _noalloc (no
  * caller workspace), pkv_write_attention_varlen / _e4m3 (write and attend in
@@ -129,6 +130,30 @@ pkv_status pkv_write_e4m3(const void* k_new, const void* v_new, const int64_t* s
                           int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_blocks,
                           int block_size, int num_kv_heads, int head_dim, pkv_dtype src_dtype,
                           float k_scale, float v_scale, int32_t* error_flag, void* stream);
+
+/*
+ * pkv_stage_inputs - copy a step's packed inputs into device memory.
+ *
+ * "Inside the engine: kernels, CUDA graphs and the life of a request",
+ * section on CUDA graphs (a captured step runs on fixed buffers, so each
+ * step's inputs are copied into them first), and "Model execution", section
+ * "Flattening a step" (the step's inputs are copied to the device
+ * asynchronously; nothing waits for them on the host).  One kernel copies
+ * nbytes from src to dst with the device's own loads: src may be pinned host
+ * memory mapped into the device's address space (the loads cross the host
+ * link) or device memory.  The kernel lets the next kernel on the stream
+ * launch at once, and that kernel's dependency wait returns only after the
+ * copy is complete, so a step's attention kernels overlap their set-up with
+ * the transfer.  It starts copying after earlier work on the stream ends.
+ *
+ *   dst     device memory, 16-byte aligned, nbytes long.
+ *   src     device-accessible memory, 16-byte aligned, nbytes long, not
+ *           overlapping dst.
+ *   nbytes  a multiple of 16 (else PKV_ERR_INVALID_ARG); 0 is a no-op.
+ * Returns PKV_OK, PKV_ERR_INVALID_ARG (null or misaligned pointer, bad size)
+ * or PKV_ERR_CUDA (launch failure).
+ */
+pkv_status pkv_stage_inputs(void* dst, const void* src, int64_t nbytes, void* stream);
 
 /*
  * pkv_num_splits - how many KV splits the decode path should use.

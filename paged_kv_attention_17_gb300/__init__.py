@@ -19,6 +19,7 @@ from ._binding import (EXPORTS, FLAG_BAD_BLOCK, FLAG_BAD_LENGTHS, FLAG_BAD_SLOT,
                        pkv_attention_varlen_e4m3, pkv_attention_varlen_noalloc,
                        pkv_build_metadata,
                        pkv_cascade_attention, pkv_cascade_splits, pkv_cascade_workspace_bytes,
-                       pkv_num_splits, pkv_status_string, pkv_workspace_bytes, pkv_write,
+                       pkv_num_splits, pkv_stage_inputs, pkv_status_string, pkv_workspace_bytes,
+                       pkv_write,
                        pkv_write_attention_varlen, pkv_write_attention_varlen_e4m3,
                        pkv_write_e4m3)

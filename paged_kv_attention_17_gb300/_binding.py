@@ -22,7 +22,7 @@ PKV_DECODE_MAX_QLEN = 4
 FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
 
 # Every symbol include/pkv.h declares.
-EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_num_splits", "pkv_workspace_bytes",
+EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_stage_inputs", "pkv_num_splits", "pkv_workspace_bytes",
            "pkv_attention_varlen", "pkv_write_attention_varlen", "pkv_attention_varlen_window",
            "pkv_attention_varlen_e4m3", "pkv_write_attention_varlen_e4m3",
            "pkv_attention_varlen_noalloc", "pkv_cascade_splits", "pkv_cascade_workspace_bytes",
@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
         L.pkv_write_e4m3.argtypes = [vp, vp, vp, i64, vp, vp, i64, i32, i32, i32, i32, f32, f32,
                                      vp, vp]
         L.pkv_write_e4m3.restype = i32
+        L.pkv_stage_inputs.argtypes = [vp, vp, i64, vp]
+        L.pkv_stage_inputs.restype = i32
         L.pkv_num_splits.argtypes = [i32] * 7
         L.pkv_num_splits.restype = i32
         L.pkv_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -147,6 +149,24 @@ def pkv_write_e4m3(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scal
                                 int(bs), int(hkv), int(d), _dtype_code(k_new.dtype),
                                 float(k_scale), float(v_scale), _ptr(error_flag), _stream(stream))
     _check("pkv_write_e4m3", code)
+
+
+def pkv_stage_inputs(dst, src, stream=None):
+    """Copy the bytes of src (pinned host memory the device can address, or
+    device memory) into the device tensor dst with one library kernel that
+    lets the next kernel on the stream start at once.  Both contiguous, same
+    byte size (a multiple of 16), 16-byte aligned."""
+    if not dst.is_cuda:
+        raise ValueError("dst must be a device tensor")
+    if not src.is_cuda and not src.is_pinned():
+        raise ValueError("src must be pinned host memory or a device tensor")
+    if not dst.is_contiguous() or not src.is_contiguous():
+        raise ValueError("dst and src must be contiguous")
+    n = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != n:
+        raise ValueError("dst and src differ in size")
+    _check("pkv_stage_inputs", lib().pkv_stage_inputs(_ptr(dst), _ptr(src), int(n),
+                                                      _stream(stream)))
 
 
 def pkv_num_splits(num_seqs, max_query_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,

@@ -9,6 +9,8 @@
 #include "common.cuh"
 
 namespace pkv {
+cudaError_t launch_stage_copy(void* dst, const void* src, int64_t bytes, int num_sms,
+                              cudaStream_t stream);
 cudaError_t launch_kv_write(const void* k_new, const void* v_new, const int64_t* slots,
                             int64_t num_tokens, void* k_cache, void* v_cache, int64_t num_slots,
                             uint32_t row_bytes, int32_t* flag, int num_sms, cudaStream_t stream);
@@ -325,6 +327,16 @@ pkv_status pkv_write(const void* k_new, const void* v_new, const int64_t* slot_m
   cudaError_t e = launch_kv_write(k_new, v_new, slot_mapping, num_tokens, k_cache, v_cache,
                                   num_blocks * kBlock, static_cast<uint32_t>(row_bytes), error_flag,
                                   sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_stage_inputs(void* dst, const void* src, int64_t nbytes, void* stream) {
+  if (nbytes < 0 || nbytes % 16 != 0) return PKV_ERR_INVALID_ARG;
+  if (nbytes == 0) return PKV_OK;
+  if (!dst || !src || !aligned(dst, 16) || !aligned(src, 16)) return PKV_ERR_INVALID_ARG;
+  const int sms = current_sms();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  cudaError_t e = launch_stage_copy(dst, src, nbytes, sms, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -97,6 +97,62 @@ __global__ void __launch_bounds__(256) kv_write_e4m3_kernel(
   }
 }
 
+// Staging copy of a step's packed inputs (pkv_stage_inputs): 16-byte words
+// from src (device memory, or pinned host memory mapped into the device's
+// address space) to dst in device memory.  "Inside the engine ...", section
+// on CUDA graphs: inputs are copied asynchronously into fixed buffers before
+// the step's kernels run.  Done with the device's own loads rather than a
+// copy-engine transfer, so it sits in the kernels' dependent-launch chain:
+// the next kernel is released at once (its set-up and hinted loads overlap
+// the transfer) and its dependency wait returns when the copy is complete.
+// A CUDA graph holding copy nodes instead runs them on the copy engine
+// between the kernels, each a few microseconds with the chain broken.
+// Every thread issues all its loads before its first store, so one round
+// trip over the host link covers the whole transfer.
+constexpr int kStageWords = 4;          // 16-byte words per thread per pass
+
+__global__ void __launch_bounds__(256) stage_copy_kernel(const uint4* __restrict__ src,
+                                                         uint4* __restrict__ dst, int64_t words) {
+  pdl_launch_dependents();
+  pdl_wait_primary();                   // earlier work on the stream may still use src or dst
+  const int64_t pass = static_cast<int64_t>(gridDim.x) * blockDim.x * kStageWords;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x * kStageWords + threadIdx.x;
+       base < words; base += pass) {
+    uint4 w[kStageWords];
+#pragma unroll
+    for (int u = 0; u < kStageWords; ++u) {
+      const int64_t i = base + static_cast<int64_t>(u) * blockDim.x;
+      if (i < words) w[u] = __ldcs(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kStageWords; ++u) {
+      const int64_t i = base + static_cast<int64_t>(u) * blockDim.x;
+      if (i < words) dst[i] = w[u];
+    }
+  }
+}
+
+cudaError_t launch_stage_copy(void* dst, const void* src, int64_t bytes, int num_sms,
+                              cudaStream_t stream) {
+  const int64_t words = bytes / 16;
+  const int threads = 256;
+  int64_t blocks = (words + threads * kStageWords - 1) / (threads * kStageWords);
+  const int64_t cap = static_cast<int64_t>(num_sms) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stage_copy_kernel, static_cast<const uint4*>(src),
+                            static_cast<uint4*>(dst), words);
+}
+
 static cudaLaunchConfig_t write_config(int64_t total, int num_sms, cudaStream_t stream,
                                        cudaLaunchAttribute* attr) {
   const int threads = 256;

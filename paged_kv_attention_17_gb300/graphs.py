@@ -11,16 +11,25 @@ buckets and keeps a static memory pool.
 ``DecodeGraphRunner`` records, per capture size b (and per host staging slot),
 one graph holding a whole decode step on static buffers:
 
-1. the copy of the step's packed inputs from pinned host memory to the device,
+1. the step's packed inputs (q, new K/V, metadata) from pinned host memory
+   into the device,
 2.-3. ``pkv_write_attention_varlen``: the new tokens' K/V stored by the decode
    kernel itself, then attention (one query token per request),
 
 (``pkv_write_attention_varlen_e4m3`` over an 8-bit E4M3 cache),
-4. the copy of the output rows (and the error flag) back to pinned host memory.
+4. the output rows back to pinned host memory.
 
-With ``zero_copy`` the graph has no copy nodes: its kernels read the pinned
-staging and write the pinned output rows through the device's mapping of host
-memory (no memcpy or memset node breaks the kernels' dependent-launch chain).
+How step 1 and 4 are done (``inputs``):
+
+* ``"stage"`` (default): ``pkv_stage_inputs``, one library kernel, reads the
+  pinned staging over the host link in one burst into a device buffer and
+  releases the attention kernels at once, so their set-up overlaps the
+  transfer; the kernels write the output rows into pinned host memory.
+* ``"mapped"``: no copy at all; the attention kernels read the pinned
+  staging in place, each CTA paying host-link round trips for its metadata,
+  table entries and q rows.
+* ``"memcpy"``: copy nodes (copy engine) before and after the kernels; each
+  costs a few microseconds and breaks the kernels' dependent-launch chain.
 
 A step of B <= b requests is padded with requests of no token and no context
 (query_start_loc repeats B, seq_len 0, slot -1): both calls treat them as
@@ -116,14 +125,18 @@ class DecodeGraphRunner:
     out), used in place.  max_seq_len bounds every request's context (it sizes the split
     count at capture).  The output of a step stays valid in the returned host
     tensor until its staging slot is reused (``slots`` steps later).
-    zero_copy (default): the kernels use the pinned staging and output in
-    place over the host-device link (NVLink-C2C on a Grace-Blackwell node);
-    otherwise the graph copies them with memcpy nodes.
+    inputs: "stage" (default), "mapped" or "memcpy" - how the packed inputs
+    reach the kernels and the output rows reach the host (module docstring).
     """
 
+    INPUT_PATHS = ("stage", "mapped", "memcpy")
+
     def __init__(self, k_cache, v_cache, num_q_heads, softmax_scale, max_blocks_per_seq,
-                 max_seq_len, max_batch=64, sizes=None, slots=2, zero_copy=True,
+                 max_seq_len, max_batch=64, sizes=None, slots=2, inputs="stage",
                  kv_scales=None):
+        if inputs not in self.INPUT_PATHS:
+            raise ValueError(f"inputs must be one of {self.INPUT_PATHS}")
+        self.inputs = inputs
         self.k_cache, self.v_cache = k_cache, v_cache
         self.device = k_cache.device
         self.e4m3 = k_cache.dtype == torch.uint8
@@ -138,7 +151,6 @@ class DecodeGraphRunner:
         self.scale = float(softmax_scale)
         self.max_blocks = int(max_blocks_per_seq)
         self.max_seq_len = int(max_seq_len)
-        self.zero_copy = bool(zero_copy)
         ladder = sizes if sizes is not None else capture_ladder(max(int(max_batch), 1))
         self.sizes = sorted({int(s) for s in ladder if 1 <= int(s) <= max_batch})
         if not self.sizes or self.sizes[-1] < max_batch:
@@ -187,10 +199,14 @@ class DecodeGraphRunner:
 
     def _record(self, b, slot):
         lay = self.layouts[b]
-        if self.zero_copy:
+        if self.inputs == "mapped":
             # the kernels read the pinned staging and write the pinned output
             # rows in place (host memory mapped into the device's address space)
             v = self._views(self.host_in[slot], b)
+            out = self.host_out[slot][:b]
+        elif self.inputs == "stage":
+            B.pkv_stage_inputs(self.dev_in[:lay.nbytes], self.host_in[slot][:lay.nbytes])
+            v = self._views(self.dev_in, b)
             out = self.host_out[slot][:b]
         else:
             v = self._views(self.dev_in, b)
@@ -212,7 +228,7 @@ class DecodeGraphRunner:
                                          v["seq_lens"], v["block_table"], 1, self.max_seq_len,
                                          self.scale, causal=True, num_splits=self.splits[b],
                                          workspace=self.workspace, error_flag=self.flag)
-        if not self.zero_copy:
+        if self.inputs == "memcpy":
             self.host_out[slot][:b].copy_(self.out[:b], non_blocking=True)
             self.host_flag[slot].copy_(self.flag, non_blocking=True)
 
@@ -286,9 +302,9 @@ class DecodeGraphRunner:
 
     def result(self, step: Step):
         """Wait for the step; returns (output rows [n, hq, D] in pinned host
-        memory, device error flag value).  With zero_copy the flag is not reset
-        per step: it holds every error since the runner was made."""
+        memory, device error flag value).  Unless inputs is "memcpy" the flag is
+        not reset per step: it holds every error since the runner was made."""
         self.events[step.slot].synchronize()
-        if self.zero_copy:
+        if self.inputs != "memcpy":
             return self.host_out[step.slot][:step.n], int(self.flag.item())
         return self.host_out[step.slot][:step.n], int(self.host_flag[step.slot][0])

@@ -24,15 +24,15 @@ def _subset(w, idx):
                                k_new=w.k_new[idx], v_new=w.v_new[idx])
 
 
-@pytest.mark.parametrize("zero_copy", [False, True])
-def test_graph_runner_steps_match_oracle(zero_copy):
+@pytest.mark.parametrize("inputs", ["stage", "mapped", "memcpy"])
+def test_graph_runner_steps_match_oracle(inputs):
     rng = np.random.Generator(np.random.PCG64(5))
     ctx = rng.integers(1, 700, size=8)
     w = workloads.build("graphs", "bf16", 32, 8, 128, [(int(c) - 1, 1) for c in ctx], seed=11)
     kc, vc = to_torch(w.k_pool, "bf16", "cuda"), to_torch(w.v_pool, "bf16", "cuda")
     width = 48
     runner = DecodeGraphRunner(kc, vc, 32, w.softmax_scale, width, 700, max_batch=8,
-                               sizes=[1, 2, 4, 8], zero_copy=zero_copy)
+                               sizes=[1, 2, 4, 8], inputs=inputs)
     for idx in ([0], [0, 1, 2], list(range(8)), [3, 4, 5, 6, 7], [6, 2]):
         sub = _subset(w, np.array(idx))
         meta = metadata.build(sub.requests, sub.block_size)
@@ -88,3 +88,19 @@ def test_graph_runner_over_an_e4m3_cache():
         slots = meta["slot_mapping"]
         got_k = kc.view(-1, 8, 128)[torch.from_numpy(slots).cuda()].cpu().numpy()
         assert np.array_equal(got_k, kc_ref.reshape(-1, 8, 128)[slots])
+
+
+@pytest.mark.parametrize("nbytes", [16, 4096, 16 * 1000 + 16 * 7, 5 << 20])
+def test_stage_inputs_copies_pinned_host_bytes_exactly(nbytes):
+    import paged_kv_attention_17_gb300 as pkv
+    g = torch.Generator().manual_seed(nbytes)
+    src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g).pin_memory()
+    dst = torch.zeros(nbytes + 64, dtype=torch.uint8, device="cuda")
+    pkv.pkv_stage_inputs(dst[:nbytes], src)
+    dev_src = src.cuda()
+    dst2 = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    pkv.pkv_stage_inputs(dst2, dev_src)            # device memory as the source too
+    torch.cuda.synchronize()
+    assert torch.equal(dst[:nbytes].cpu(), src)
+    assert int(dst[nbytes:].count_nonzero()) == 0  # nothing written past the end
+    assert torch.equal(dst2, dev_src)

@@ -128,6 +128,20 @@ def test_attention_host_validation(pkv, over, code):
     assert _attn_call(pkv, **over) == code
 
 
+def test_stage_inputs_host_validation(pkv):
+    L = pkv.lib()
+    vp = ctypes.c_void_p
+    # zero bytes is a no-op; sizes that are not whole 16-byte words, negative
+    # sizes, null and misaligned pointers are rejected before any launch
+    assert L.pkv_stage_inputs(None, None, 0, None) == 0
+    assert L.pkv_stage_inputs(vp(16), vp(16), 24, None) == 1
+    assert L.pkv_stage_inputs(vp(16), vp(16), -16, None) == 1
+    assert L.pkv_stage_inputs(None, vp(16), 32, None) == 1
+    assert L.pkv_stage_inputs(vp(16), None, 32, None) == 1
+    assert L.pkv_stage_inputs(vp(24), vp(16), 32, None) == 1
+    assert L.pkv_stage_inputs(vp(16), vp(40), 32, None) == 1
+
+
 def test_write_host_validation(pkv):
     L = pkv.lib()
     vp = ctypes.c_void_p
