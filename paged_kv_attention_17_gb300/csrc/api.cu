@@ -282,7 +282,11 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
         (!sw && (!encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
                  !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))))
       return PKV_ERR_CUDA;
-    e = launch_prefill(a, qmap, kmap_sw, vmap_sw, st);
+    // the decode kernel (and the combine) ahead of it release it only after
+    // their own dependency waits: its inputs are complete at launch
+    AttnArgs p = a;
+    p.defer_wait = 1;
+    e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

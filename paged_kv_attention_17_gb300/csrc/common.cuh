@@ -66,6 +66,9 @@ struct AttnArgs {
   // Fused write (decode-class steps): each CTA stores the K/V rows (its KV
   // head) of the new tokens whose positions it reads, before loading them.
   int fuse_write;
+  // Prefill launched behind the same call's decode kernel: its dependency
+  // wait moves from the start to each CTA's exit (see prefill.cu).
+  int defer_wait;
   const void* k_new;      // [num_tokens, hkv, D], the cache's element type
   const void* v_new;
   const int64_t* slots;   // slot_mapping

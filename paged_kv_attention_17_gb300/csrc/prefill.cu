@@ -256,7 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h0 = packed ? 0 : 2 * yidx;                  // query heads h0, h0 + 1 (same KV head)
   const int tglob = static_cast<int>(blockIdx.x / static_cast<unsigned>(ys));
 
-  pdl_wait_primary();
+  // defer_wait: launched behind the decode kernel of the same call, whose
+  // CTAs release this grid only after their own dependency wait, so every
+  // input read here is already complete; the wait moves to each CTA's exit,
+  // keeping the call complete only when both grids are, and the prefill
+  // tiles run in the decode grid's tail
+  if (!a.defer_wait) pdl_wait_primary();
   pdl_launch_dependents();
 
   // ---- which (request, query tile) this CTA owns: warp 0 scans the long
@@ -299,7 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   const int r = misc[0];
-  if (r < 0) return;                                     // past the last tile
+  if (r < 0) {                                           // past the last tile
+    if (a.defer_wait) pdl_wait_primary();
+    return;
+  }
   const int tile = misc[1];
   const int q0 = packed ? 0 : __ldg(a.qsl + r);
   const int q1 = packed ? static_cast<int>(a.num_tokens) : __ldg(a.qsl + r + 1);
@@ -307,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L = packed ? a.prefix_len : __ldg(a.seq_lens + r);
   if (q0 < 0 || q1 > a.num_tokens || (n > L && !packed) || n > a.max_query_len) {
     if (threadIdx.x == 0 && h0 == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
+    if (a.defer_wait) pdl_wait_primary();
     return;
   }
   const int g = packed ? yidx % a.hkv : h0 / a.group;
@@ -318,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nblk_ctx = (kv_len + kBlock - 1) / kBlock;
   if ((L + kBlock - 1) / kBlock > a.max_blocks_per_seq) {
     if (threadIdx.x == 0) raise_flag(a.flag, PKV_FLAG_BAD_LENGTHS);
+    if (a.defer_wait) pdl_wait_primary();
     return;
   }
   // sliding window: key tiles wholly below the first row's window start are
@@ -341,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c) a.ws_o[w * 128 + c] = 0.f;
         a.ws_lse[w] = -INFINITY;
       }
+      if (a.defer_wait) pdl_wait_primary();
       return;
     }
   }
@@ -703,6 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase),
                  "r"(kTmemCols));
+  if (a.defer_wait) pdl_wait_primary();
 }
 
 // The tensor-core path pairs two query heads of one KV head per CTA, so the
