@@ -612,31 +612,13 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
   const bool tc = prefill_packed_supported(head_dim, dtype == PKV_BF16,
                                            num_q_heads / num_kv_heads) &&
                   softmax_scale > 0.f;
-  if (S > 0) {
-    // 1. every row over the shared prefix, split S ways: partials 0..S-1
-    AttnArgs p = a;
-    p.block_table = shared_block_table;
-    p.max_blocks_per_seq = shared_blocks;
-    p.num_seqs = 1;
-    p.max_query_len = static_cast<int>(num_tokens);
-    p.max_seq_len = shared_blocks * kBlock;
-    p.causal = 0;
-    p.num_splits = S;
-    p.long_rows = 1;
-    p.cascade = 1;
-    p.prefix_len = shared_blocks * kBlock;
-    if (tc) {
-      CUtensorMap qmap, kmap_sw = kmap, vmap_sw = vmap;
-      if (!encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, p.group) ||
-          (!sw && (!encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
-                   !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))))
-        return PKV_ERR_CUDA;
-      e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
-    } else {
-      e = launch_decode(p, kmap, vmap, et, head_dim, /*pdl=*/true, st);
-    }
-  }
-  if (e == cudaSuccess) {
+  // Two independent passes write disjoint partials; the merge reads both.
+  // With the tensor-core prefix pass the own-key pass goes first and the
+  // prefix pass behind it defers its dependency wait to its CTAs' exits (its
+  // inputs are complete once the own-key CTAs release it), so the prefix
+  // tiles run in the own-key grid's tail; the CUDA-core prefix pass runs
+  // first, in stream order.
+  auto own_keys = [&]() -> cudaError_t {
     // 2. each request over its own keys (causal): partial S
     AttnArgs u = a;
     u.seq_lens = suffix_lens;
@@ -650,8 +632,35 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
     u.long_rows = max_query_len > kDecodeMaxQ ? 1 : 0;
     u.cascade = 2;
     u.cascade_slot = S;
-    e = launch_decode(u, kmap, vmap, et, head_dim, /*pdl=*/true, st);
+    return launch_decode(u, kmap, vmap, et, head_dim, /*pdl=*/true, st);
+  };
+  if (tc) e = own_keys();
+  if (e == cudaSuccess && S > 0) {
+    // 1. every row over the shared prefix, split S ways: partials 0..S-1
+    AttnArgs p = a;
+    p.block_table = shared_block_table;
+    p.max_blocks_per_seq = shared_blocks;
+    p.num_seqs = 1;
+    p.max_query_len = static_cast<int>(num_tokens);
+    p.max_seq_len = shared_blocks * kBlock;
+    p.causal = 0;
+    p.num_splits = S;
+    p.long_rows = 1;
+    p.cascade = 1;
+    p.prefix_len = shared_blocks * kBlock;
+    p.defer_wait = tc ? 1 : 0;
+    if (tc) {
+      CUtensorMap qmap, kmap_sw = kmap, vmap_sw = vmap;
+      if (!encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, p.group) ||
+          (!sw && (!encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
+                   !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))))
+        return PKV_ERR_CUDA;
+      e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
+    } else {
+      e = launch_decode(p, kmap, vmap, et, head_dim, /*pdl=*/true, st);
+    }
   }
+  if (e == cudaSuccess && !tc) e = own_keys();
   if (e == cudaSuccess) {
     // 3. merge the S + 1 partials of every row
     AttnArgs c = a;
