@@ -243,6 +243,13 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Bring `bytes` contiguous bytes at p into L2 with one bulk operation (a hint
+// carried out by the asynchronous copy unit; p 16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue / wait until the previous kernel's writes are visible.
 __device__ __forceinline__ void pdl_launch_dependents() {

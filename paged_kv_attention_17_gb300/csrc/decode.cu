@@ -436,13 +436,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   bool hint_ok = false;
   if (z == 0 && a.window == 0 && a.cascade == 0) {
     // ---- L2 warm-up while the previous kernel finishes: the K/V blocks this
-    //      CTA will most likely read (the hinted split range, cut at the
-    //      request's length, the table row and a cap), each warp its own
-    //      tiles.  The table and lengths read here may still change before the
-    //      wait, so they only steer prefetches: every value used below is
-    //      re-read after the wait, and L2 stays coherent with the previous
-    //      kernel's writes.  Only the first row tile of a request warms L2
-    //      (the others share its blocks or exit at once). ----
+    //      split will most likely read (the hinted split range, cut at the
+    //      request's length, the table row and a cap).  A block of the cache
+    //      holds every KV head's rows contiguously, and the CTAs of the split
+    //      (one per KV head) read the same blocks, so CTA g warms every
+    //      hkv-th block of the range whole, K and V, with one bulk prefetch
+    //      each: a few operations of the asynchronous copy unit instead of a
+    //      line-by-line stream of load-unit requests, which the loads after
+    //      the wait would queue behind.  The table and lengths read here may
+    //      still change before the wait, so they only steer prefetches: every
+    //      value used below is re-read after the wait, and L2 stays coherent
+    //      with the previous kernel's writes.  Only the first row tile of a
+    //      request warms L2 (the others share its blocks or exit at once). ----
     // L2-only loads (ld.global.cg): nothing read before the wait may sit in L1,
     // where the read-only loads after the wait could find a stale copy
     const int len_hint = min(max(__ldcg(a.seq_lens + r), 0), a.max_seq_len);
@@ -454,25 +459,19 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
                                : min(min(min(spec_b0 + per_spec, (len_hint + kBlock - 1) / kBlock),
                                          spec_b0 + pf_cap),
                                      nb_spec);
-    constexpr int kLines = C::kRowBytes / 128 > 0 ? C::kRowBytes / 128 : 1;  // lines per row
-    const int64_t head_off = static_cast<int64_t>(g) * C::kRowBytes;
-    const int64_t slot_bytes = static_cast<int64_t>(a.hkv) * C::kRowBytes;
     if (p_act && spec_possible && spec_b0 + pw < sb1) {
       e_hint = __ldcg(table + spec_b0 + pw);
       hint_ok = true;
     }
-    for (int j0 = 0; !producer && spec_b0 + warp + W * j0 < sb1; j0 += 32) {
-      const int bb = spec_b0 + warp + W * (j0 + lane);
-      const int32_t e = bb < sb1 ? __ldcg(table + bb) : -1;
-      for (int i = 0; i < 32 && spec_b0 + warp + W * (j0 + i) < sb1; ++i) {
-        const int32_t id = __shfl_sync(0xffffffffu, e, i);
+    if (!producer && warp == 0) {
+      const int64_t block_bytes = static_cast<int64_t>(kBlock) * a.hkv * C::kRowBytes;
+      for (int bb = spec_b0 + g + a.hkv * lane; bb < sb1; bb += 32 * a.hkv) {
+        const int32_t id = __ldcg(table + bb);
         if (id < 0 || id >= a.num_blocks) continue;
-        for (int u = lane; u < kBlock * kLines; u += 32) {
-          const int64_t off = (static_cast<int64_t>(id) * kBlock + u / kLines) * slot_bytes +
-                              head_off + (u % kLines) * 128;
-          prefetch_l2(static_cast<const uint8_t*>(a.k_cache) + off);
-          prefetch_l2(static_cast<const uint8_t*>(a.v_cache) + off);
-        }
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.k_cache) + id * block_bytes,
+                         static_cast<uint32_t>(block_bytes));
+        bulk_prefetch_l2(static_cast<const uint8_t*>(a.v_cache) + id * block_bytes,
+                         static_cast<uint32_t>(block_bytes));
       }
     }
   }
