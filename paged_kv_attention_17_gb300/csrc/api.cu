@@ -274,6 +274,11 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     return PKV_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // an unsplit launch of a few requests starts the longest first, unless a
+  // prefill launch follows: that one starts once every decode CTA has
+  // started, which the long CTAs first would delay
+  const bool prefill_follows = tc_prefill && max_query_len > kDecodeMaxQ;
+  a.lpt = splits == 1 && num_seqs >= 2 && num_seqs <= kLptMaxSeqs && !prefill_follows ? 1 : 0;
   cudaError_t e = launch_decode(a, kmap, vmap, et, head_dim, /*pdl=*/true, st);
   if (e == cudaSuccess && splits > 1) e = launch_combine(a, et, head_dim, st);
   if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ) {
@@ -632,6 +637,8 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
     u.long_rows = max_query_len > kDecodeMaxQ ? 1 : 0;
     u.cascade = 2;
     u.cascade_slot = S;
+    // (no longest-first order when the deferred prefix pass follows it)
+    u.lpt = !tc && num_seqs >= 2 && num_seqs <= kLptMaxSeqs ? 1 : 0;
     return launch_decode(u, kmap, vmap, et, head_dim, /*pdl=*/true, st);
   };
   if (tc) e = own_keys();

@@ -23,6 +23,7 @@ enum class ElemType { kF32, kBf16, kE4m3 };
 constexpr int kBlock = 16;                       // tokens per KV-cache block
 constexpr int kDecodeMaxQ = PKV_DECODE_MAX_QLEN; // decode-class bound on q_len
 constexpr int kMaxSplits = 64;
+constexpr int kLptMaxSeqs = 256;                // longest-first dispatch: up to this many requests
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // ~2 s per wait
@@ -69,6 +70,9 @@ struct AttnArgs {
   // Prefill launched behind the same call's decode kernel: its dependency
   // wait moves from the start to each CTA's exit (see prefill.cu).
   int defer_wait;
+  // Unsplit decode launch of 2..256 requests: blockIdx.z is read as a rank of
+  // the requests by decreasing seq_len (longest first; see decode.cu).
+  int lpt;
   const void* k_new;      // [num_tokens, hkv, D], the cache's element type
   const void* v_new;
   const int64_t* slots;   // slot_mapping

@@ -229,11 +229,13 @@ struct DecodeCfg {
   // Consumer (compute) warps per CTA, plus one TMA producer warp.  CUDA-core
   // build: 11 + 1 warps (three per SM sub-partition, 168 registers each) for
   // 4-row tiles, whose register-q path fits that budget; wider tiles keep
-  // 255 registers with 7 + 1 warps; one CTA per SM.  Tensor-core build: 6 + 1
-  // warps and a 96 KB ring (two or four stages per warp), so two CTAs fit on
-  // an SM and the next launch's CTAs become resident (and warm L2) while this
-  // one streams.
-  static constexpr int kWarps = kMma ? 6 : (R == 4 ? 11 : 7);
+  // 255 registers with 7 + 1 warps; one CTA per SM.  Tensor-core build: a 96
+  // KB ring, so two CTAs fit on an SM and the next launch's CTAs become
+  // resident (and warm L2) while this one streams; 6 + 1 warps (two stages of
+  // bf16 per warp), or 7 + 1 over an E4M3 cache, whose half-size stages still
+  // give each warp three and whose longer per-block path gains from the extra
+  // warp (8 + 1 would leave 96 registers a thread).
+  static constexpr int kWarps = kMma ? (kIsE4m3<T> ? 7 : 6) : (R == 4 ? 11 : 7);
   static constexpr int kRingBudget = kMma ? 98304 : 196608;
   static constexpr int kStagesRaw = kRingBudget / (kWarps * kStageBytes);
   static constexpr int kStagesPerWarp = kStagesRaw < 1 ? 1 : (kStagesRaw > 6 ? 6 : kStagesRaw);
@@ -324,6 +326,48 @@ __device__ __forceinline__ int64_t part_row(const AttnArgs& a, int s, int r, int
                    : ws_row(a, s, r, i, h);
 }
 
+// Longest-first dispatch of an unsplit launch (at most kLptMaxSeqs requests):
+// the request whose rank, by decreasing seq_len (ties by index), equals
+// `rank`.  After the dependency wait every CTA computes the same ranking from
+// the same seq_lens, so the ranks are a bijection onto the requests; the
+// request's query_start_loc pair and seq_len, loaded in the same round trip,
+// are returned too.  Before the wait (hint = true, L2-only loads of values
+// that may still change) the result only steers the L2 warm-up.  Keys are
+// unique (length in the high bits, reversed index in the low nine), so a
+// request's rank is the number of keys above its own.  Called by every thread.
+__device__ __forceinline__ int request_by_length_rank(const AttnArgs& a, int rank, bool hint,
+                                                      int& q0, int& q1, int& len) {
+  __shared__ uint32_t s_key[kLptMaxSeqs];
+  __shared__ int s_len[kLptMaxSeqs];
+  __shared__ int s_qsl[kLptMaxSeqs + 1];
+  __shared__ int s_pick;
+  const int n = a.num_seqs;
+  for (int i = threadIdx.x; i <= n; i += blockDim.x) {
+    s_qsl[i] = hint ? __ldcg(a.qsl + i) : __ldg(a.qsl + i);
+    if (i < n) {
+      const int L = hint ? __ldcg(a.seq_lens + i) : __ldg(a.seq_lens + i);
+      s_len[i] = L;
+      s_key[i] = (static_cast<uint32_t>(min(max(L, 0), (1 << 22) - 1)) << 9) |
+                 static_cast<uint32_t>(511 - i);
+    }
+  }
+  if (threadIdx.x == 0) s_pick = rank;     // (every rank is taken below)
+  __syncthreads();
+  for (int c = threadIdx.x; c < n; c += blockDim.x) {
+    const uint32_t kc = s_key[c];
+    int above = 0;
+    for (int j = 0; j < n; ++j) above += s_key[j] > kc ? 1 : 0;
+    if (above == rank) s_pick = c;
+  }
+  __syncthreads();
+  const int r = s_pick;
+  q0 = s_qsl[r];
+  q1 = s_qsl[r + 1];
+  len = s_len[r];
+  __syncthreads();                          // the arrays are reused by a second call
+  return r;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -410,7 +454,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   const int g = blockIdx.x % a.hkv;
   const int s = blockIdx.x / a.hkv;
   const int z = blockIdx.y;
-  const int r = blockIdx.z;
+  // the request: blockIdx.z, or (longest-first launches) the request of that
+  // rank by length, hinted before the wait and settled after it
+  int hq0 = 0, hq1 = 0, hlen = 0;
+  const int r_grid = a.lpt ? request_by_length_rank(a, blockIdx.z, true, hq0, hq1, hlen)
+                           : static_cast<int>(blockIdx.z);
 
   // ---- set-up that reads no input: under programmatic dependent launch it
   //      overlaps the tail of the previous kernel in the stream ----
@@ -427,7 +475,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
     fence_mbar_init();
   }
   __syncthreads();
-  const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
+  const int32_t* table_hint = a.block_table + static_cast<int64_t>(r_grid) * a.max_blocks_per_seq;
   // the split range a context of max_seq_len keys gives (the pre-launch hint)
   const int nb_spec = min((a.max_seq_len + kBlock - 1) / kBlock, a.max_blocks_per_seq);
   const int per_spec = a.num_splits > 1 ? (nb_spec + a.num_splits - 1) / a.num_splits : nb_spec;
@@ -450,8 +498,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
     //      request warms L2 (the others share its blocks or exit at once). ----
     // L2-only loads (ld.global.cg): nothing read before the wait may sit in L1,
     // where the read-only loads after the wait could find a stale copy
-    const int len_hint = min(max(__ldcg(a.seq_lens + r), 0), a.max_seq_len);
-    const int n_hint = __ldcg(a.qsl + r + 1) - __ldcg(a.qsl + r);
+    const int len_hint = min(max(__ldcg(a.seq_lens + r_grid), 0), a.max_seq_len);
+    const int n_hint = __ldcg(a.qsl + r_grid + 1) - __ldcg(a.qsl + r_grid);
     const bool runs_here = n_hint >= 1 && (n_hint <= kDecodeMaxQ || a.long_rows);
     // tensor-core build without a split: the blocks of the first ring fill
     const int pf_cap = kMma && a.num_splits == 1 ? C::kStages : C::kPrefetchBlocks;
@@ -460,13 +508,13 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
                                          spec_b0 + pf_cap),
                                      nb_spec);
     if (p_act && spec_possible && spec_b0 + pw < sb1) {
-      e_hint = __ldcg(table + spec_b0 + pw);
+      e_hint = __ldcg(table_hint + spec_b0 + pw);
       hint_ok = true;
     }
     if (!producer && warp == 0) {
       const int64_t block_bytes = static_cast<int64_t>(kBlock) * a.hkv * C::kRowBytes;
       for (int bb = spec_b0 + g + a.hkv * lane; bb < sb1; bb += 32 * a.hkv) {
-        const int32_t id = __ldcg(table + bb);
+        const int32_t id = __ldcg(table_hint + bb);
         if (id < 0 || id >= a.num_blocks) continue;
         bulk_prefetch_l2(static_cast<const uint8_t*>(a.k_cache) + id * block_bytes,
                          static_cast<uint32_t>(block_bytes));
@@ -477,20 +525,27 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   }
 
   // where this request's rows start in q (an address hint, read L2-only)
-  const int q0_hint = kMma && !producer && a.cascade != 1 ? __ldcg(a.qsl + r) : 0;
+  const int q0_hint = kMma && !producer && a.cascade != 1 ? __ldcg(a.qsl + r_grid) : 0;
 
   // ---- inputs only after the wait ----
   pdl_wait_primary();
   pdl_launch_dependents();
+  // longest request first: the grid's CTAs start in block-index order, so an
+  // unsplit launch of requests of unequal length ends with a tail of long
+  // ones unless blockIdx.z is read as a rank of the requests by length
+  int lq0 = 0, lq1 = 0, llen = 0;
+  const int r = a.lpt ? request_by_length_rank(a, blockIdx.z, false, lq0, lq1, llen) : r_grid;
+  const int32_t* table = a.block_table + static_cast<int64_t>(r) * a.max_blocks_per_seq;
   // The request's metadata and the table entries of the hinted split range
   // are the first loads after the wait (everything after depends on them);
   // the speculative q rows and K/V boxes go out behind them.
   // cascade prefix pass: one request holding every row of the batch, over the
   // prefix_len shared keys
   const bool prefix_pass = a.cascade == 1;
-  const int md_q0 = prefix_pass ? 0 : ld_early(a.qsl + r);
-  const int md_q1 = prefix_pass ? static_cast<int>(a.num_tokens) : ld_early(a.qsl + r + 1);
-  const int md_L = prefix_pass ? a.prefix_len : ld_early(a.seq_lens + r);
+  const int md_q0 = prefix_pass ? 0 : (a.lpt ? lq0 : ld_early(a.qsl + r));
+  const int md_q1 = prefix_pass ? static_cast<int>(a.num_tokens)
+                                : (a.lpt ? lq1 : ld_early(a.qsl + r + 1));
+  const int md_L = prefix_pass ? a.prefix_len : (a.lpt ? llen : ld_early(a.seq_lens + r));
   // the table entries of warp pw's first two blocks of the hinted split range:
   // the verdict on the speculative block and the first loads need no second
   // round trip when the real range starts at the hinted block

@@ -165,6 +165,27 @@ def test_split_count_changes_nothing_f32():
             assert np.abs(a - b).max() <= 1e-3
 
 
+@pytest.mark.parametrize("num_seqs", [2, 37, 256, 257])
+def test_longest_first_dispatch_unsplit(num_seqs):
+    # An unsplit launch of 2..256 requests reads blockIdx.z as a rank of the
+    # requests by decreasing seq_len; ties (equal lengths), idle requests (no
+    # new token) and a prefill chunk in the batch must all keep their own
+    # rows.  257 requests take the plain order.
+    rng = np.random.Generator(np.random.PCG64(num_seqs))
+    ctx = rng.choice([1, 16, 17, 200, 200, 513], size=num_seqs)
+    shape = [(int(c) - 1, 1) for c in ctx]
+    shape[0] = (0, 0)                        # idle request
+    if num_seqs > 2:
+        shape[1] = (40, 9)                   # a short prefill chunk
+    w = workloads.build(f"lpt_{num_seqs}", "bf16", 8, 2, 128, shape, seed=num_seqs)
+    dev = device_inputs(w)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    out, lse, flag = run_step(dev, num_splits=1)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    _check_lse(lse, lse_ref)
+
+
 def test_split_heuristic_rule():
     # one wave of split CTAs over 7/8 of the decode CTA slots (two per SM for
     # the bf16 tensor-core build), at least 8 blocks per split, split off once
