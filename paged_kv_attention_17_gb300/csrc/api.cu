@@ -106,6 +106,47 @@ bool encode_cache_map(CUtensorMap* map, const void* base, int64_t num_slots, int
   return r == CUDA_SUCCESS;
 }
 
+// 4-D map for the tensor-core decode over a cache viewed as (column within a
+// 128-byte slice, slot, slice, KV head): a box is every 128-byte column slice
+// of 16 slots' rows of one head, landing slice-major ([slice][16 rows][128
+// B], 128B swizzle), so one copy brings a block's K (or V) of one head.  The
+// dimensions' strides need not increase: the slot stride is a whole cache
+// row, the slice stride 128 bytes, the head stride one head's row.
+bool encode_slices_map(CUtensorMap* map, const void* base, int64_t num_slots, int hkv, int d,
+                       ElemType et) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t es = et == ElemType::kBf16 ? 2 : 1;
+  const CUtensorMapDataType dt = et == ElemType::kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const cuuint64_t row = static_cast<cuuint64_t>(d) * es;   // one head's row, bytes
+  if (row % 128 != 0) return false;
+  cuuint64_t dims[4] = {128 / es, static_cast<cuuint64_t>(num_slots), row / 128,
+                        static_cast<cuuint64_t>(hkv)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(hkv) * row, 128, row};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kBlock),
+                       static_cast<cuuint32_t>(row / 128), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The decode kernel's maps: rows of several 128-byte slices (bf16, D 128)
+// take the 4-D slice map; other tensor-core rows the 128B-swizzled 3-D map
+// (one slice per row); the CUDA-core build unswizzled whole rows.
+bool encode_decode_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* k_cache,
+                        const void* v_cache, int64_t num_slots, int hkv, int d, ElemType et) {
+  const bool sw = decode_swizzled(et, d);
+  const int64_t row = static_cast<int64_t>(d) * (et == ElemType::kF32 ? 4 : (et == ElemType::kBf16 ? 2 : 1));
+  if (sw && row > 128)
+    return encode_slices_map(kmap, k_cache, num_slots, hkv, d, et) &&
+           encode_slices_map(vmap, v_cache, num_slots, hkv, d, et);
+  return encode_cache_map(kmap, k_cache, num_slots, hkv, d, et, sw) &&
+         encode_cache_map(vmap, v_cache, num_slots, hkv, d, et, sw);
+}
+
 // 3-D map over q viewed as [num_tokens, num_q_heads, head_dim]: a box is 128
 // tokens of one head (or, with heads_per_box = a GQA group, 128 / group tokens
 // of the group's heads), 64 columns wide (128 bytes, 128B swizzle).
@@ -265,12 +306,9 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     a.wv_scale = v_scale;
   }
 
-  // the decode kernel's tensor-core build takes 128B-swizzled boxes, the
-  // same maps the tensor-core prefill takes
-  const bool sw = decode_swizzled(et, head_dim);
+  // the decode kernel's maps (the tensor-core prefill encodes its own below)
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, sw) ||
-      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, sw))
+  if (!encode_decode_maps(&kmap, &vmap, k_cache, v_cache, num_slots, num_kv_heads, head_dim, et))
     return PKV_ERR_CUDA;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -282,10 +320,10 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
   cudaError_t e = launch_decode(a, kmap, vmap, et, head_dim, /*pdl=*/true, st);
   if (e == cudaSuccess && splits > 1) e = launch_combine(a, et, head_dim, st);
   if (e == cudaSuccess && tc_prefill && max_query_len > kDecodeMaxQ) {
-    CUtensorMap qmap, kmap_sw = kmap, vmap_sw = vmap;
+    CUtensorMap qmap, kmap_sw, vmap_sw;
     if (num_tokens > 0x7FFFFFFFll || !encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim) ||
-        (!sw && (!encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
-                 !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))))
+        !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
+        !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
       return PKV_ERR_CUDA;
     // the decode kernel (and the combine) ahead of it release it only after
     // their own dependency waits: its inputs are complete at launch
@@ -605,10 +643,8 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
   a.num_blocks = num_blocks;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
-  const bool sw = decode_swizzled(et, head_dim);
   CUtensorMap kmap, vmap;
-  if (!encode_cache_map(&kmap, k_cache, num_slots, num_kv_heads, head_dim, et, sw) ||
-      !encode_cache_map(&vmap, v_cache, num_slots, num_kv_heads, head_dim, et, sw))
+  if (!encode_decode_maps(&kmap, &vmap, k_cache, v_cache, num_slots, num_kv_heads, head_dim, et))
     return PKV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -657,10 +693,10 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
     p.prefix_len = shared_blocks * kBlock;
     p.defer_wait = tc ? 1 : 0;
     if (tc) {
-      CUtensorMap qmap, kmap_sw = kmap, vmap_sw = vmap;
+      CUtensorMap qmap, kmap_sw, vmap_sw;
       if (!encode_q_map(&qmap, q, num_tokens, num_q_heads, head_dim, p.group) ||
-          (!sw && (!encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
-                   !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))))
+          !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
+          !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
         return PKV_ERR_CUDA;
       e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
     } else {

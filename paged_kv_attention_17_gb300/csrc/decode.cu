@@ -220,11 +220,14 @@ struct DecodeCfg {
   // (16 rows of the head's kRowBytes); the register-q path has the 8 lanes of
   // a quarter-warp read 8 consecutive 16-byte chunks of one key row, the
   // generic path rotates each lane's chunk order by its key, so neither
-  // conflicts on shared-memory banks.  Tensor-core build: each 128-byte
-  // column slice of a row is its own box in the 128B-swizzled layout, so the
-  // ldmatrix row reads of 8 consecutive keys hit 8 distinct bank groups.
-  static constexpr int kBoxes = kMma ? kRowBytes / 128 : 1;
-  static constexpr int kBoxBytes = kBlock * kRowBytes / kBoxes;
+  // conflicts on shared-memory banks.  Tensor-core build: the rows' 128-byte
+  // column slices land slice-major ([slice][16 rows][128 B], 128B-swizzled),
+  // so the ldmatrix row reads of 8 consecutive keys hit 8 distinct bank
+  // groups; one 4-D box (column, slot, slice, head) brings all slices of a
+  // block, since the copy unit takes a warp's boxes one at a time (~37 ns
+  // each), which bounds a block's issue, not its bytes.
+  static constexpr int kBoxes = 1;                          // boxes per block of K (of V)
+  static constexpr int kBoxBytes = kMma ? kBlock * 128 : kBlock * kRowBytes;  // per column slice
   static constexpr int kStageBytes = 2 * kBlock * kRowBytes;   // one block of K and of V
   // Consumer (compute) warps per CTA, plus one TMA producer warp.  CUDA-core
   // build: 11 + 1 warps (three per SM sub-partition, 168 registers each) for
@@ -587,12 +590,14 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   // barrier's byte count.
   const uint64_t pol = l2_policy_evict_first();
   auto issue_box = [&](int st, int row) {
-    const int b = pp % C::kBoxes;
     const bool v = pp >= C::kBoxes;
     uint64_t* bar = v ? &vfull[st] : &kfull[st];
-    if (b == 0) mbar_arrive_expect_tx(bar, kBlock * C::kRowBytes);
-    tma_load_3d(smem + st * C::kStageBytes + (v ? kBlock * C::kRowBytes : 0) + b * C::kBoxBytes,
-                v ? &vmap : &kmap, bar, b * (128 / static_cast<int>(sizeof(T))), g, row, pol);
+    mbar_arrive_expect_tx(bar, kBlock * C::kRowBytes);
+    uint8_t* dst = smem + st * C::kStageBytes + (v ? kBlock * C::kRowBytes : 0);
+    if constexpr (C::kMma && C::kRowBytes > 128)   // several 128-byte slices: the 4-D map
+      tma_load_4d(dst, v ? &vmap : &kmap, bar, 0, row, 0, g, pol);
+    else
+      tma_load_3d(dst, v ? &vmap : &kmap, bar, 0, g, row, pol);
   };
   // Speculative first block: warp pw's first block of the hinted split range
   // goes into its stage 0 at once - the K/V data is read after the wait,
