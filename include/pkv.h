@@ -40,10 +40,11 @@
  * Entry points: pkv_write / pkv_write_e4m3 (slot-mapped write), pkv_stage_inputs
  * (a step's packed inputs copied to the device), pkv_num_splits
  * and pkv_workspace_bytes (split-KV sizing), pkv_attention_varlen and its
- * variants _window (sliding window), _e4m3 (8-bit cache) and _noalloc (no
- * caller workspace), pkv_write_attention_varlen / _e4m3 (write and attend in
- * one call, the write folded into the decode kernel for decode steps), pkv_cascade_splits / pkv_cascade_workspace_bytes /
- * pkv_cascade_attention (requests sharing a block-aligned prefix),
+ * variants _window (sliding window), _e4m3 (8-bit cache), _e4m3_window and
+ * _noalloc (no caller workspace), pkv_write_attention_varlen / _e4m3 (write
+ * and attend in one call, the write folded into the decode kernel for decode
+ * steps), pkv_cascade_splits / pkv_cascade_workspace_bytes /
+ * pkv_cascade_attention / _e4m3 (requests sharing a block-aligned prefix),
  * pkv_build_metadata (the step's flat-batch metadata, host only) and
  * pkv_status_string.
  */
@@ -290,8 +291,10 @@ pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const
  * value j for v_scale * value(code), so
  *   out[t, h, :] = v_scale * sum_j softmax_j(softmax_scale * k_scale *
  *                  q[t,h,:] . value(K code_j)) value(V code_j)
- * (lse_out: the natural-log log-sum-exp of those scaled scores).  Codes are
- * widened to fp32 in registers; the arithmetic is that of the bf16 path.
+ * (lse_out: the natural-log log-sum-exp of those scaled scores).  At head_dim
+ * 128 codes are widened exactly to f16 and contracted on tensor cores with q
+ * scaled by a power of two (fp32 accumulation, P rounded to f16 for P.V); at
+ * head_dim 64 they are widened to fp32 in registers.
  *   q, out            device bf16 [num_tokens, num_q_heads, head_dim].
  *   k_cache, v_cache  device uint8 [num_blocks, 16, num_kv_heads, head_dim].
  *   k_scale, v_scale  finite, > 0 (else PKV_ERR_INVALID_ARG).
@@ -308,6 +311,21 @@ pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const v
                                      float softmax_scale, float k_scale, float v_scale, int causal,
                                      int num_splits, void* workspace, size_t workspace_bytes,
                                      int32_t* error_flag, int64_t num_blocks, void* stream);
+
+/*
+ * pkv_attention_varlen_e4m3_window - pkv_attention_varlen_e4m3 with a sliding
+ * window: the row at position p keeps keys j with p - window < j, on top of
+ * the causal limit, as pkv_attention_varlen_window.
+ *   window  >= 0 (0: no window; negative: PKV_ERR_INVALID_ARG).
+ * Everything else as pkv_attention_varlen_e4m3.
+ */
+pkv_status pkv_attention_varlen_e4m3_window(
+    const void* q, const void* k_cache, const void* v_cache, void* out, float* lse_out,
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* block_table,
+    int max_blocks_per_seq, int num_seqs, int64_t num_tokens, int max_query_len, int max_seq_len,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, float softmax_scale,
+    float k_scale, float v_scale, int causal, int window, int num_splits, void* workspace,
+    size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks, void* stream);
 
 /*
  * pkv_write_attention_varlen_e4m3 - pkv_write_e4m3 then
@@ -427,6 +445,23 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
                                  float softmax_scale, int prefix_splits, void* workspace,
                                  size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
                                  pkv_dtype dtype, void* stream);
+
+/*
+ * pkv_cascade_attention_e4m3 - pkv_cascade_attention over an E4M3 cache (the
+ * format of pkv_write_e4m3; k_scale, v_scale finite and > 0, else
+ * PKV_ERR_INVALID_ARG).  q and out are bf16.  The prefix pass runs on the
+ * split-KV kernel's CUDA-core tiles, the own-key pass on the decode kernel
+ * (tensor cores at head_dim 128); prefix_splits 0 takes the split count the
+ * CUDA-core pass is sized for.  Everything else as pkv_cascade_attention.
+ */
+pkv_status pkv_cascade_attention_e4m3(
+    const void* q, const void* k_cache, const void* v_cache, void* out, float* lse_out,
+    const int32_t* query_start_loc, const int32_t* suffix_lens, const int32_t* suffix_block_table,
+    int max_blocks_per_seq, const int32_t* shared_block_table, int shared_blocks, int num_seqs,
+    int64_t num_tokens, int max_query_len, int max_suffix_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, float softmax_scale, float k_scale, float v_scale,
+    int prefix_splits, void* workspace, size_t workspace_bytes, int32_t* error_flag,
+    int64_t num_blocks, void* stream);
 
 /*
  * pkv_build_metadata - the flat-batch metadata of one step, on the host.

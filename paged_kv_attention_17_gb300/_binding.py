@@ -25,6 +25,7 @@ FLAG_BAD_BLOCK, FLAG_BAD_SLOT, FLAG_BAD_LENGTHS, FLAG_TIMEOUT = 1, 2, 4, 8
 EXPORTS = ("pkv_write", "pkv_write_e4m3", "pkv_stage_inputs", "pkv_num_splits", "pkv_workspace_bytes",
            "pkv_attention_varlen", "pkv_write_attention_varlen", "pkv_attention_varlen_window",
            "pkv_attention_varlen_e4m3", "pkv_write_attention_varlen_e4m3",
+           "pkv_attention_varlen_e4m3_window", "pkv_cascade_attention_e4m3",
            "pkv_attention_varlen_noalloc", "pkv_cascade_splits", "pkv_cascade_workspace_bytes",
            "pkv_cascade_attention", "pkv_build_metadata", "pkv_status_string")
 
@@ -77,6 +78,10 @@ def lib() -> ctypes.CDLL:
                                                 i32, i32, i32, i32, i32, f32, f32, f32, i32, i32,
                                                 vp, sz, vp, i64, vp]
         L.pkv_attention_varlen_e4m3.restype = i32
+        L.pkv_attention_varlen_e4m3_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                                       i64, i32, i32, i32, i32, i32, i32, f32, f32,
+                                                       f32, i32, i32, i32, vp, sz, vp, i64, vp]
+        L.pkv_attention_varlen_e4m3_window.restype = i32
         L.pkv_attention_varlen_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64,
                                                    i32, i32, i32, i32, i32, i32, ctypes.c_float,
                                                    i32, i32, vp, i64, i32, vp]
@@ -89,6 +94,10 @@ def lib() -> ctypes.CDLL:
                                             i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp,
                                             i64, i32, vp]
         L.pkv_cascade_attention.restype = i32
+        L.pkv_cascade_attention_e4m3.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32,
+                                                 i64, i32, i32, i32, i32, i32, i32, f32, f32, f32,
+                                                 i32, vp, sz, vp, i64, vp]
+        L.pkv_cascade_attention_e4m3.restype = i32
         L.pkv_build_metadata.argtypes = [i32, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp, vp,
                                          vp, vp]
         L.pkv_build_metadata.restype = i32
@@ -293,10 +302,11 @@ def pkv_write_attention_varlen_e4m3(k_new, v_new, slot_mapping, q, k_cache, v_ca
 def pkv_attention_varlen_e4m3(q, k_cache, v_cache, out, query_start_loc, seq_lens, block_table,
                               max_query_len, max_seq_len, softmax_scale, k_scale, v_scale,
                               causal=True, num_splits=0, workspace=None, lse_out=None,
-                              error_flag=None, stream=None):
+                              error_flag=None, stream=None, window=0):
     """pkv_attention_varlen over uint8 caches of E4M3 codes (key code c stands
     for k_scale * value(c), value code c for v_scale * value(c)); q and out
-    are bf16.  Workspace handling as pkv_attention_varlen."""
+    are bf16.  Workspace handling as pkv_attention_varlen; ``window`` > 0
+    calls pkv_attention_varlen_e4m3_window."""
     if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
         raise TypeError("E4M3 caches are uint8 tensors of codes")
     if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
@@ -305,7 +315,17 @@ def pkv_attention_varlen_e4m3(q, k_cache, v_cache, out, query_start_loc, seq_len
     nb, bs, hkv, _ = k_cache.shape
     num_seqs = int(seq_lens.numel())
     splits, workspace, ws_bytes = _splits_and_workspace(
-        q, hkv, num_seqs, max_query_len, max_seq_len, num_splits, workspace)
+        q, hkv, num_seqs, max_query_len, split_span(max_seq_len, window), num_splits, workspace)
+    if window:
+        code = lib().pkv_attention_varlen_e4m3_window(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out),
+            _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]),
+            num_seqs, int(n_tok), int(max_query_len), int(max_seq_len), int(hq), int(hkv),
+            int(d), int(bs), float(softmax_scale), float(k_scale), float(v_scale),
+            1 if causal else 0, int(window), splits, _ptr(workspace), int(ws_bytes),
+            _ptr(error_flag), int(nb), _stream(stream))
+        _check("pkv_attention_varlen_e4m3_window", code)
+        return out
     code = lib().pkv_attention_varlen_e4m3(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
         _ptr(seq_lens), _ptr(block_table), int(block_table.shape[1]), num_seqs, int(n_tok),
@@ -353,12 +373,16 @@ def pkv_cascade_workspace_bytes(num_tokens, num_q_heads, head_dim, prefix_splits
 def pkv_cascade_attention(q, k_cache, v_cache, out, query_start_loc, suffix_lens,
                           suffix_block_table, shared_block_table, max_query_len, max_suffix_len,
                           softmax_scale, prefix_splits=0, workspace=None, lse_out=None,
-                          error_flag=None, stream=None):
+                          error_flag=None, stream=None, kv_scales=None):
     """Attention of a batch whose requests share the blocks of
     ``shared_block_table`` (int32 [shared_blocks]) as a prefix, each followed
     by its own ``suffix_lens[r]`` keys in ``suffix_block_table`` row r.
     ``workspace`` (uint8, >= pkv_cascade_workspace_bytes) is allocated here
-    if None."""
+    if None.  uint8 caches of E4M3 codes take ``kv_scales`` = (k_scale,
+    v_scale) and bf16 q / out (pkv_cascade_attention_e4m3)."""
+    e4m3 = k_cache.dtype == torch.uint8
+    if e4m3 and kv_scales is None:
+        raise ValueError("an E4M3 (uint8) cache needs kv_scales=(k_scale, v_scale)")
     n_tok, hq, d = q.shape
     nb, bs, hkv, _ = k_cache.shape
     num_seqs = int(suffix_lens.numel())
@@ -367,11 +391,24 @@ def pkv_cascade_attention(q, k_cache, v_cache, out, query_start_loc, suffix_lens
     if shared == 0:
         splits = 0
     elif splits == 0 and n_tok > 0:
-        splits = pkv_cascade_splits(n_tok, shared, hq, hkv, d, q.dtype, q.device.index)
+        # (an E4M3 prefix pass runs on the CUDA-core tiles: the fp32 rule)
+        splits = pkv_cascade_splits(n_tok, shared, hq, hkv, d,
+                                    torch.float32 if e4m3 else q.dtype, q.device.index)
     need = pkv_cascade_workspace_bytes(n_tok, hq, d, splits)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
+    if e4m3:
+        code = lib().pkv_cascade_attention_e4m3(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out),
+            _ptr(query_start_loc), _ptr(suffix_lens), _ptr(suffix_block_table),
+            int(suffix_block_table.shape[1]), _ptr(shared_block_table) if shared else None,
+            shared, num_seqs, int(n_tok), int(max_query_len), int(max_suffix_len), int(hq),
+            int(hkv), int(d), int(bs), float(softmax_scale), float(kv_scales[0]),
+            float(kv_scales[1]), splits, _ptr(workspace), int(ws_bytes), _ptr(error_flag),
+            int(nb), _stream(stream))
+        _check("pkv_cascade_attention_e4m3", code)
+        return out
     code = lib().pkv_cascade_attention(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse_out), _ptr(query_start_loc),
         _ptr(suffix_lens), _ptr(suffix_block_table), int(suffix_block_table.shape[1]),

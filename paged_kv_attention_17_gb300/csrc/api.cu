@@ -340,6 +340,32 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
 
 }  // namespace
 
+// The prefix split count: splits of whole 128-key tiles over the
+// tensor-core prefix pass's 256-row tiles (tc), or of >= 8 blocks over the
+// CUDA-core pass's 16-row tiles, filling 7/8 of the SMs.
+static int cascade_split_rule(int64_t num_tokens, int shared_blocks, int num_q_heads,
+                              int num_kv_heads, int head_dim, bool tc, int device) {
+  if (num_tokens < 1 || shared_blocks < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+      num_q_heads % num_kv_heads != 0)
+    return -1;
+  if (shared_blocks == 0) return 0;
+  const int sms = device_sms(device);
+  if (sms <= 0) return -1;
+  const int group = num_q_heads / num_kv_heads;
+  // tensor-core prefix pass: 256 (token, head) rows per CTA, splits of whole
+  // 128-key tiles; CUDA-core pass: 16-row tiles, splits of >= 8 blocks
+  (void)head_dim;
+  const int rows = tc ? 256 : kCascadeRows;
+  const int64_t tiles = static_cast<int64_t>(num_kv_heads) * ((group * num_tokens + rows - 1) / rows);
+  const int64_t target =
+      static_cast<int64_t>(sms) * 7 / 8;
+  int64_t s = target / tiles;
+  int64_t by_len = tc ? (shared_blocks + 7) / 8 : shared_blocks / kMinBlocksPerSplit;
+  if (s > by_len) s = by_len;
+  if (s > kMaxSplits - 1) s = kMaxSplits - 1;        // + the own-key partial <= kMaxSplits
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
 extern "C" {
 
 const char* pkv_status_string(pkv_status s) {
@@ -544,25 +570,13 @@ pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const v
 
 int pkv_cascade_splits(int64_t num_tokens, int shared_blocks, int num_q_heads, int num_kv_heads,
                        int head_dim, pkv_dtype dtype, int device) {
-  if (num_tokens < 1 || shared_blocks < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
-      num_q_heads % num_kv_heads != 0 || !valid_dtype(dtype))
+  if (!valid_dtype(dtype) || num_q_heads < 1 || num_kv_heads < 1 ||
+      num_q_heads % num_kv_heads != 0)
     return -1;
-  if (shared_blocks == 0) return 0;
-  const int sms = device_sms(device);
-  if (sms <= 0) return -1;
-  const int group = num_q_heads / num_kv_heads;
-  // tensor-core prefix pass: 256 (token, head) rows per CTA, splits of whole
-  // 128-key tiles; CUDA-core pass: 16-row tiles, splits of >= 8 blocks
-  const bool tc = prefill_packed_supported(head_dim, dtype == PKV_BF16, group);
-  const int rows = tc ? 256 : kCascadeRows;
-  const int64_t tiles = static_cast<int64_t>(num_kv_heads) * ((group * num_tokens + rows - 1) / rows);
-  const int64_t target =
-      static_cast<int64_t>(sms) * 7 / 8;
-  int64_t s = target / tiles;
-  int64_t by_len = tc ? (shared_blocks + 7) / 8 : shared_blocks / kMinBlocksPerSplit;
-  if (s > by_len) s = by_len;
-  if (s > kMaxSplits - 1) s = kMaxSplits - 1;        // + the own-key partial <= kMaxSplits
-  return static_cast<int>(s < 1 ? 1 : s);
+  return cascade_split_rule(num_tokens, shared_blocks, num_q_heads, num_kv_heads, head_dim,
+                            prefill_packed_supported(head_dim, dtype == PKV_BF16,
+                                                     num_q_heads / num_kv_heads),
+                            device);
 }
 
 size_t pkv_cascade_workspace_bytes(int64_t num_tokens, int num_q_heads, int head_dim,
@@ -572,17 +586,19 @@ size_t pkv_cascade_workspace_bytes(int64_t num_tokens, int num_q_heads, int head
   return align256(rows * head_dim * sizeof(float)) + align256(rows * sizeof(float));
 }
 
-pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void* v_cache,
-                                 void* out, float* lse_out, const int32_t* query_start_loc,
-                                 const int32_t* suffix_lens, const int32_t* suffix_block_table,
-                                 int max_blocks_per_seq, const int32_t* shared_block_table,
-                                 int shared_blocks, int num_seqs, int64_t num_tokens,
-                                 int max_query_len, int max_suffix_len, int num_q_heads,
-                                 int num_kv_heads, int head_dim, int block_size,
-                                 float softmax_scale, int prefix_splits, void* workspace,
-                                 size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
-                                 pkv_dtype dtype, void* stream) {
-  if (!valid_dtype(dtype) || num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
+// The cascade call over a cache of element type et (E4M3: k_scale folded
+// into the score scale, v_scale into the output).
+static pkv_status cascade_call(const void* q, const void* k_cache, const void* v_cache,
+                               void* out, float* lse_out, const int32_t* query_start_loc,
+                               const int32_t* suffix_lens, const int32_t* suffix_block_table,
+                               int max_blocks_per_seq, const int32_t* shared_block_table,
+                               int shared_blocks, int num_seqs, int64_t num_tokens,
+                               int max_query_len, int max_suffix_len, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               float softmax_scale, int prefix_splits, void* workspace,
+                               size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+                               ElemType et, float k_scale, float v_scale, void* stream) {
+  if (num_seqs < 0 || num_tokens < 0 || num_q_heads < 1 ||
       num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || shared_blocks < 0 ||
       prefix_splits < 0 || prefix_splits > kMaxSplits - 1 || num_blocks < 1 ||
       max_suffix_len < 0 || max_query_len < 0 || !std::isfinite(softmax_scale))
@@ -613,14 +629,15 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
       cudaGetLastError();
       return PKV_ERR_CUDA;
     }
-    S = pkv_cascade_splits(num_tokens, shared_blocks, num_q_heads, num_kv_heads, head_dim, dtype,
+    S = cascade_split_rule(num_tokens, shared_blocks, num_q_heads, num_kv_heads, head_dim,
+                           prefill_packed_supported(head_dim, et == ElemType::kBf16,
+                                                    num_q_heads / num_kv_heads),
                            dev);
     if (S < 1) return PKV_ERR_CUDA;
   }
   const size_t need = pkv_cascade_workspace_bytes(num_tokens, num_q_heads, head_dim, S);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
     return PKV_ERR_WORKSPACE;
-  const ElemType et = dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32;
   const size_t rows = static_cast<size_t>(S + 1) * num_tokens * num_q_heads;
 
   AttnArgs a;
@@ -634,8 +651,8 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
   a.hq = num_q_heads;
   a.hkv = num_kv_heads;
   a.group = num_q_heads / num_kv_heads;
-  a.scale_log2 = softmax_scale * kLog2e;
-  a.v_scale = 1.f;
+  a.scale_log2 = softmax_scale * kLog2e * (et == ElemType::kE4m3 ? k_scale : 1.f);
+  a.v_scale = et == ElemType::kE4m3 ? v_scale : 1.f;
   a.ws_o = static_cast<float*>(workspace);
   a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                       align256(rows * head_dim * sizeof(float)));
@@ -650,7 +667,7 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
   cudaError_t e = cudaSuccess;
   // tensor cores for the prefix pass (bf16, head_dim 128, a GQA group that
   // divides 128 rows, positive scale); the CUDA-core tiles otherwise
-  const bool tc = prefill_packed_supported(head_dim, dtype == PKV_BF16,
+  const bool tc = prefill_packed_supported(head_dim, et == ElemType::kBf16,
                                            num_q_heads / num_kv_heads) &&
                   softmax_scale > 0.f;
   // Two independent passes write disjoint partials; the merge reads both.
@@ -716,6 +733,57 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
     return PKV_ERR_CUDA;
   }
   return PKV_OK;
+}
+
+pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void* v_cache,
+                                 void* out, float* lse_out, const int32_t* query_start_loc,
+                                 const int32_t* suffix_lens, const int32_t* suffix_block_table,
+                                 int max_blocks_per_seq, const int32_t* shared_block_table,
+                                 int shared_blocks, int num_seqs, int64_t num_tokens,
+                                 int max_query_len, int max_suffix_len, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 float softmax_scale, int prefix_splits, void* workspace,
+                                 size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks,
+                                 pkv_dtype dtype, void* stream) {
+  if (!valid_dtype(dtype)) return PKV_ERR_INVALID_ARG;
+  return cascade_call(q, k_cache, v_cache, out, lse_out, query_start_loc, suffix_lens,
+                      suffix_block_table, max_blocks_per_seq, shared_block_table, shared_blocks,
+                      num_seqs, num_tokens, max_query_len, max_suffix_len, num_q_heads,
+                      num_kv_heads, head_dim, block_size, softmax_scale, prefix_splits, workspace,
+                      workspace_bytes, error_flag, num_blocks,
+                      dtype == PKV_BF16 ? ElemType::kBf16 : ElemType::kF32, 1.f, 1.f, stream);
+}
+
+pkv_status pkv_cascade_attention_e4m3(
+    const void* q, const void* k_cache, const void* v_cache, void* out, float* lse_out,
+    const int32_t* query_start_loc, const int32_t* suffix_lens, const int32_t* suffix_block_table,
+    int max_blocks_per_seq, const int32_t* shared_block_table, int shared_blocks, int num_seqs,
+    int64_t num_tokens, int max_query_len, int max_suffix_len, int num_q_heads, int num_kv_heads,
+    int head_dim, int block_size, float softmax_scale, float k_scale, float v_scale,
+    int prefix_splits, void* workspace, size_t workspace_bytes, int32_t* error_flag,
+    int64_t num_blocks, void* stream) {
+  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_INVALID_ARG;
+  return cascade_call(q, k_cache, v_cache, out, lse_out, query_start_loc, suffix_lens,
+                      suffix_block_table, max_blocks_per_seq, shared_block_table, shared_blocks,
+                      num_seqs, num_tokens, max_query_len, max_suffix_len, num_q_heads,
+                      num_kv_heads, head_dim, block_size, softmax_scale, prefix_splits, workspace,
+                      workspace_bytes, error_flag, num_blocks, ElemType::kE4m3, k_scale, v_scale,
+                      stream);
+}
+
+pkv_status pkv_attention_varlen_e4m3_window(
+    const void* q, const void* k_cache, const void* v_cache, void* out, float* lse_out,
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* block_table,
+    int max_blocks_per_seq, int num_seqs, int64_t num_tokens, int max_query_len, int max_seq_len,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, float softmax_scale,
+    float k_scale, float v_scale, int causal, int window, int num_splits, void* workspace,
+    size_t workspace_bytes, int32_t* error_flag, int64_t num_blocks, void* stream) {
+  if (!valid_scale(k_scale) || !valid_scale(v_scale) || window < 0) return PKV_ERR_INVALID_ARG;
+  return attention(q, k_cache, v_cache, out, lse_out, query_start_loc, seq_lens, block_table,
+                   max_blocks_per_seq, num_seqs, num_tokens, max_query_len, max_seq_len,
+                   num_q_heads, num_kv_heads, head_dim, block_size, softmax_scale, k_scale,
+                   v_scale, causal, window, num_splits, workspace, workspace_bytes, error_flag,
+                   num_blocks, ElemType::kE4m3, stream);
 }
 
 }  // extern "C"

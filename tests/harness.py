@@ -93,7 +93,7 @@ def run_step(d, num_splits=0, write=True, with_lse=True, causal=None, workspace=
             d["q"], d["k_cache"], d["v_cache"], out, d["qsl"], d["seq_lens"], d["block_table"],
             meta["max_query_len"], meta["max_seq_len"], w.softmax_scale, w.k_scale, w.v_scale,
             causal=w.causal if causal is None else causal, num_splits=num_splits,
-            workspace=workspace, lse_out=lse, error_flag=flag)
+            workspace=workspace, lse_out=lse, error_flag=flag, window=getattr(w, "window", 0))
         return out, lse, flag
     pkv.pkv_attention_varlen(d["q"], d["k_cache"], d["v_cache"], out, d["qsl"], d["seq_lens"],
                              d["block_table"], meta["max_query_len"], meta["max_seq_len"],

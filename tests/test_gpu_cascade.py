@@ -128,3 +128,47 @@ def test_cascade_64x4k_sampled_rows():
     assert int(flag.item()) == 0
     toks = [0, 1, 17, 31, 32, 62, 63]
     _check(out, lse, w, "bf16", toks)
+
+
+def run_cascade_e4m3(d, prefix_splits=0):
+    w = d["w"]
+    flag = torch.zeros(1, dtype=torch.int32, device=d["q"].device)
+    pkv.pkv_write_e4m3(d["k_new"], d["v_new"], d["slot_mapping"], d["k_cache"], d["v_cache"],
+                       w.k_scale, w.v_scale, error_flag=flag)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=d["q"].device)
+    pkv.pkv_cascade_attention(d["q"], d["k_cache"], d["v_cache"], out, d["qsl"],
+                              d["suffix_lens"], d["suffix_table"], d["shared_table"],
+                              d["meta"]["max_query_len"], d["max_suffix_len"], w.softmax_scale,
+                              prefix_splits=prefix_splits, lse_out=lse, error_flag=flag,
+                              kv_scales=(w.k_scale, w.v_scale))
+    return out, lse, flag
+
+
+@pytest.mark.parametrize("prefix_splits", [1, 3, 0])
+@pytest.mark.parametrize("shared_blocks", [1, 5, 40])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 1, 64), (12, 4, 128)])
+def test_cascade_over_e4m3_cache(prefix_splits, shared_blocks, hq, hkv, d):
+    # pkv_cascade_attention_e4m3: the prefix pass on the CUDA-core tiles, the
+    # own-key pass on the decode kernel, against plain attention over the
+    # dequantised full tables
+    rng = np.random.Generator(np.random.PCG64(shared_blocks * 17 + hq))
+    shape = [(int(c), 1) for c in rng.integers(0, 200, size=12)] + [(0, 1), (15, 2), (16, 1)]
+    w = workloads.build_cascade("casc_e4m3", "bf16", hq, hkv, d, shared_blocks, shape, rng=rng,
+                                kv_dtype="e4m3", k_scale=0.6, v_scale=0.35)
+    dev = cascade_inputs(w)
+    out, lse, flag = run_cascade_e4m3(dev, prefix_splits)
+    assert int(flag.item()) == 0
+    _check(out, lse, w, "bf16")
+
+
+def test_cascade_e4m3_rejects_bad_scales():
+    w = workloads.build_cascade("casc_e4m3_bad", "bf16", 8, 2, 128, 2, [(3, 1)], seed=1,
+                                kv_dtype="e4m3", k_scale=0.5, v_scale=0.5)
+    dev = cascade_inputs(w)
+    out = torch.empty_like(dev["q"])
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_cascade_attention(dev["q"], dev["k_cache"], dev["v_cache"], out, dev["qsl"],
+                                  dev["suffix_lens"], dev["suffix_table"], dev["shared_table"],
+                                  dev["meta"]["max_query_len"], dev["max_suffix_len"],
+                                  w.softmax_scale, kv_scales=(0.0, 0.5))

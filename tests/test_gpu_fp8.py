@@ -3,8 +3,11 @@
 pkv_write_e4m3 must store exactly the oracle's codes (``oracle.fp8.quantize``:
 value / scale in fp32, nearest code, ties to even, saturating at 448).
 pkv_attention_varlen_e4m3 is held to the bf16 bar (max |err| <= 1e-2, mean
-|err| <= 1e-3): the codes widen exactly to fp32, so the only differences from
-the oracle are those of the bf16 path (fp32 accumulation, bf16 output).
+|err| <= 1e-3): the codes widen exactly (to f16 on the tensor-core path, to
+fp32 on the CUDA-core tiles), so the only differences from the oracle are
+those of the bf16 path (fp32 accumulation, P rounded to 16 bits, bf16 output).
+The sliding-window and shared-prefix forms over an E4M3 cache are held to the
+same bar.
 """
 
 import numpy as np
@@ -190,3 +193,49 @@ def test_matches_the_bf16_path_on_the_dequantised_cache():
     assert rows
     diff = (out8.float() - out16.float())[rows].abs().max().item()
     assert diff <= 2.0 ** -8, diff
+
+
+@pytest.mark.parametrize("window", [1, 16, 100, 1000])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_sliding_window_over_e4m3_cache(window, splits):
+    # pkv_attention_varlen_e4m3_window: decodes, short tails and prefill
+    # chunks, each row keeping only its `window` most recent keys
+    rng = np.random.Generator(np.random.PCG64(window * 13 + splits))
+    ctx = rng.integers(1, 1500, size=8)
+    shape = [(int(c), 1) for c in ctx] + [(200, 3), (0, 40), (900, 130), (16, 1)]
+    w = workloads.build("fp8_window", "bf16", 32, 8, 128, shape, rng=rng, kv_dtype="e4m3",
+                        k_scale=0.6, v_scale=0.4, window=window)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev, num_splits=splits)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    if window == 1:
+        # one visible key: each output is that key's dequantised V, a value
+        # bf16 cannot hold, so the bound is bf16's own rounding of it (the
+        # absolute bounds assume averaged outputs; these reach |o| ~ 5)
+        got = out.float().cpu().double().numpy()
+        assert np.all(np.abs(got - o_ref) <= 2.0 ** -8 * np.abs(o_ref) + 1e-30)
+    else:
+        _check(out, o_ref)
+    _check_lse(lse, lse_ref)
+
+
+def test_window_zero_over_e4m3_is_the_plain_call():
+    w = workloads.build("fp8_w0", "bf16", 16, 4, 128, [(300, 1), (40, 5), (1000, 1)], seed=3,
+                        kv_dtype="e4m3", k_scale=0.5, v_scale=0.5)
+    dev = device_inputs(w)
+    out0, lse0, flag0 = run_step(dev, num_splits=2)
+    m = dev["meta"]
+    out1 = torch.empty_like(out0)
+    pkv.pkv_attention_varlen_e4m3(dev["q"], dev["k_cache"], dev["v_cache"], out1, dev["qsl"],
+                                  dev["seq_lens"], dev["block_table"], m["max_query_len"],
+                                  m["max_seq_len"], w.softmax_scale, w.k_scale, w.v_scale,
+                                  num_splits=2, window=0)
+    huge = torch.empty_like(out0)
+    pkv.pkv_attention_varlen_e4m3(dev["q"], dev["k_cache"], dev["v_cache"], huge, dev["qsl"],
+                                  dev["seq_lens"], dev["block_table"], m["max_query_len"],
+                                  m["max_seq_len"], w.softmax_scale, w.k_scale, w.v_scale,
+                                  num_splits=2, window=1 << 20)
+    torch.cuda.synchronize()
+    assert int(flag0.item()) == 0
+    assert torch.equal(out0, out1) and torch.equal(out0, huge)

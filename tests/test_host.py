@@ -142,6 +142,28 @@ def test_stage_inputs_host_validation(pkv):
     assert L.pkv_stage_inputs(vp(16), vp(40), 32, None) == 1
 
 
+def test_e4m3_window_and_cascade_host_validation(pkv):
+    # the E4M3 sliding-window and shared-prefix entry points reject bad scales
+    # and a negative window before touching any pointer or launching
+    L = pkv.lib()
+    vp = ctypes.c_void_p
+    win = lambda ks, vs, window: L.pkv_attention_varlen_e4m3_window(
+        None, None, None, None, None, None, None, None, 4, 1, 1, 1, 64, 8, 2, 128, 16,
+        0.1, ks, vs, 1, window, 0, None, 0, None, 4, None)
+    assert win(0.0, 1.0, 0) == 1
+    assert win(1.0, float("inf"), 0) == 1
+    assert win(1.0, 1.0, -1) == 1
+    casc = lambda ks, vs: L.pkv_cascade_attention_e4m3(
+        None, None, None, None, None, None, None, None, 4, None, 0, 1, 1, 1, 64, 8, 2, 128, 16,
+        0.1, ks, vs, 0, None, 0, None, 4, None)
+    assert casc(-1.0, 1.0) == 1
+    assert casc(1.0, float("nan")) == 1
+    # valid scales: an empty batch is a no-op
+    assert L.pkv_cascade_attention_e4m3(None, vp(16), vp(16), None, None, None, None, None, 4,
+                                        None, 0, 0, 0, 1, 64, 8, 2, 128, 16, 0.1, 1.0, 1.0, 0,
+                                        None, 0, None, 4, None) == 0
+
+
 def test_write_host_validation(pkv):
     L = pkv.lib()
     vp = ctypes.c_void_p

@@ -157,11 +157,14 @@ def build(name: str, dtype: str, hq: int, hkv: int, d: int,
 
 def build_cascade(name: str, dtype: str, hq: int, hkv: int, d: int, shared_blocks: int,
                   shape: list[tuple[int, int]], seed: int = 0, spare_blocks: int = 3,
-                  rng: np.random.Generator | None = None, replicas: int = 1) -> Workload:
+                  rng: np.random.Generator | None = None, replicas: int = 1,
+                  kv_dtype: str | None = None, k_scale: float = 1.0,
+                  v_scale: float = 1.0) -> Workload:
     """Requests that share a prefix of ``shared_blocks`` blocks: each (c, s)
     pair is a request with c cached keys of its own after the prefix and s new
     tokens; its table is the shared blocks followed by its own.  Replicas
-    repeat the batch on disjoint blocks (a prefix of their own each)."""
+    repeat the batch on disjoint blocks (a prefix of their own each).
+    kv_dtype "e4m3": the pools hold E4M3 codes (as ``build``)."""
     rng = rng if rng is not None else np.random.Generator(np.random.PCG64(seed))
     own = [_blocks_needed(c + s, BLOCK_SIZE) for c, s in shape]
     per_rep = shared_blocks + sum(own)
@@ -179,14 +182,18 @@ def build_cascade(name: str, dtype: str, hq: int, hkv: int, d: int, shared_block
         reps.append(reqs)
     n = sum(s for _, s in shape)
     pool_shape = (num_blocks, BLOCK_SIZE, hkv, d)
-    k_pool, v_pool = _values(rng, pool_shape, dtype), _values(rng, pool_shape, dtype)
+    if kv_dtype == "e4m3":
+        k_pool, v_pool = _codes(rng, pool_shape), _codes(rng, pool_shape)
+    else:
+        k_pool, v_pool = _values(rng, pool_shape, dtype), _values(rng, pool_shape, dtype)
     q = _values(rng, (n, hq, d), dtype)
     k_new = _values(rng, (n, hkv, d), dtype)
     v_new = _values(rng, (n, hkv, d), dtype)
     return Workload(name=name, dtype=dtype, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                     num_blocks=num_blocks, requests=reps[0], q=q, k_new=k_new, v_new=v_new,
                     k_pool=k_pool, v_pool=v_pool, softmax_scale=float(1.0 / np.sqrt(d)),
-                    replicas=reps, shared_blocks=shared_blocks)
+                    replicas=reps, shared_blocks=shared_blocks, kv_dtype=kv_dtype,
+                    k_scale=float(k_scale), v_scale=float(v_scale))
 
 
 def cascade_64x4k(seed: int = 0, replicas: int = 1) -> Workload:
