@@ -1647,9 +1647,23 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   for (int u = 0; u < kMaxPer; ++u) {
     const int sp = warp + 4 * u;
     if (sp < S) {
+      // one 16-byte (D 128) or 8-byte (D 64) load per partial: a row is D
+      // floats, so the lane's slice is aligned
       const float* src = a.ws_o + prow(sp) * D + lane * kDPL;
+      if constexpr (kDPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        part[u][0] = v.x;
+        part[u][1] = v.y;
+        part[u][2] = v.z;
+        part[u][3] = v.w;
+      } else if constexpr (kDPL == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        part[u][0] = v.x;
+        part[u][1] = v.y;
+      } else {
 #pragma unroll
-      for (int e = 0; e < kDPL; ++e) part[u][e] = src[e];
+        for (int e = 0; e < kDPL; ++e) part[u][e] = src[e];
+      }
     }
   }
   if (CASCADE) {
