@@ -371,6 +371,20 @@ __device__ __forceinline__ int request_by_length_rank(const AttnArgs& a, int ran
   return r;
 }
 
+// A lane's kDPL consecutive floats of a partial row in one vector store (the
+// row is D floats and the lane's slice starts at a multiple of kDPL floats).
+template <int kDPL>
+__device__ __forceinline__ void store_partial(float* dst, const float (&o)[kDPL]) {
+  if constexpr (kDPL == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+  } else if constexpr (kDPL == 2) {
+    *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kDPL; ++e) dst[e] = o[e];
+  }
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -1587,13 +1601,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
       // slot of a request)
       const int64_t w = part_row(a, a.cascade == 2 ? a.cascade_slot : s, r, q0 + i, i, h);
 #pragma unroll
-      for (int e = 0; e < C::kDPL; ++e) a.ws_o[w * D + lane * C::kDPL + e] = o[e] * inv;
+      for (int e = 0; e < C::kDPL; ++e) o[e] *= inv;
+      store_partial<C::kDPL>(a.ws_o + w * D + lane * C::kDPL, o);
       if (lane == 0) a.ws_lse[w] = lse2;
     } else {
       const int64_t t = q0 + i;
+      const int64_t base = (t * a.hq + h) * D + lane * C::kDPL;
+      if constexpr (sizeof(QT) == 2 && C::kDPL == 4) {
+        // four bf16 outputs of the lane in one 8-byte store
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + base) =
+            make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
+      } else {
 #pragma unroll
-      for (int e = 0; e < C::kDPL; ++e)
-        store_elem<QT>(a.out, (t * a.hq + h) * D + lane * C::kDPL + e, o[e] * inv);
+        for (int e = 0; e < C::kDPL; ++e) store_elem<QT>(a.out, base + e, o[e] * inv);
+      }
       if (a.lse_out != nullptr && lane == 0) a.lse_out[t * a.hq + h] = lse2 * kLn2;
     }
   }
