@@ -1585,9 +1585,19 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
         const float f = ex2(mw[w * R + rho] - M);
         lsum = fmaf(f, lw[w * R + rho], lsum);
         if constexpr (kMma) lnorm = fmaf(f, lrw[w * R + rho], lnorm);
+        // the lane's slice in one shared-memory load (aw starts 3 x W x R
+        // floats in, a multiple of 16 bytes; rows are D floats)
+        const float* src = aw + (w * R + rho) * D + lane * C::kDPL;
+        if constexpr (C::kDPL == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          o[0] = fmaf(f, v.x, o[0]);
+          o[1] = fmaf(f, v.y, o[1]);
+          o[2] = fmaf(f, v.z, o[2]);
+          o[3] = fmaf(f, v.w, o[3]);
+        } else {
 #pragma unroll
-        for (int e = 0; e < C::kDPL; ++e)
-          o[e] = fmaf(f, aw[(w * R + rho) * D + lane * C::kDPL + e], o[e]);
+          for (int e = 0; e < C::kDPL; ++e) o[e] = fmaf(f, src[e], o[e]);
+        }
       }
     }
     if constexpr (!kMma) lnorm = lsum;
