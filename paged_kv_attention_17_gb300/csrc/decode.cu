@@ -175,6 +175,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
       : "r"(two_codes));
   return h2;
 }
+// four E4M3 codes (a word, element 0 in the low byte) -> f16x2 of codes 0, 1
+// and of codes 2, 3: the word's 16-bit halves feed the conversions directly
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo,
+                                                  uint32_t& hi) {
+  asm("{\n\t.reg .b16 c0, c1;\n\tmov.b32 {c0, c1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c0;\n\tcvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
+}
 // (lo, hi) -> bf16x2 / f16x2, round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -1093,8 +1102,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
               return (t & 3) == 0 ? c4.x : (t & 3) == 1 ? c4.y : (t & 3) == 2 ? c4.z : c4.w;
             };
             const uint32_t w0 = word(kc[0][t >> 2]), w1 = word(kc[1][t >> 2]);
-            mma_s(t, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
-                  e4m3x2_to_f16x2(w1 >> 16));
+            uint32_t a0, a1, a2, a3;
+            e4m3x4_to_f16x2x2(w0, a0, a2);
+            e4m3x4_to_f16x2x2(w1, a1, a3);
+            mma_s(t, a0, a1, a2, a3);
           }
         } else {
           // matrix mi: keys 8 (mi & 1) .. +7, 16-byte chunk 2 (t % 4) + (mi >> 1)
@@ -1220,10 +1231,13 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
             const uint32_t a0 = word(vc[0]), a1 = word(vc[1]), b0 = word(vc[2]), b1 = word(vc[3]);
             const uint32_t alo = prmt(a0, a1, 0x5140), ahi = prmt(a0, a1, 0x7362);
             const uint32_t blo = prmt(b0, b1, 0x5140), bhi = prmt(b0, b1, 0x7362);
-            mma_o(2 * w, e4m3x2_to_f16x2(alo), e4m3x2_to_f16x2(alo >> 16), e4m3x2_to_f16x2(blo),
-                  e4m3x2_to_f16x2(blo >> 16));
-            mma_o(2 * w + 1, e4m3x2_to_f16x2(ahi), e4m3x2_to_f16x2(ahi >> 16),
-                  e4m3x2_to_f16x2(bhi), e4m3x2_to_f16x2(bhi >> 16));
+            uint32_t x0, x1, y0, y1;
+            e4m3x4_to_f16x2x2(alo, x0, x1);
+            e4m3x4_to_f16x2x2(blo, y0, y1);
+            mma_o(2 * w, x0, x1, y0, y1);
+            e4m3x4_to_f16x2x2(ahi, x0, x1);
+            e4m3x4_to_f16x2x2(bhi, y0, y1);
+            mma_o(2 * w + 1, x0, x1, y0, y1);
           }
         } else {
           // matrix mi (.trans): keys 8 (mi >> 1) .. +7, chunk 2 (mt % 4) + (mi & 1)
