@@ -28,7 +28,7 @@ int decode_ctas_per_sm(ElemType et, int head_dim);
 bool prefill_supported(int head_dim, bool bf16, int group);
 bool prefill_packed_supported(int head_dim, bool bf16, int group);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t stream);
+                           const CUtensorMap& vmap, int head_dim, cudaStream_t stream);
 }  // namespace pkv
 
 using namespace pkv;
@@ -329,7 +329,7 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     // their own dependency waits: its inputs are complete at launch
     AttnArgs p = a;
     p.defer_wait = 1;
-    e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
+    e = launch_prefill(p, qmap, kmap_sw, vmap_sw, head_dim, st);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -715,7 +715,7 @@ static pkv_status cascade_call(const void* q, const void* k_cache, const void* v
           !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
           !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
         return PKV_ERR_CUDA;
-      e = launch_prefill(p, qmap, kmap_sw, vmap_sw, st);
+      e = launch_prefill(p, qmap, kmap_sw, vmap_sw, head_dim, st);
     } else {
       e = launch_decode(p, kmap, vmap, et, head_dim, /*pdl=*/true, st);
     }

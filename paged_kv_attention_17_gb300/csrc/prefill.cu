@@ -225,10 +225,17 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 }  // namespace
 
+// D: head_dim, 128 or 64.  The layouts are those of D = 128 (two 64-column
+// halves of Q, K and V, O_t in 128 TMEM columns); D = 64 fills one half of
+// each and the first 64 columns of O_t.
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  constexpr int kH = D / 64;                             // 64-column halves of a row
+  constexpr int kOC = D / 32;                            // 32-column chunks of an O row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tk >= a.num_tokens) continue;
         const int64_t w = (static_cast<int64_t>(split) * a.num_tokens + tk) * a.hq +
                           g * a.group + rho % a.group;
-        for (int c = 0; c < 128; ++c) a.ws_o[w * 128 + c] = 0.f;
+        for (int c = 0; c < D; ++c) a.ws_o[w * D + c] = 0.f;
         a.ws_lse[w] = -INFINITY;
       }
       if (a.defer_wait) pdl_wait_primary();
@@ -393,10 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
-      mbar_arrive_expect_tx(bar_q, 4 * kHalf);
+      mbar_arrive_expect_tx(bar_q, 2 * kH * kHalf);
       const uint64_t pol_q = l2_policy_evict_first();
       for (int t = 0; t < 2; ++t)
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < kH; ++hh) {
           if (packed)   // 128 rows = tok_per_tile tokens x the GQA group of KV head g
             tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64, g * a.group,
                         (2 * tile + t) * tok_per_tile, pol_q);
@@ -431,12 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
-        if (lane == 0) mbar_arrive_expect_tx(fullb, 2 * kHalf);
+        if (lane == 0) mbar_arrive_expect_tx(fullb, kH * kHalf);
         __syncwarp();
         if (lane < kKeys / kBlock) {
           uint8_t* dst = kst + part * 2 * kHalf;
           const CUtensorMap* map = part == 0 ? &kmap : &vmap;
-          for (int hh = 0; hh < 2; ++hh)
+          for (int hh = 0; hh < kH; ++hh)
             tma_load_3d(dst + hh * kHalf + lane * (kBlock * 128), map, fullb, hh * 64, g, slot,
                         pol_kv);
         }
@@ -461,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group 1's P.V of tile k and the reverse.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(kQRows, kKeys, 0);
-      const uint32_t id_o = idesc_bf16(kQRows, 128, 1);
+      const uint32_t id_o = idesc_bf16(kQRows, D, 1);
       // Descriptors are built once; a step only adds its byte offset >> 4 to
       // the start-address field (every address stays below 256 KB, so the
       // 14-bit field never carries).
@@ -469,11 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq = sdesc(smem_u32(smem + kOffQ), 16, 1024);
       const uint64_t dk = sdesc(kv_addr0, 16, 1024);
       const uint64_t dv = sdesc(kv_addr0 + 2 * kHalf, kHalf, 1024);
-      auto issue_s = [&](int t, int kt) {                // S_t = Q_t K^T, D = 128 in 8 steps
+      auto issue_s = [&](int t, int kt) {                // S_t = Q_t K^T, D / 16 steps
         const uint64_t a0 = dq + static_cast<uint64_t>((t * 2 * kHalf) >> 4);
         const uint64_t b0 = dk + static_cast<uint64_t>(((kt % kStages) * kStageBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < D / 16; ++k) {
           const uint64_t off = static_cast<uint64_t>(((k >> 2) * kHalf + (k & 3) * 32) >> 4);
           umma(tbase + t * kKeys, a0 + off, b0 + off, id_s, k > 0);
         }
@@ -621,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < kOC; ++c) {
             float v[32];
             tmem_ld32(t_o + c * 32, v);
 #pragma unroll
@@ -643,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t == 0 && kt == ntk - 1 && key0 + row >= kv_len) {
         uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kHalf + row * 128;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
+        for (int hh = 0; hh < kH; ++hh)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(vrow + hh * kHalf + c * 16) = make_uint4(0, 0, 0, 0);
@@ -667,11 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t w = (static_cast<int64_t>(split) * a.num_tokens + tk) * a.hq +
                           g * a.group + rho % a.group;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kOC; ++c) {
           float v[32];
           tmem_ld32(t_o + c * 32, v);
           if (tk < a.num_tokens) {
-            float4* dst = reinterpret_cast<float4*>(a.ws_o + w * 128 + c * 32);
+            float4* dst = reinterpret_cast<float4*>(a.ws_o + w * D + c * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               dst[q] = make_float4(v[4 * q] * inv, v[4 * q + 1] * inv, v[4 * q + 2] * inv,
@@ -682,9 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
       const bool store = i_r < n;
       __nv_bfloat16* orow =
-          static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(q0 + i_r) * a.hq + h) * 128;
+          static_cast<__nv_bfloat16*>(a.out) + (static_cast<int64_t>(q0 + i_r) * a.hq + h) * D;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kOC; ++c) {
         float v[32];
         tmem_ld32(t_o + c * 32, v);
         if (store) {
@@ -720,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The tensor-core path pairs two query heads of one KV head per CTA, so the
 // GQA group size must be even; other shapes run long rows on CUDA cores.
 bool prefill_supported(int head_dim, bool bf16, int group) {
-  return bf16 && head_dim == 128 && group % 2 == 0;
+  return bf16 && (head_dim == 128 || head_dim == 64) && group % 2 == 0;
 }
 
 // Shared-prefix mode needs whole GQA groups in a 128-row tile.
@@ -729,14 +736,18 @@ bool prefill_packed_supported(int head_dim, bool bf16, int group) {
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, cudaStream_t stream) {
+                           const CUtensorMap& vmap, int head_dim, cudaStream_t stream) {
+  if (head_dim != 128 && head_dim != 64) return cudaErrorInvalidValue;
   static unsigned done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !((done >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemAlloc);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) done |= 1u << dev;
   }
@@ -760,7 +771,8 @@ cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, qmap, kmap, vmap, a);
+  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, prefill_kernel<128>, qmap, kmap, vmap, a)
+                         : cudaLaunchKernelEx(&cfg, prefill_kernel<64>, qmap, kmap, vmap, a);
 }
 
 }  // namespace pkv

@@ -186,6 +186,34 @@ def test_longest_first_dispatch_unsplit(num_seqs):
     _check_lse(lse, lse_ref)
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 4), (16, 2), (32, 4), (64, 8)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tensor_core_prefill_head_dim_64(hq, hkv, causal):
+    # head_dim 64 with an even GQA group: long requests take the tensor-core
+    # prefill (one 64-column half of each tile), beside decode rows and tails
+    shape = [(0, 300), (500, 129), (40, 2), (1000, 1), (0, 1024), (77, 5)]
+    w = workloads.build("d64_prefill", "bf16", hq, hkv, 64, shape, seed=hq + hkv, causal=causal)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    _check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("window", [0, 200])
+def test_tensor_core_prefill_head_dim_64_long_chunk(window):
+    # a 2048-token chunk on a 1000-token prefix at GQA 32/8, every row
+    w = workloads.build("d64_chunk", "bf16", 32, 8, 64, [(1000, 2048), (300, 1)], seed=64,
+                        window=window)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    _check_lse(lse, lse_ref)
+
+
 def test_split_heuristic_rule():
     # one wave of split CTAs over 7/8 of the decode CTA slots (two per SM for
     # the bf16 tensor-core build), at least 8 blocks per split, split off once
