@@ -196,7 +196,9 @@ size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_
  * computed as an online softmax over key tiles ("Never materialise the TxT
  * matrix"); requests with n <= PKV_DECODE_MAX_QLEN take the split-KV decode
  * kernel (partials merged by a log-sum-exp combine kernel when num_splits >
- * 1), longer ones the tiled prefill kernel.
+ * 1), longer ones the tiled prefill kernel: on tensor cores for bf16 at
+ * head_dim 64 or 128 with an even GQA group, else on the decode kernel's
+ * CUDA-core 16-row tiles.
  *
  *   q, out            device [num_tokens, num_q_heads, head_dim], dtype.
  *   lse_out           device fp32 [num_tokens, num_q_heads] or NULL: natural-log
@@ -392,15 +394,15 @@ pkv_status pkv_attention_varlen_noalloc(const void* q, const void* k_cache, cons
  * row; the prefix is read from HBM once for all requests, split
  * prefix_splits ways over the key axis), each request over its own keys,
  * and a log-sum-exp merge of the prefix_splits + 1 partials per row.  The
- * prefix pass runs on the tensor cores for bf16, head_dim 128 and an even GQA
+ * prefix pass runs on the tensor cores for bf16, head_dim 64 or 128 and an even GQA
  * group that divides 128 (each 128-row tile holds 128 / group tokens with
  * their whole group, so one K/V tile feeds every head of the KV head) and a
  * positive softmax_scale, else on the split-KV kernel's CUDA-core tiles; the
- * own-key pass and the merge always run on CUDA cores.
+ * own-key pass runs on the decode kernel and the merge on CUDA cores.
  */
 
 /* pkv_cascade_splits - prefix splits for num_tokens rows over shared_blocks
- * blocks.  Tensor-core prefix pass (bf16, head_dim 128, even GQA group
+ * blocks.  Tensor-core prefix pass (bf16, head_dim 64 or 128, even GQA group
  * dividing 128): U = num_kv_heads x ceil(group x num_tokens / 256) row tiles,
  * T = floor(7 x SMs / 8), min(max(1, floor(T / U)), ceil(shared_blocks / 8),
  * 63) - each split at least one 128-key tile.  CUDA-core pass (otherwise):
