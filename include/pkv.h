@@ -197,7 +197,8 @@ size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_
  * matrix"); requests with n <= PKV_DECODE_MAX_QLEN take the split-KV decode
  * kernel (partials merged by a log-sum-exp combine kernel when num_splits >
  * 1), longer ones the tiled prefill kernel: on tensor cores for bf16 at
- * head_dim 64 or 128 with an even GQA group, else on the decode kernel's
+ * head_dim 64 or 128 (two query heads of a KV head per CTA, or with an odd
+ * GQA group two query tiles of one head), else on the decode kernel's
  * CUDA-core 16-row tiles.
  *
  *   q, out            device [num_tokens, num_q_heads, head_dim], dtype.

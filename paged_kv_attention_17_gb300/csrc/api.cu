@@ -329,6 +329,7 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     // their own dependency waits: its inputs are complete at launch
     AttnArgs p = a;
     p.defer_wait = 1;
+    p.pair_tiles = a.group % 2 != 0 ? 1 : 0;
     e = launch_prefill(p, qmap, kmap_sw, vmap_sw, head_dim, st);
   }
   if (e != cudaSuccess) {

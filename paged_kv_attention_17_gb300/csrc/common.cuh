@@ -70,6 +70,9 @@ struct AttnArgs {
   // Prefill launched behind the same call's decode kernel: its dependency
   // wait moves from the start to each CTA's exit (see prefill.cu).
   int defer_wait;
+  // Prefill: an odd GQA group pairs two query tiles of one head per CTA
+  // instead of two query heads of one tile (see prefill.cu).
+  int pair_tiles;
   // Unsplit decode launch of 2..256 requests: blockIdx.z is read as a rank of
   // the requests by decreasing seq_len (longest first; see decode.cu).
   int lpt;

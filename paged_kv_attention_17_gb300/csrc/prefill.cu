@@ -258,9 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // kv head and prefix split) varying fastest, so every head pair's heaviest
   // query tiles are dispatched in the first waves (longest work first) and
   // the CTAs reading the same K/V tiles run side by side.
-  const int ys = packed ? a.hkv * a.num_splits : a.hq / 2;
+  // Tile-pair mode (an odd GQA group, where two query heads of one KV head
+  // cannot pair up): both softmax warpgroups take query head h0, over the
+  // consecutive query tiles 2u and 2u + 1 of one request.
+  const bool pairs = !packed && a.pair_tiles != 0;
+  const int ys = packed ? a.hkv * a.num_splits : (pairs ? a.hq : a.hq / 2);
   const int yidx = static_cast<int>(blockIdx.x % static_cast<unsigned>(ys));
-  const int h0 = packed ? 0 : 2 * yidx;                  // query heads h0, h0 + 1 (same KV head)
+  // query heads h0, h0 + 1 (same KV head), or h0 alone in tile-pair mode
+  const int h0 = packed ? 0 : (pairs ? yidx : 2 * yidx);
   const int tglob = static_cast<int>(blockIdx.x / static_cast<unsigned>(ys));
 
   // defer_wait: launched behind the decode kernel of the same call, whose
@@ -286,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r < a.num_seqs) {
         const int n = __ldg(a.qsl + r + 1) - __ldg(a.qsl + r);
         nt = n > kDecodeMaxQ ? (n + kQRows - 1) / kQRows : 0;
+        if (pairs) nt = (nt + 1) / 2;                    // units: pairs of tiles
       }
       int inc = nt;
 #pragma unroll
@@ -328,8 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = packed ? yidx % a.hkv : h0 / a.group;
   const int split = packed ? yidx / a.hkv : 0;
   const int tok_per_tile = kQRows / a.group;             // packed: tokens per 128-row tile
-  const int i0 = tile * kQRows;
-  const int i_hi = min(i0 + kQRows, n) - 1;              // last real row of the tile
+  // first row of the unit (its first tile), and the unit's last real row
+  const int i0 = (pairs ? 2 * tile : tile) * kQRows;
+  const int i_hi = min(i0 + (pairs ? 2 : 1) * kQRows, n) - 1;
   const int kv_len = a.causal ? (L - n + i_hi + 1) : L;
   const int nblk_ctx = (kv_len + kBlock - 1) / kBlock;
   if ((L + kBlock - 1) / kBlock > a.max_blocks_per_seq) {
@@ -408,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64, g * a.group,
                         (2 * tile + t) * tok_per_tile, pol_q);
           else
-            tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64, h0 + t,
-                        q0 + i0, pol_q);
+            tma_load_3d(smem + kOffQ + (2 * t + hh) * kHalf, &qmap, bar_q, hh * 64,
+                        pairs ? h0 : h0 + t, q0 + i0 + (pairs ? t * kQRows : 0), pol_q);
         }
     }
     int kt = 0;
@@ -535,14 +542,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= softmax / epilogue: thread = query row of tile t =================
     const int t = warp >> 2;                             // 0: warps 0-3, 1: warps 4-7
     const int row = threadIdx.x - t * kQRows;            // 0..127 == TMEM lane
-    const int h = h0 + t;
-    const int i_r = i0 + row;
+    const int h = pairs ? h0 : h0 + t;
+    const int i0t = i0 + (pairs ? t * kQRows : 0);       // this warpgroup's tile
+    const int i_r = i0t + row;
     const int i_eff = min(i_r, n - 1);                   // padding rows mirror the last row
     const int lim = a.causal ? (L - n + i_eff + 1) : L;  // keys < lim are visible
-    const int lim_min = a.causal ? min(L - n + i0 + 1, L) : L;   // smallest lim of the tile
+    const int lim_min = a.causal ? min(L - n + i0t + 1, L) : L;  // smallest lim of the tile
     // window start of the row (keys >= lo are visible) and the tile's largest
     const int lo = a.window > 0 ? L - n + i_eff - a.window + 1 : 0;
-    const int lo_max = a.window > 0 ? L - n + min(i0 + kQRows, n) - 1 - a.window + 1 : 0;
+    const int lo_max = a.window > 0 ? L - n + min(i0t + kQRows, n) - 1 - a.window + 1 : 0;
     const uint32_t lane_base = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t t_s = lane_base + t * kKeys, t_o = lane_base + 2 * kKeys + t * 128;
     const float sc = a.scale_log2;
@@ -724,15 +732,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.defer_wait) pdl_wait_primary();
 }
 
-// The tensor-core path pairs two query heads of one KV head per CTA, so the
-// GQA group size must be even; other shapes run long rows on CUDA cores.
+// The tensor-core path pairs two query heads of one KV head per CTA, or with
+// an odd GQA group two query tiles of one head (AttnArgs::pair_tiles).
 bool prefill_supported(int head_dim, bool bf16, int group) {
-  return bf16 && (head_dim == 128 || head_dim == 64) && group % 2 == 0;
+  return bf16 && (head_dim == 128 || head_dim == 64) && group >= 1;
 }
 
-// Shared-prefix mode needs whole GQA groups in a 128-row tile.
+// Shared-prefix mode needs an even GQA group whose whole groups fill a
+// 128-row tile.
 bool prefill_packed_supported(int head_dim, bool bf16, int group) {
-  return prefill_supported(head_dim, bf16, group) && kQRows % group == 0;
+  return prefill_supported(head_dim, bf16, group) && group % 2 == 0 && kQRows % group == 0;
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
@@ -758,7 +767,8 @@ cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUt
   const int64_t tiles = a.cascade == 1
                             ? (a.num_tokens * a.group + 2 * kQRows - 1) / (2 * kQRows)
                             : (a.num_tokens + kQRows - 1) / kQRows + long_reqs;
-  const int64_t ys = a.cascade == 1 ? static_cast<int64_t>(a.hkv) * a.num_splits : a.hq / 2;
+  const int64_t ys = a.cascade == 1 ? static_cast<int64_t>(a.hkv) * a.num_splits
+                                    : (a.pair_tiles ? a.hq : a.hq / 2);
   if (tiles <= 0) return cudaSuccess;
   if (ys < 1 || tiles * ys > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};

@@ -214,6 +214,35 @@ def test_tensor_core_prefill_head_dim_64_long_chunk(window):
     _check_lse(lse, lse_ref)
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 128), (12, 4, 128), (15, 3, 64), (8, 8, 64)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tensor_core_prefill_odd_groups(hq, hkv, d, causal):
+    # an odd GQA group (1, 3, 5): the tensor-core prefill pairs two query tiles
+    # of one head; 1, 2, 3 and 9 tiles per request (the last pair half empty),
+    # on empty and cached prefixes, beside decode rows
+    shape = [(0, 100), (300, 256), (40, 300), (1000, 1), (0, 1100), (77, 5)]
+    w = workloads.build("odd_group", "bf16", hq, hkv, d, shape, seed=hq * 3 + d, causal=causal)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    _check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_tensor_core_prefill_odd_group_long_chunk(window):
+    # MHA (group 1) at 32 heads: a 2048-token chunk on a 700-token prefix
+    w = workloads.build("mha_chunk", "bf16", 32, 32, 128, [(700, 2048), (90, 1)], seed=7,
+                        window=window)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref, "bf16")
+    _check_lse(lse, lse_ref)
+
+
 def test_split_heuristic_rule():
     # one wave of split CTAs over 7/8 of the decode CTA slots (two per SM for
     # the bf16 tensor-core build), at least 8 blocks per split, split off once
