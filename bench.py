@@ -49,6 +49,9 @@ WORKLOAD_TEXT = {
                               "v_scale = 0.5; q, new K/V and out bf16)",
     "decode_8k_e4m3": "decode_8k over an 8-bit E4M3 KV cache (k_scale = v_scale = 0.5; q, new "
                       "K/V and out bf16): 512-block table from a shuffled 8192-block pool",
+    "prefill_8k_e4m3": "prefill_8k over an 8-bit E4M3 KV cache (k_scale = v_scale = 0.5; q, new "
+                       "K/V and out bf16): the write quantises the 8192 tokens into 512 "
+                       "shuffled blocks",
 }
 
 
@@ -757,12 +760,22 @@ def run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, 
         dv.copy_(host["v_new"], non_blocking=True)
         for k in dmeta:
             dmeta[k].copy_(hr[k], non_blocking=True)
-        pkv.pkv_write(dk, dv, dmeta["slot_mapping"], common["k_cache"], common["v_cache"],
-                      error_flag=flag)
-        pkv.pkv_attention_varlen(dq, common["k_cache"], common["v_cache"], out, dmeta["qsl"],
-                                 dmeta["seq_lens"], dmeta["block_table"], m["max_query_len"],
-                                 m["max_seq_len"], w.softmax_scale, causal=w.causal,
-                                 num_splits=splits, workspace=workspace, error_flag=flag)
+        if w.kv_dtype == "e4m3":
+            pkv.pkv_write_e4m3(dk, dv, dmeta["slot_mapping"], common["k_cache"],
+                               common["v_cache"], w.k_scale, w.v_scale, error_flag=flag)
+            pkv.pkv_attention_varlen_e4m3(
+                dq, common["k_cache"], common["v_cache"], out, dmeta["qsl"], dmeta["seq_lens"],
+                dmeta["block_table"], m["max_query_len"], m["max_seq_len"], w.softmax_scale,
+                w.k_scale, w.v_scale, causal=w.causal, num_splits=splits, workspace=workspace,
+                error_flag=flag)
+        else:
+            pkv.pkv_write(dk, dv, dmeta["slot_mapping"], common["k_cache"], common["v_cache"],
+                          error_flag=flag)
+            pkv.pkv_attention_varlen(dq, common["k_cache"], common["v_cache"], out,
+                                     dmeta["qsl"], dmeta["seq_lens"], dmeta["block_table"],
+                                     m["max_query_len"], m["max_seq_len"], w.softmax_scale,
+                                     causal=w.causal, num_splits=splits, workspace=workspace,
+                                     error_flag=flag)
         hout.copy_(out, non_blocking=True)
 
     k = min(args.steps, 2000) if decode_like else max(1, min(args.steps, 5))

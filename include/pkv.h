@@ -296,14 +296,18 @@ pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const
  *                  q[t,h,:] . value(K code_j)) value(V code_j)
  * (lse_out: the natural-log log-sum-exp of those scaled scores).  At head_dim
  * 128 codes are widened exactly to f16 and contracted on tensor cores with q
- * scaled by a power of two (fp32 accumulation, P rounded to f16 for P.V); at
- * head_dim 64 they are widened to fp32 in registers.
+ * scaled by a power of two (fp32 accumulation, P rounded to f16 for P.V): the
+ * decode kernel's mma.sync tiles for decode rows, and for longer requests the
+ * tcgen05 prefill tiles (codes widened in shared memory, each q row rewritten
+ * as f16 scaled so its largest magnitude lies in [2^14, 2^15)); at head_dim
+ * 64 they are widened to fp32 in registers on CUDA cores.
  *   q, out            device bf16 [num_tokens, num_q_heads, head_dim].
  *   k_cache, v_cache  device uint8 [num_blocks, 16, num_kv_heads, head_dim].
  *   k_scale, v_scale  finite, > 0 (else PKV_ERR_INVALID_ARG).
- * Everything else as pkv_attention_varlen, workspace included.  Requests
- * with n > PKV_DECODE_MAX_QLEN run on the decode kernel's CUDA-core tiles
- * (no tensor-core prefill for this format).
+ * Everything else as pkv_attention_varlen, workspace included: requests with
+ * n > PKV_DECODE_MAX_QLEN take the tensor-core prefill where the bf16 call's
+ * would at head_dim 128 (a positive softmax_scale, no window below 128 keys),
+ * else the decode kernel's CUDA-core tiles.
  */
 pkv_status pkv_attention_varlen_e4m3(const void* q, const void* k_cache, const void* v_cache,
                                      void* out, float* lse_out, const int32_t* query_start_loc,
@@ -452,10 +456,14 @@ pkv_status pkv_cascade_attention(const void* q, const void* k_cache, const void*
 /*
  * pkv_cascade_attention_e4m3 - pkv_cascade_attention over an E4M3 cache (the
  * format of pkv_write_e4m3; k_scale, v_scale finite and > 0, else
- * PKV_ERR_INVALID_ARG).  q and out are bf16.  The prefix pass runs on the
- * split-KV kernel's CUDA-core tiles, the own-key pass on the decode kernel
- * (tensor cores at head_dim 128); prefix_splits 0 takes the split count the
- * CUDA-core pass is sized for.  Everything else as pkv_cascade_attention.
+ * PKV_ERR_INVALID_ARG).  q and out are bf16.  At head_dim 128 the prefix
+ * pass runs on the tensor-core prefill tiles where the bf16 call's would
+ * (even GQA group dividing 128, positive softmax_scale; codes widened to f16,
+ * q rows scaled to f16 by powers of two) and prefix_splits 0 takes
+ * pkv_cascade_splits(..., PKV_BF16, ...); otherwise it runs on the split-KV
+ * kernel's CUDA-core tiles and takes pkv_cascade_splits(..., PKV_F32, ...).
+ * The own-key pass runs on the decode kernel (tensor cores at head_dim 128).
+ * Everything else as pkv_cascade_attention.
  */
 pkv_status pkv_cascade_attention_e4m3(
     const void* q, const void* k_cache, const void* v_cache, void* out, float* lse_out,

@@ -391,9 +391,10 @@ def pkv_cascade_attention(q, k_cache, v_cache, out, query_start_loc, suffix_lens
     if shared == 0:
         splits = 0
     elif splits == 0 and n_tok > 0:
-        # (an E4M3 prefix pass runs on the CUDA-core tiles: the fp32 rule)
-        splits = pkv_cascade_splits(n_tok, shared, hq, hkv, d,
-                                    torch.float32 if e4m3 else q.dtype, q.device.index)
+        # (an E4M3 prefix pass takes the tensor-core tiles where bf16 at
+        # head_dim 128 would, else the CUDA-core tiles: the fp32 rule)
+        rule = (torch.bfloat16 if d == 128 else torch.float32) if e4m3 else q.dtype
+        splits = pkv_cascade_splits(n_tok, shared, hq, hkv, d, rule, q.device.index)
     need = pkv_cascade_workspace_bytes(n_tok, hq, d, splits)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)

@@ -25,10 +25,11 @@ cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStr
 int decode_rows_per_tile(int group, int max_query_len, bool long_rows);
 bool decode_swizzled(ElemType et, int head_dim);
 int decode_ctas_per_sm(ElemType et, int head_dim);
-bool prefill_supported(int head_dim, bool bf16, int group);
-bool prefill_packed_supported(int head_dim, bool bf16, int group);
+bool prefill_supported(int head_dim, ElemType et, int group);
+bool prefill_packed_supported(int head_dim, ElemType et, int group);
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int head_dim, cudaStream_t stream);
+                           const CUtensorMap& vmap, int head_dim, ElemType et,
+                           cudaStream_t stream);
 }  // namespace pkv
 
 using namespace pkv;
@@ -280,7 +281,7 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
   // only.  Windows shorter than its 128-key tile run on the CUDA-core tiles:
   // a tensor-core tile would be mostly masked, and rows averaging so few keys
   // have outputs large enough for its bf16 P rounding to show.
-  const bool tc_prefill = prefill_supported(head_dim, bf16, num_q_heads / num_kv_heads) &&
+  const bool tc_prefill = prefill_supported(head_dim, et, num_q_heads / num_kv_heads) &&
                           softmax_scale > 0.f && (window == 0 || window >= kTcMinWindow);
   // E4M3 caches: decode rows take the register-q tiles, longer requests the
   // CUDA-core tiles of the same kernel
@@ -330,7 +331,7 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
     AttnArgs p = a;
     p.defer_wait = 1;
     p.pair_tiles = a.group % 2 != 0 ? 1 : 0;
-    e = launch_prefill(p, qmap, kmap_sw, vmap_sw, head_dim, st);
+    e = launch_prefill(p, qmap, kmap_sw, vmap_sw, head_dim, et, st);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -575,7 +576,9 @@ int pkv_cascade_splits(int64_t num_tokens, int shared_blocks, int num_q_heads, i
       num_q_heads % num_kv_heads != 0)
     return -1;
   return cascade_split_rule(num_tokens, shared_blocks, num_q_heads, num_kv_heads, head_dim,
-                            prefill_packed_supported(head_dim, dtype == PKV_BF16,
+                            prefill_packed_supported(head_dim,
+                                                     dtype == PKV_BF16 ? ElemType::kBf16
+                                                                       : ElemType::kF32,
                                                      num_q_heads / num_kv_heads),
                             device);
 }
@@ -631,7 +634,7 @@ static pkv_status cascade_call(const void* q, const void* k_cache, const void* v
       return PKV_ERR_CUDA;
     }
     S = cascade_split_rule(num_tokens, shared_blocks, num_q_heads, num_kv_heads, head_dim,
-                           prefill_packed_supported(head_dim, et == ElemType::kBf16,
+                           prefill_packed_supported(head_dim, et,
                                                     num_q_heads / num_kv_heads),
                            dev);
     if (S < 1) return PKV_ERR_CUDA;
@@ -668,7 +671,7 @@ static pkv_status cascade_call(const void* q, const void* k_cache, const void* v
   cudaError_t e = cudaSuccess;
   // tensor cores for the prefix pass (bf16, head_dim 128, a GQA group that
   // divides 128 rows, positive scale); the CUDA-core tiles otherwise
-  const bool tc = prefill_packed_supported(head_dim, et == ElemType::kBf16,
+  const bool tc = prefill_packed_supported(head_dim, et,
                                            num_q_heads / num_kv_heads) &&
                   softmax_scale > 0.f;
   // Two independent passes write disjoint partials; the merge reads both.
@@ -716,7 +719,7 @@ static pkv_status cascade_call(const void* q, const void* k_cache, const void* v
           !encode_cache_map(&kmap_sw, k_cache, num_slots, num_kv_heads, head_dim, et, true) ||
           !encode_cache_map(&vmap_sw, v_cache, num_slots, num_kv_heads, head_dim, et, true))
         return PKV_ERR_CUDA;
-      e = launch_prefill(p, qmap, kmap_sw, vmap_sw, head_dim, st);
+      e = launch_prefill(p, qmap, kmap_sw, vmap_sw, head_dim, et, st);
     } else {
       e = launch_decode(p, kmap, vmap, et, head_dim, /*pdl=*/true, st);
     }

@@ -35,6 +35,16 @@
 // units, so every p = 2^(s - reference) stays at most 2^8 - far from overflow
 // in fp32 and in the bf16 P - and o = acc / l does not depend on which
 // reference acc and l share: the same online softmax with fewer O rescales.
+//
+// E4M3 caches (head_dim 128): the tiles arrive as 8-bit codes into a one-tile
+// code buffer (K and V halves with their own barriers), and two more warps
+// (10, 11) widen them exactly to f16 in the layout the bf16 tiles have, ring
+// stage by ring stage, zeroing key rows past the context.  The MMAs run as
+// kind::f16 with f16 operands: each softmax thread first rewrites its bf16 Q
+// row in place as f16 scaled by 2^-e, e chosen per row so the row's largest
+// magnitude lands in [2^14, 2^15) (exact for every element within 2^31 of the
+// largest), and scales its scores back by 2^e together with softmax_scale *
+// k_scale; P goes to TMEM as f16 and v_scale joins the final 1 / l.
 #include <algorithm>
 
 #include "common.cuh"
@@ -46,18 +56,24 @@ namespace {
 constexpr int kQRows = 128;          // query rows per tile
 constexpr int kKeys = 128;           // keys per K/V tile (8 blocks)
 constexpr int kStages = 2;
-constexpr int kThreads = 320;        // 2 softmax warpgroups + producer warp + MMA warp
-constexpr int kHalf = 16384;         // 64 columns of a 128-row bf16 tile (128-byte rows)
+constexpr int kHalf = 16384;         // 64 columns of a 128-row 16-bit tile (128-byte rows)
+constexpr int kCodeBytes = kKeys * 128;   // one K (or V) tile of E4M3 codes at head_dim 128
+
+// 2 softmax warpgroups + producer warp + MMA warp (+ 2 widening warps for E4M3)
+__host__ __device__ constexpr int threads_for(bool f8) { return f8 ? 384 : 320; }
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr int kOffQ = 0;                                  // 2 query tiles x 2 halves
 constexpr int kOffKV = 4 * kHalf;                         // stages x (K 2 halves, V 2 halves)
 constexpr int kStageBytes = 4 * kHalf;
-constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-constexpr int kNumBars = 1 + 4 * kStages + 6;   // q, k_full[], v_full[], k_empty[], v_empty[], s[2], p[2], o[2]
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 32;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
+constexpr int kOffCode = kOffKV + kStages * kStageBytes;  // E4M3: K codes, V codes
+__host__ __device__ constexpr int off_bar(bool f8) { return f8 ? kOffCode + 2 * kCodeBytes : kOffCode; }
+// q, k_full[], v_full[], k_empty[], v_empty[], s[2], p[2], o[2]; E4M3 adds
+// code_full[2], code_empty[2] (K, V) and q_ready
+__host__ __device__ constexpr int num_bars(bool f8) { return 1 + 4 * kStages + 6 + (f8 ? 5 : 0); }
+__host__ __device__ constexpr int off_misc(bool f8) { return off_bar(f8) + num_bars(f8) * 8; }
+__host__ __device__ constexpr int smem_alloc(bool f8) { return off_misc(f8) + 32 + 1024; }
+static_assert(smem_alloc(true) <= 232448, "E4M3 prefill shared memory");
 // TMEM: S_t in columns [128 t, 128 t + 128) - its first 64 columns take P_t
 // (bf16 pairs) once the scores are read - and O_t in [256 + 128 t, ...).
 constexpr int kTmemCols = 512;
@@ -74,9 +90,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   return d;
 }
 
-// instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N
-__device__ __forceinline__ uint32_t idesc_bf16(int m, int n, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+// instruction descriptor, kind::f16: A and B both bf16 (or both f16), fp32
+// accumulator, M x N
+__device__ __forceinline__ uint32_t idesc_f16kind(int m, int n, int b_mn_major, bool f16) {
+  const uint32_t ab = f16 ? 0u : (1u << 7) | (1u << 10);
+  return (1u << 4) | ab | (static_cast<uint32_t>(b_mn_major) << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
@@ -222,24 +240,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// four E4M3 codes of a word (element 0 in the low byte) -> f16 pairs (0, 1)
+// and (2, 3); every E4M3 value is an f16 value, so the widening is exact
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 c0, c1;\n\tmov.b32 {c0, c1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c0;\n\tcvt.rn.f16x2.e4m3x2 %1, c1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// bf16 pair -> fp32 pair scaled by f (exact: a power of two in range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float f) {
+  return pack_f16(__uint_as_float(w << 16) * f, __uint_as_float(w & 0xFFFF0000u) * f);
+}
 
 }  // namespace
 
 // D: head_dim, 128 or 64.  The layouts are those of D = 128 (two 64-column
 // halves of Q, K and V, O_t in 128 TMEM columns); D = 64 fills one half of
-// each and the first 64 columns of O_t.
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+// each and the first 64 columns of O_t.  F8: an E4M3 cache (D = 128).
+template <int D, bool F8>
+__global__ void __launch_bounds__(threads_for(F8), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                    const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(!F8 || D == 128, "E4M3 tiles at head_dim 128");
+  constexpr int kThreads = threads_for(F8);
   constexpr int kH = D / 64;                             // 64-column halves of a row
   constexpr int kOC = D / 32;                            // 32-column chunks of an O row
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + off_bar(F8));
   uint64_t* bar_q = bars;
   // K and V halves of a stage have their own barriers: K(k) is free once
   // S1(k) has run, V(k) only after PV1(k), so K(k+2) can load earlier.
@@ -250,7 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_s = bars + 1 + 4 * kStages;              // [tile]
   uint64_t* bar_p = bar_s + 2;                           // [tile]
   uint64_t* bar_o = bar_s + 4;                           // [tile]
-  int* misc = reinterpret_cast<int*>(smem + kOffMisc);   // [0] request, [1] tile, [2] tmem
+  // E4M3: codes landed / codes widened, per half (K, V); Q rewritten as f16
+  uint64_t* code_full = bars + num_bars(false);
+  uint64_t* code_empty = code_full + 2;
+  uint64_t* bar_qr = code_full + 4;
+  int* misc = reinterpret_cast<int*>(smem + off_misc(F8));   // [0] request, [1] tile, [2] tmem
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool packed = a.cascade == 1;                    // shared-prefix mode
@@ -374,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
+      // E4M3: a stage is full once both widening warps have written it
+      mbar_init(&k_full[s], F8 ? 2 : 1);
+      mbar_init(&v_full[s], F8 ? 2 : 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
     }
@@ -383,6 +425,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_s[i], 1);
       mbar_init(&bar_p[i], kQRows);
       mbar_init(&bar_o[i], 1);
+    }
+    if (F8) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&code_full[i], 1);
+        mbar_init(&code_empty[i], 2);
+      }
+      mbar_init(bar_qr, 2 * kQRows);
     }
     fence_mbar_init();
   }
@@ -420,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     int kt = 0;
+    int issued[2] = {0, 0};                              // E4M3: code tiles issued per half
     for (; kt < ntk; ++kt) {
       const int st = kt % kStages;
       const int blk = (kt_base + kt) * (kKeys / kBlock) + (lane & 7);
@@ -432,6 +482,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const int slot = ent >= 0 ? ent * kBlock : oob;   // past the context: zero fill
+      if constexpr (F8) {
+        // the K codes of the tile, then its V codes, each into its one-tile
+        // buffer once the widening warps have read the previous tile's
+        for (int part = 0; part < 2; ++part) {
+          if (kt >= 1) {
+            uint32_t w = 1;
+            if (lane == 0) w = mbar_wait(&code_empty[part], (kt - 1) & 1) ? 1u : 0u;
+            if (!__shfl_sync(0xffffffffu, w, 0)) {
+              ok = false;
+              break;
+            }
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&code_full[part], kCodeBytes);
+          __syncwarp();
+          if (lane < kKeys / kBlock)
+            tma_load_3d(smem + kOffCode + part * kCodeBytes + lane * (kBlock * 128),
+                        part == 0 ? &kmap : &vmap, &code_full[part], 0, g, slot, pol_kv);
+          __syncwarp();
+          issued[part] = kt + 1;
+        }
+        if (!ok) break;
+        continue;
+      }
       uint8_t* kst = smem + kOffKV + st * kStageBytes;
       // K half of the stage, then its V half, each once its previous tile is done
       for (int part = 0; part < 2; ++part) {
@@ -461,9 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     // let every issued load land before the CTA can exit
     if (lane == 0) {
-      for (int kk = max(0, kt - kStages); kk < min(kt + 1, ntk); ++kk) {
-        if (!mbar_wait(&k_full[kk % kStages], (kk / kStages) & 1)) break;
-        if (kk < kt && !mbar_wait(&v_full[kk % kStages], (kk / kStages) & 1)) break;
+      if constexpr (F8) {
+        for (int part = 0; part < 2; ++part)
+          if (issued[part] > 0 && !mbar_wait(&code_full[part], (issued[part] - 1) & 1)) break;
+      } else {
+        for (int kk = max(0, kt - kStages); kk < min(kt + 1, ntk); ++kk) {
+          if (!mbar_wait(&k_full[kk % kStages], (kk / kStages) & 1)) break;
+          if (kk < kt && !mbar_wait(&v_full[kk % kStages], (kk / kStages) & 1)) break;
+        }
       }
       mbar_wait(bar_q, 0);
     }
@@ -474,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // after PV_t(k) has read them; group 0's softmax of tile k+1 overlaps
     // group 1's P.V of tile k and the reverse.
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(kQRows, kKeys, 0);
-      const uint32_t id_o = idesc_bf16(kQRows, D, 1);
+      const uint32_t id_s = idesc_f16kind(kQRows, kKeys, 0, F8);
+      const uint32_t id_o = idesc_f16kind(kQRows, D, 1, F8);
       // Descriptors are built once; a step only adds its byte offset >> 4 to
       // the start-address field (every address stays below 256 KB, so the
       // 14-bit field never carries).
@@ -511,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         return true;
       };
-      ok = mbar_wait(bar_q, 0) && wait_k(0);
+      ok = mbar_wait(F8 ? bar_qr : bar_q, 0) && wait_k(0);
       if (ok) {
         issue_s(0, 0);
         issue_s(1, 0);
@@ -538,6 +616,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     }
     __syncwarp();
+  } else if (warp >= 10) {
+    if constexpr (F8) {
+      // ================= E4M3 widening (warps 10, 11) =================
+      // Unit u = ct + 64 i: the 16 codes of 16-byte chunk j of key row r of
+      // the tile (both buffers 128B-swizzled: chunk j of row r sits at
+      // position j ^ (r & 7)), widened into f16 chunks 2 (j % 4) and
+      // 2 (j % 4) + 1 of column half j / 4 of the ring stage.  The 8 lanes of
+      // a shared-memory phase take 8 rows of one chunk: no bank conflicts.
+      const int ct = threadIdx.x - 10 * 32;
+      const int j = (ct >> 3) & 7;
+      const int c0 = 2 * (j & 3);
+      for (int kt = 0; ok && kt < ntk; ++kt) {
+        const int st = kt % kStages;
+        const int key0 = (kt_base + kt) * kKeys;
+        for (int part = 0; part < 2; ++part) {
+          uint32_t w = 1;
+          if (lane == 0) {
+            w = mbar_wait(&code_full[part], kt & 1) ? 1u : 0u;
+            if (w && kt >= kStages)
+              w = mbar_wait(part == 0 ? &k_empty[st] : &v_empty[st], ((kt / kStages) - 1) & 1)
+                      ? 1u : 0u;
+          }
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* src = smem + kOffCode + part * kCodeBytes;
+          uint8_t* dst = smem + kOffKV + st * kStageBytes + part * 2 * kHalf + (j >> 2) * kHalf;
+#pragma unroll 4
+          for (int i = 0; i < kKeys / 8; ++i) {
+            const int r = (ct & 7) + 8 * i;
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;  // key rows past the context: zero
+            if (key0 + r < kv_len) {
+              const uint4 cw = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7)) << 4));
+              widen4(cw.x, o0.x, o0.y);
+              widen4(cw.y, o0.z, o0.w);
+              widen4(cw.z, o1.x, o1.y);
+              widen4(cw.w, o1.z, o1.w);
+            }
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((c0 ^ (r & 7)) << 4)) = o0;
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+          }
+          // the widened stage is read by the tensor cores (async proxy)
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&code_empty[part]);
+            mbar_arrive(part == 0 ? &k_full[st] : &v_full[st]);
+          }
+        }
+      }
+      if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
+    }
   } else {
     // ================= softmax / epilogue: thread = query row of tile t =================
     const int t = warp >> 2;                             // 0: warps 0-3, 1: warps 4-7
@@ -553,9 +684,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lo_max = a.window > 0 ? L - n + min(i0t + kQRows, n) - 1 - a.window + 1 : 0;
     const uint32_t lane_base = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t t_s = lane_base + t * kKeys, t_o = lane_base + 2 * kKeys + t * 128;
-    const float sc = a.scale_log2;
+    float sc = a.scale_log2;
+    if constexpr (F8) {
+      // this row of Q as f16 scaled by 2^-e, in place (each 16-byte chunk
+      // keeps its swizzled position); its scores are scaled back by 2^e
+      const bool got = mbar_wait(bar_q, 0);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+      } else {
+        uint8_t* qrow = smem + kOffQ + 2 * t * kHalf + row * 128;
+        uint32_t mx = 0;                                 // two |bf16| maxima, as integers
+#pragma unroll
+        for (int c = 0; c < 2 * 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + (c >> 3) * kHalf + (c & 7) * 16);
+          mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
+          mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+        }
+        const uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);
+        // largest |q| in [2^E, 2^(E+1)): e = E - 14 (clamped so 2^-e and 2^e
+        // are normal floats; a zero row takes the lower bound)
+        const int e = min(max(static_cast<int>(m16 >> 7) - 127 - 14, -100), 113);
+        const float down = __int_as_float((127 - e) << 23);
+#pragma unroll
+        for (int c = 0; c < 2 * 8; ++c) {
+          uint4* pc = reinterpret_cast<uint4*>(qrow + (c >> 3) * kHalf + (c & 7) * 16);
+          uint4 v = *pc;
+          v.x = bf16x2_to_f16x2_scaled(v.x, down);
+          v.y = bf16x2_to_f16x2_scaled(v.y, down);
+          v.z = bf16x2_to_f16x2_scaled(v.z, down);
+          v.w = bf16x2_to_f16x2_scaled(v.w, down);
+          *pc = v;
+        }
+        sc *= __int_as_float((127 + e) << 23);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(bar_qr);
+      }
+    }
     float m = -INFINITY, l = 0.f;
-    for (int kt = 0; kt < ntk; ++kt) {
+    for (int kt = 0; ok && kt < ntk; ++kt) {
       const bool got = mbar_wait(&bar_s[t], kt & 1);
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
@@ -623,7 +789,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) w[j] = pack_bf16(s[64 * c + 2 * j], s[64 * c + 2 * j + 1]);
+        for (int j = 0; j < 32; ++j)
+          w[j] = F8 ? pack_f16(s[64 * c + 2 * j], s[64 * c + 2 * j + 1])
+                    : pack_bf16(s[64 * c + 2 * j], s[64 * c + 2 * j + 1]);
         tmem_st32u(t_s + 32 * c, w);
       }
       if (kt > 0) {
@@ -646,7 +814,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      if (t == 0 && kt == ntk - 1) {
+      // (E4M3: the widening warps zero those rows)
+      if (!F8 && t == 0 && kt == ntk - 1) {
         // key rows of the last V tile past the context are zeroed, once the
         // tile's V half has landed (its barrier is separate from K's)
         const bool got_v = mbar_wait(&v_full[kt % kStages], (kt / kStages) & 1);
@@ -655,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      if (t == 0 && kt == ntk - 1 && key0 + row >= kv_len) {
+      if (!F8 && t == 0 && kt == ntk - 1 && key0 + row >= kv_len) {
         uint8_t* vrow = smem + kOffKV + (kt % kStages) * kStageBytes + 2 * kHalf + row * 128;
 #pragma unroll
         for (int hh = 0; hh < kH; ++hh)
@@ -674,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = false;
     } else {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (F8 ? a.v_scale : 1.f) / l : 0.f;
       if (packed) {
         // row (token, head) of the 256-row pair: fp32 partial and log2 lse
         const int64_t rho = (2 * static_cast<int64_t>(tile) + t) * kQRows + row;
@@ -734,29 +903,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // The tensor-core path pairs two query heads of one KV head per CTA, or with
 // an odd GQA group two query tiles of one head (AttnArgs::pair_tiles).
-bool prefill_supported(int head_dim, bool bf16, int group) {
-  return bf16 && (head_dim == 128 || head_dim == 64) && group >= 1;
+bool prefill_supported(int head_dim, ElemType et, int group) {
+  return ((et == ElemType::kBf16 && (head_dim == 128 || head_dim == 64)) ||
+          (et == ElemType::kE4m3 && head_dim == 128)) &&
+         group >= 1;
 }
 
 // Shared-prefix mode needs an even GQA group whose whole groups fill a
 // 128-row tile.
-bool prefill_packed_supported(int head_dim, bool bf16, int group) {
-  return prefill_supported(head_dim, bf16, group) && group % 2 == 0 && kQRows % group == 0;
+bool prefill_packed_supported(int head_dim, ElemType et, int group) {
+  return prefill_supported(head_dim, et, group) && group % 2 == 0 && kQRows % group == 0;
 }
 
 cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                           const CUtensorMap& vmap, int head_dim, cudaStream_t stream) {
-  if (head_dim != 128 && head_dim != 64) return cudaErrorInvalidValue;
+                           const CUtensorMap& vmap, int head_dim, ElemType et,
+                           cudaStream_t stream) {
+  if (!prefill_supported(head_dim, et, 1)) return cudaErrorInvalidValue;
+  const bool f8 = et == ElemType::kE4m3;
   static unsigned done = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 32 || !((done >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(prefill_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc);
+    e = cudaFuncSetAttribute(prefill_kernel<128, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc(false));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemAlloc);
+      e = cudaFuncSetAttribute(prefill_kernel<64, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc(false));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<128, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem_alloc(true));
     if (e != cudaSuccess) return e;
     if (dev < 32) done |= 1u << dev;
   }
@@ -773,16 +949,17 @@ cudaError_t launch_prefill(const AttnArgs& a, const CUtensorMap& qmap, const CUt
   if (ys < 1 || tiles * ys > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles * ys));      // (tile, head pair), pair fastest
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.blockDim = dim3(threads_for(f8));
+  cfg.dynamicSmemBytes = smem_alloc(f8);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, prefill_kernel<128>, qmap, kmap, vmap, a)
-                         : cudaLaunchKernelEx(&cfg, prefill_kernel<64>, qmap, kmap, vmap, a);
+  if (f8) return cudaLaunchKernelEx(&cfg, prefill_kernel<128, true>, qmap, kmap, vmap, a);
+  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, prefill_kernel<128, false>, qmap, kmap, vmap, a)
+                         : cudaLaunchKernelEx(&cfg, prefill_kernel<64, false>, qmap, kmap, vmap, a);
 }
 
 }  // namespace pkv

@@ -3,9 +3,11 @@
 pkv_write_e4m3 must store exactly the oracle's codes (``oracle.fp8.quantize``:
 value / scale in fp32, nearest code, ties to even, saturating at 448).
 pkv_attention_varlen_e4m3 is held to the bf16 bar (max |err| <= 1e-2, mean
-|err| <= 1e-3): the codes widen exactly (to f16 on the tensor-core path, to
-fp32 on the CUDA-core tiles), so the only differences from the oracle are
-those of the bf16 path (fp32 accumulation, P rounded to 16 bits, bf16 output).
+|err| <= 1e-3): the codes widen exactly (to f16 on the tensor-core paths, to
+fp32 on the CUDA-core tiles) and q rows enter the f16 contractions scaled by
+powers of two (exact for every element within 2^31 of its row's largest), so
+the only differences from the oracle are those of the bf16 path (fp32
+accumulation, P rounded to 16 bits, bf16 output).
 The sliding-window and shared-prefix forms over an E4M3 cache are held to the
 same bar.
 """
@@ -193,6 +195,95 @@ def test_matches_the_bf16_path_on_the_dequantised_cache():
     assert rows
     diff = (out8.float() - out16.float())[rows].abs().max().item()
     assert diff <= 2.0 ** -8, diff
+
+
+# --------------------------------------------------------------------------
+# Requests longer than the decode bound at head_dim 128: the tcgen05 prefill
+# tiles, over codes widened to f16 in shared memory and q rows rescaled to f16
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (32, 8), (4, 4), (12, 4)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tensor_core_prefill(hq, hkv, causal):
+    # head pairs (even groups) and tile pairs (groups 1 and 3); 1, 2, 3 and 9
+    # query tiles with ragged tails, on empty and cached prefixes, beside
+    # decode rows and short tails
+    shape = [(0, 100), (300, 256), (40, 300), (1000, 1), (0, 1100), (77, 5)]
+    w = workloads.build("fp8_prefill", "bf16", hq, hkv, 128, shape, seed=hq * 5 + hkv,
+                        causal=causal, kv_dtype="e4m3", k_scale=0.45, v_scale=0.3)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref)
+    _check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("window", [0, 300])
+def test_tensor_core_prefill_long_chunk(window):
+    # a 2048-token chunk on a 1000-token prefix at GQA 32/8, every row
+    w = workloads.build("fp8_chunk", "bf16", 32, 8, 128, [(1000, 2048), (300, 1)], seed=81,
+                        window=window, kv_dtype="e4m3", k_scale=0.5, v_scale=0.5)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref)
+    _check_lse(lse, lse_ref)
+
+
+def test_tensor_core_prefill_q_rows_of_any_magnitude():
+    # every (token, head) row of q scaled by its own power of two in
+    # 2^-8 .. 2^20 (exact in bf16), with softmax_scale 2^-14 / sqrt(D) keeping
+    # the largest rows' scores moderate: rows up to ~5e6 in magnitude, beyond
+    # f16's 65504, are rewritten as f16 scaled to their own range, beside rows
+    # so small their softmax is near uniform
+    w = workloads.build("fp8_qscale", "bf16", 8, 2, 128, [(0, 300), (50, 130), (200, 1)],
+                        seed=91, kv_dtype="e4m3", k_scale=0.5, v_scale=0.5,
+                        scale=2.0 ** -14 / np.sqrt(128))
+    rng = np.random.Generator(np.random.PCG64(92))
+    f = np.ldexp(1.0, rng.integers(-8, 21, size=w.q.shape[:2]))[..., None]
+    q = (w.q.astype(np.uint32) << 16).view(np.float32) * f.astype(np.float32)
+    w.q = workloads.f32_to_bf16_bits(q)
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref)
+    _check_lse(lse, lse_ref)
+
+
+def test_tensor_core_prefill_ignores_codes_past_the_context():
+    # every slot no request reads holds the NaN code 0x7F: the key rows of a
+    # last tile past the context are zeroed when widened, so nothing leaks
+    w = workloads.build("fp8_stale", "bf16", 8, 2, 128, [(0, 200), (30, 150), (500, 1)],
+                        seed=93, kv_dtype="e4m3", k_scale=0.5, v_scale=0.5, pool_blocks=64)
+    dev = device_inputs(w)
+    meta = dev["meta"]
+    used = np.zeros(w.num_blocks * 16, dtype=bool)
+    for r, L in enumerate(meta["seq_lens"]):
+        for j in range(int(L)):
+            used[int(meta["block_table"][r, j // 16]) * 16 + j % 16] = True
+    stale = torch.from_numpy(~used).cuda()
+    for c in (dev["k_cache"], dev["v_cache"]):
+        c.view(w.num_blocks * 16, -1)[stale] = 0x7F
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    _check(out, o_ref)
+    _check_lse(lse, lse_ref)
+
+
+def test_prefill_8k_full_size_all_rows():
+    # all 8192 rows x 32 heads of the 8k causal prefill over an E4M3 cache
+    w = workloads.prefill_8k_e4m3()
+    dev = device_inputs(w)
+    out, lse, flag = run_step(dev)
+    o_ref, lse_ref, *_ = ref.paged_step(w)
+    assert int(flag.item()) == 0
+    _check(out, o_ref)
+    _check_lse(lse, lse_ref)
 
 
 @pytest.mark.parametrize("window", [1, 16, 100, 1000])

@@ -265,6 +265,13 @@ def decode_8k_e4m3(seed: int = 0, replicas: int = 1) -> Workload:
                  v_scale=0.5)
 
 
+def prefill_8k_e4m3(seed: int = 0, replicas: int = 1) -> Workload:
+    """prefill_8k over an 8-bit E4M3 cache (k_scale = v_scale = 0.5): the
+    8192 new tokens are quantised into the cache by the write, then attended."""
+    return build("prefill_8k_e4m3", "bf16", 32, 8, 128, [(0, 8192)], seed=seed,
+                 replicas=replicas, kv_dtype="e4m3", k_scale=0.5, v_scale=0.5)
+
+
 NAMED = {
     "tiny_mixed_f32": tiny_mixed_f32,
     "decode_8k": decode_8k,
@@ -273,6 +280,7 @@ NAMED = {
     "prefill_8k": prefill_8k,
     "decode_8k_e4m3": decode_8k_e4m3,
     "batched_decode_64_e4m3": batched_decode_64_e4m3,
+    "prefill_8k_e4m3": prefill_8k_e4m3,
     "cascade_64x4k": cascade_64x4k,
 }
 
