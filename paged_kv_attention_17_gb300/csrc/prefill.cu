@@ -36,15 +36,17 @@
 // in fp32 and in the bf16 P - and o = acc / l does not depend on which
 // reference acc and l share: the same online softmax with fewer O rescales.
 //
-// E4M3 caches (head_dim 128): the tiles arrive as 8-bit codes into a one-tile
-// code buffer (K and V halves with their own barriers), and two more warps
-// (10, 11) widen them exactly to f16 in the layout the bf16 tiles have, ring
-// stage by ring stage, zeroing key rows past the context.  The MMAs run as
-// kind::f16 with f16 operands: each softmax thread first rewrites its bf16 Q
-// row in place as f16 scaled by 2^-e, e chosen per row so the row's largest
-// magnitude lands in [2^14, 2^15) (exact for every element within 2^31 of the
-// largest), and scales its scores back by 2^e together with softmax_scale *
-// k_scale; P goes to TMEM as f16 and v_scale joins the final 1 / l.
+// E4M3 caches (head_dim 128): a K (or V) tile arrives as 16 KB of 8-bit codes
+// in the second half of its 32 KB ring slot, as early as a bf16 tile would,
+// and two more warps (10, 11) widen it in place, exactly, to the f16 tile the
+// MMAs read (the bf16 tiles' layout), zeroing key rows past the context: each
+// thread loads all its codes, the two warps meet at a named barrier, then
+// write.  The MMAs run as kind::f16 with f16 operands: each softmax thread
+// first rewrites its bf16 Q row in place as f16 scaled by 2^-e, e chosen per
+// row so the row's largest magnitude lands in [2^14, 2^15) (exact for every
+// element within 2^31 of the largest), and scales its scores back by 2^e
+// together with softmax_scale * k_scale; P goes to TMEM as f16 and v_scale
+// joins the final 1 / l.
 #include <algorithm>
 
 #include "common.cuh"
@@ -58,18 +60,19 @@ constexpr int kKeys = 128;           // keys per K/V tile (8 blocks)
 constexpr int kStages = 2;
 constexpr int kHalf = 16384;         // 64 columns of a 128-row 16-bit tile (128-byte rows)
 constexpr int kCodeBytes = kKeys * 128;   // one K (or V) tile of E4M3 codes at head_dim 128
+static_assert(kCodeBytes == kHalf, "a code tile fills the second half of its ring slot");
 
-// 2 softmax warpgroups + producer warp + MMA warp (+ 2 widening warps for E4M3)
+// 2 softmax warpgroups + producer warp + MMA warp (+ 2 widening warps for
+// E4M3: 12 warps keep three per SM sub-partition and 168 registers a thread)
 __host__ __device__ constexpr int threads_for(bool f8) { return f8 ? 384 : 320; }
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr int kOffQ = 0;                                  // 2 query tiles x 2 halves
 constexpr int kOffKV = 4 * kHalf;                         // stages x (K 2 halves, V 2 halves)
 constexpr int kStageBytes = 4 * kHalf;
-constexpr int kOffCode = kOffKV + kStages * kStageBytes;  // E4M3: K codes, V codes
-__host__ __device__ constexpr int off_bar(bool f8) { return f8 ? kOffCode + 2 * kCodeBytes : kOffCode; }
+__host__ __device__ constexpr int off_bar(bool) { return kOffKV + kStages * kStageBytes; }
 // q, k_full[], v_full[], k_empty[], v_empty[], s[2], p[2], o[2]; E4M3 adds
-// code_full[2], code_empty[2] (K, V) and q_ready
+// code_full[K, V][stage] and q_ready
 __host__ __device__ constexpr int num_bars(bool f8) { return 1 + 4 * kStages + 6 + (f8 ? 5 : 0); }
 __host__ __device__ constexpr int off_misc(bool f8) { return off_bar(f8) + num_bars(f8) * 8; }
 __host__ __device__ constexpr int smem_alloc(bool f8) { return off_misc(f8) + 32 + 1024; }
@@ -287,10 +290,10 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
   uint64_t* bar_s = bars + 1 + 4 * kStages;              // [tile]
   uint64_t* bar_p = bar_s + 2;                           // [tile]
   uint64_t* bar_o = bar_s + 4;                           // [tile]
-  // E4M3: codes landed / codes widened, per half (K, V); Q rewritten as f16
+  // E4M3: a stage's codes landed ([part * kStages + stage], part 0 K, 1 V;
+  // k_full / v_full then mean widened); Q rewritten as f16
   uint64_t* code_full = bars + num_bars(false);
-  uint64_t* code_empty = code_full + 2;
-  uint64_t* bar_qr = code_full + 4;
+  uint64_t* bar_qr = code_full + 2 * kStages;
   int* misc = reinterpret_cast<int*>(smem + off_misc(F8));   // [0] request, [1] tile, [2] tmem
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -427,10 +430,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
       mbar_init(&bar_o[i], 1);
     }
     if (F8) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&code_full[i], 1);
-        mbar_init(&code_empty[i], 2);
-      }
+      for (int i = 0; i < 2 * kStages; ++i) mbar_init(&code_full[i], 1);
       mbar_init(bar_qr, 2 * kQRows);
     }
     fence_mbar_init();
@@ -469,7 +469,6 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
         }
     }
     int kt = 0;
-    int issued[2] = {0, 0};                              // E4M3: code tiles issued per half
     for (; kt < ntk; ++kt) {
       const int st = kt % kStages;
       const int blk = (kt_base + kt) * (kKeys / kBlock) + (lane & 7);
@@ -482,33 +481,12 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
         }
       }
       const int slot = ent >= 0 ? ent * kBlock : oob;   // past the context: zero fill
-      if constexpr (F8) {
-        // the K codes of the tile, then its V codes, each into its one-tile
-        // buffer once the widening warps have read the previous tile's
-        for (int part = 0; part < 2; ++part) {
-          if (kt >= 1) {
-            uint32_t w = 1;
-            if (lane == 0) w = mbar_wait(&code_empty[part], (kt - 1) & 1) ? 1u : 0u;
-            if (!__shfl_sync(0xffffffffu, w, 0)) {
-              ok = false;
-              break;
-            }
-          }
-          if (lane == 0) mbar_arrive_expect_tx(&code_full[part], kCodeBytes);
-          __syncwarp();
-          if (lane < kKeys / kBlock)
-            tma_load_3d(smem + kOffCode + part * kCodeBytes + lane * (kBlock * 128),
-                        part == 0 ? &kmap : &vmap, &code_full[part], 0, g, slot, pol_kv);
-          __syncwarp();
-          issued[part] = kt + 1;
-        }
-        if (!ok) break;
-        continue;
-      }
       uint8_t* kst = smem + kOffKV + st * kStageBytes;
-      // K half of the stage, then its V half, each once its previous tile is done
+      // K half of the stage, then its V half, each once its previous tile is
+      // done (E4M3: the codes, into the second half of the slot)
       for (int part = 0; part < 2; ++part) {
-        uint64_t* fullb = part == 0 ? &k_full[st] : &v_full[st];
+        uint64_t* fullb = F8 ? &code_full[part * kStages + st]
+                             : (part == 0 ? &k_full[st] : &v_full[st]);
         uint64_t* emptyb = part == 0 ? &k_empty[st] : &v_empty[st];
         if (kt >= kStages) {
           uint32_t w = 1;
@@ -518,14 +496,18 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
             break;
           }
         }
-        if (lane == 0) mbar_arrive_expect_tx(fullb, kH * kHalf);
+        if (lane == 0) mbar_arrive_expect_tx(fullb, F8 ? kCodeBytes : kH * kHalf);
         __syncwarp();
         if (lane < kKeys / kBlock) {
           uint8_t* dst = kst + part * 2 * kHalf;
           const CUtensorMap* map = part == 0 ? &kmap : &vmap;
-          for (int hh = 0; hh < kH; ++hh)
-            tma_load_3d(dst + hh * kHalf + lane * (kBlock * 128), map, fullb, hh * 64, g, slot,
-                        pol_kv);
+          if constexpr (F8) {
+            tma_load_3d(dst + kHalf + lane * (kBlock * 128), map, fullb, 0, g, slot, pol_kv);
+          } else {
+            for (int hh = 0; hh < kH; ++hh)
+              tma_load_3d(dst + hh * kHalf + lane * (kBlock * 128), map, fullb, hh * 64, g, slot,
+                          pol_kv);
+          }
         }
         __syncwarp();
       }
@@ -534,14 +516,12 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
     if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
     // let every issued load land before the CTA can exit
     if (lane == 0) {
-      if constexpr (F8) {
-        for (int part = 0; part < 2; ++part)
-          if (issued[part] > 0 && !mbar_wait(&code_full[part], (issued[part] - 1) & 1)) break;
-      } else {
-        for (int kk = max(0, kt - kStages); kk < min(kt + 1, ntk); ++kk) {
-          if (!mbar_wait(&k_full[kk % kStages], (kk / kStages) & 1)) break;
-          if (kk < kt && !mbar_wait(&v_full[kk % kStages], (kk / kStages) & 1)) break;
-        }
+      for (int kk = max(0, kt - kStages); kk < min(kt + 1, ntk); ++kk) {
+        const int sk = kk % kStages;
+        if (!mbar_wait(F8 ? &code_full[sk] : &k_full[sk], (kk / kStages) & 1)) break;
+        if (kk < kt &&
+            !mbar_wait(F8 ? &code_full[kStages + sk] : &v_full[sk], (kk / kStages) & 1))
+          break;
       }
       mbar_wait(bar_q, 0);
     }
@@ -619,52 +599,60 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
   } else if (warp >= 10) {
     if constexpr (F8) {
       // ================= E4M3 widening (warps 10, 11) =================
-      // Unit u = ct + 64 i: the 16 codes of 16-byte chunk j of key row r of
-      // the tile (both buffers 128B-swizzled: chunk j of row r sits at
-      // position j ^ (r & 7)), widened into f16 chunks 2 (j % 4) and
-      // 2 (j % 4) + 1 of column half j / 4 of the ring stage.  The 8 lanes of
-      // a shared-memory phase take 8 rows of one chunk: no bank conflicts.
+      // Unit i of thread ct: the 16 codes of 16-byte chunk j of key row
+      // r = (ct % 8) + 8 i (the codes 128B-swizzled: chunk j of row r at
+      // position j ^ (r % 8)), widened into f16 chunks 2 (j % 4) and
+      // 2 (j % 4) + 1 of column half j / 4 of the slot.  The 8 lanes of a
+      // shared-memory phase take 8 rows of one chunk: no bank conflicts.  All
+      // the codes of a tile are read before any f16 chunk is written over them.
       const int ct = threadIdx.x - 10 * 32;
-      const int j = (ct >> 3) & 7;
+      const int j = (ct >> 3) & 7, r7 = ct & 7;
       const int c0 = 2 * (j & 3);
       for (int kt = 0; ok && kt < ntk; ++kt) {
         const int st = kt % kStages;
         const int key0 = (kt_base + kt) * kKeys;
         for (int part = 0; part < 2; ++part) {
           uint32_t w = 1;
-          if (lane == 0) {
-            w = mbar_wait(&code_full[part], kt & 1) ? 1u : 0u;
-            if (w && kt >= kStages)
-              w = mbar_wait(part == 0 ? &k_empty[st] : &v_empty[st], ((kt / kStages) - 1) & 1)
-                      ? 1u : 0u;
-          }
-          if (!__shfl_sync(0xffffffffu, w, 0)) {
+          if (lane == 0) w = mbar_wait(&code_full[part * kStages + st], (kt / kStages) & 1);
+          w = __shfl_sync(0xffffffffu, w, 0);
+          uint8_t* slot_base = smem + kOffKV + st * kStageBytes + part * 2 * kHalf;
+          const uint8_t* src = slot_base + kHalf + ((j ^ r7) << 4);
+          uint4 cw[kKeys / 8];
+#pragma unroll
+          for (int i = 0; i < kKeys / 8; ++i)
+            cw[i] = w ? *reinterpret_cast<const uint4*>(src + (r7 + 8 * i) * 128)
+                      : make_uint4(0, 0, 0, 0);
+          // the two warps meet once every code of the tile is read; a wait
+          // that gave up in either stops both together
+          uint32_t all_ok;
+          asm volatile(
+              "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+              "bar.red.and.pred q, 1, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+              : "=r"(all_ok)
+              : "r"(w)
+              : "memory");
+          if (!all_ok) {
             ok = false;
             break;
           }
-          const uint8_t* src = smem + kOffCode + part * kCodeBytes;
-          uint8_t* dst = smem + kOffKV + st * kStageBytes + part * 2 * kHalf + (j >> 2) * kHalf;
-#pragma unroll 4
+          uint8_t* dst = slot_base + (j >> 2) * kHalf;
+#pragma unroll
           for (int i = 0; i < kKeys / 8; ++i) {
-            const int r = (ct & 7) + 8 * i;
+            const int r = r7 + 8 * i;
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;  // key rows past the context: zero
             if (key0 + r < kv_len) {
-              const uint4 cw = *reinterpret_cast<const uint4*>(src + r * 128 + ((j ^ (r & 7)) << 4));
-              widen4(cw.x, o0.x, o0.y);
-              widen4(cw.y, o0.z, o0.w);
-              widen4(cw.z, o1.x, o1.y);
-              widen4(cw.w, o1.z, o1.w);
+              widen4(cw[i].x, o0.x, o0.y);
+              widen4(cw[i].y, o0.z, o0.w);
+              widen4(cw[i].z, o1.x, o1.y);
+              widen4(cw[i].w, o1.z, o1.w);
             }
-            *reinterpret_cast<uint4*>(dst + r * 128 + ((c0 ^ (r & 7)) << 4)) = o0;
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((c0 ^ r7) << 4)) = o0;
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((c0 + 1) ^ r7) << 4)) = o1;
           }
-          // the widened stage is read by the tensor cores (async proxy)
+          // the widened tile is read by the tensor cores (async proxy)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&code_empty[part]);
-            mbar_arrive(part == 0 ? &k_full[st] : &v_full[st]);
-          }
+          if (lane == 0) mbar_arrive(part == 0 ? &k_full[st] : &v_full[st]);
         }
       }
       if (!ok && lane == 0) raise_flag(a.flag, PKV_FLAG_TIMEOUT);
@@ -692,11 +680,15 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
       if (!__all_sync(0xffffffffu, got)) {
         ok = false;
       } else {
+        // (chunk c visited at position c ^ (row % 8): the 8 rows of a
+        // shared-memory phase then hit distinct banks)
         uint8_t* qrow = smem + kOffQ + 2 * t * kHalf + row * 128;
+        const int sw = row & 7;
         uint32_t mx = 0;                                 // two |bf16| maxima, as integers
 #pragma unroll
         for (int c = 0; c < 2 * 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(qrow + (c >> 3) * kHalf + (c & 7) * 16);
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(qrow + (c >> 3) * kHalf + ((c & 7) ^ sw) * 16);
           mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
           mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
         }
@@ -707,7 +699,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
         const float down = __int_as_float((127 - e) << 23);
 #pragma unroll
         for (int c = 0; c < 2 * 8; ++c) {
-          uint4* pc = reinterpret_cast<uint4*>(qrow + (c >> 3) * kHalf + (c & 7) * 16);
+          uint4* pc = reinterpret_cast<uint4*>(qrow + (c >> 3) * kHalf + ((c & 7) ^ sw) * 16);
           uint4 v = *pc;
           v.x = bf16x2_to_f16x2_scaled(v.x, down);
           v.y = bf16x2_to_f16x2_scaled(v.y, down);
