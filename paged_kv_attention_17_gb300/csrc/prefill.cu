@@ -256,6 +256,20 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t& lo, uint32_t& hi) {
       : "=r"(lo), "=r"(hi)
       : "r"(w));
 }
+// 16-byte shared-memory load and store (one 128-bit access a lane)
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
 // bf16 pair -> fp32 pair scaled by f (exact: a power of two in range)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float f) {
   return pack_f16(__uint_as_float(w << 16) * f, __uint_as_float(w & 0xFFFF0000u) * f);
@@ -615,13 +629,14 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
           uint32_t w = 1;
           if (lane == 0) w = mbar_wait(&code_full[part * kStages + st], (kt / kStages) & 1);
           w = __shfl_sync(0xffffffffu, w, 0);
-          uint8_t* slot_base = smem + kOffKV + st * kStageBytes + part * 2 * kHalf;
-          const uint8_t* src = slot_base + kHalf + ((j ^ r7) << 4);
+          // (a wait that gave up reads whatever the slot holds; nothing of it
+          // is written before all_ok below stops both warps)
+          const uint32_t slot_base =
+              smem_u32(smem + kOffKV + st * kStageBytes + part * 2 * kHalf);
+          const uint32_t src = slot_base + kHalf + ((j ^ r7) << 4) + r7 * 128;
           uint4 cw[kKeys / 8];
 #pragma unroll
-          for (int i = 0; i < kKeys / 8; ++i)
-            cw[i] = w ? *reinterpret_cast<const uint4*>(src + (r7 + 8 * i) * 128)
-                      : make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < kKeys / 8; ++i) cw[i] = lds128(src + i * 8 * 128);
           // the two warps meet once every code of the tile is read; a wait
           // that gave up in either stops both together
           uint32_t all_ok;
@@ -635,7 +650,7 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
             ok = false;
             break;
           }
-          uint8_t* dst = slot_base + (j >> 2) * kHalf;
+          const uint32_t dst = slot_base + (j >> 2) * kHalf + r7 * 128;
 #pragma unroll
           for (int i = 0; i < kKeys / 8; ++i) {
             const int r = r7 + 8 * i;
@@ -646,8 +661,8 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
               widen4(cw[i].z, o1.x, o1.y);
               widen4(cw[i].w, o1.z, o1.w);
             }
-            *reinterpret_cast<uint4*>(dst + r * 128 + ((c0 ^ r7) << 4)) = o0;
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((c0 + 1) ^ r7) << 4)) = o1;
+            sts128(dst + i * 8 * 128 + ((c0 ^ r7) << 4), o0);
+            sts128(dst + i * 8 * 128 + (((c0 + 1) ^ r7) << 4), o1);
           }
           // the widened tile is read by the tensor cores (async proxy)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -682,13 +697,12 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
       } else {
         // (chunk c visited at position c ^ (row % 8): the 8 rows of a
         // shared-memory phase then hit distinct banks)
-        uint8_t* qrow = smem + kOffQ + 2 * t * kHalf + row * 128;
+        const uint32_t qrow = smem_u32(smem + kOffQ + 2 * t * kHalf + row * 128);
         const int sw = row & 7;
         uint32_t mx = 0;                                 // two |bf16| maxima, as integers
 #pragma unroll
         for (int c = 0; c < 2 * 8; ++c) {
-          const uint4 v =
-              *reinterpret_cast<const uint4*>(qrow + (c >> 3) * kHalf + ((c & 7) ^ sw) * 16);
+          const uint4 v = lds128(qrow + (c >> 3) * kHalf + ((c & 7) ^ sw) * 16);
           mx = __vmaxu2(mx, __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu));
           mx = __vmaxu2(mx, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
         }
@@ -699,13 +713,13 @@ __global__ void __launch_bounds__(threads_for(F8), 1)
         const float down = __int_as_float((127 - e) << 23);
 #pragma unroll
         for (int c = 0; c < 2 * 8; ++c) {
-          uint4* pc = reinterpret_cast<uint4*>(qrow + (c >> 3) * kHalf + ((c & 7) ^ sw) * 16);
-          uint4 v = *pc;
+          const uint32_t pc = qrow + (c >> 3) * kHalf + ((c & 7) ^ sw) * 16;
+          uint4 v = lds128(pc);
           v.x = bf16x2_to_f16x2_scaled(v.x, down);
           v.y = bf16x2_to_f16x2_scaled(v.y, down);
           v.z = bf16x2_to_f16x2_scaled(v.z, down);
           v.w = bf16x2_to_f16x2_scaled(v.w, down);
-          *pc = v;
+          sts128(pc, v);
         }
         sc *= __int_as_float((127 + e) << 23);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
