@@ -62,7 +62,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=200)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOAD_TEXT))
-    p.add_argument("--no-secondary", action="store_true", help="skip the prefill_8k line item")
+    p.add_argument("--no-secondary", action="store_true", help="skip the secondary workload lines")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args(argv)
@@ -798,7 +798,7 @@ def run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, 
             "ms_per_step": round(ms, 6), "mode": "eager API calls, pinned host buffers"}
 
 
-SECONDARY = ("batched_decode_64", "mixed_chunked", "prefill_8k")
+SECONDARY = ("batched_decode_64", "mixed_chunked", "prefill_8k", "prefill_8k_e4m3")
 
 
 def run_secondary(name, local_rank, steps, warmup, cpu_seconds):

@@ -198,7 +198,8 @@ size_t pkv_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int num_
  * kernel (partials merged by a log-sum-exp combine kernel when num_splits >
  * 1), longer ones the tiled prefill kernel: on tensor cores for bf16 at
  * head_dim 64 or 128 (two query heads of a KV head per CTA, or with an odd
- * GQA group two query tiles of one head), else on the decode kernel's
+ * GQA group two query tiles of one head; an E4M3 cache through
+ * pkv_attention_varlen_e4m3 at head_dim 128), else on the decode kernel's
  * CUDA-core 16-row tiles.
  *
  *   q, out            device [num_tokens, num_q_heads, head_dim], dtype.
