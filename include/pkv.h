@@ -269,7 +269,8 @@ pkv_status pkv_write_attention_varlen(
  * definition.  Reading taken: with window W > 0 the new token at position
  * p = L - n + i sees only keys j with p - W < j (the W most recent
  * positions, itself included), on top of the causal limit j <= p (or j < L
- * with causal == 0).  window == 0 is pkv_attention_varlen exactly.  Key
+ * with causal == 0).  window == 0 is pkv_attention_varlen exactly, and so is
+ * any window >= max_seq_len (it excludes no key; the call runs as window 0).  Key
  * blocks wholly below a tile's window start are not read, and the automatic
  * split count is sized for a context of window + PKV_DECODE_MAX_QLEN keys.
  * Windows shorter than 128 keys run every request on the split-KV kernel's

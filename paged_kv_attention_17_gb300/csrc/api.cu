@@ -237,6 +237,10 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
   const int64_t num_slots = num_blocks * kBlock;
   if (num_slots > 0x7FFFFFFFll) return PKV_ERR_UNSUPPORTED;   // TMA row coordinates are int32
 
+  // a window of at least max_seq_len positions excludes no key (a row at
+  // position p < max_seq_len sees keys j > p - window, and p - window < 0):
+  // it is the plain call, launched as such
+  if (window >= max_seq_len) window = 0;
   int splits = num_splits;
   if (splits == 0) {
     int dev = 0;

@@ -210,6 +210,42 @@ __device__ __forceinline__ float f16_hi(uint32_t w) {
   return f;
 }
 
+// D += A.B for a 16x32 A and a 32x8 B of E4M3 codes (fp32 accumulation):
+// lane 4g+q holds A rows g (a0, a2) and g+8 (a1, a3), k 4q..4q+3 (a0, a1) and
+// 16+4q..16+4q+3 (a2, a3), four codes a register, element 0 in the low byte;
+// B column g, k 4q..4q+3 (b0) and 16+4q.. (b1); D as for mma16816.
+__device__ __forceinline__ void mma16832_e4m3(float& d0, float& d1, float& d2, float& d3,
+                                              uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four values x0..x3 (each with at most 8 significant bits, magnitudes below
+// 2^8) as two E4M3 words, hi + lo = x: hi is x rounded to E4M3, lo the
+// remainder (at most 4 significant bits: exact unless below E4M3's range,
+// 2^-9), element 0 in the low byte.
+__device__ __forceinline__ void e4m3_split4(float x0, float x1, float x2, float x3,
+                                            uint32_t& hi, uint32_t& lo) {
+  uint32_t h01, h23, l01, l23;
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(h01) : "f"(x1), "f"(x0));
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(h23) : "f"(x3), "f"(x2));
+  hi = h01 | (h23 << 16);
+  uint32_t f01, f23;                                   // hi widened back (exactly) to f16
+  e4m3x4_to_f16x2x2(hi, f01, f23);
+  const float r0 = x0 - f16_lo(f01), r1 = x1 - f16_hi(f01);
+  const float r2 = x2 - f16_lo(f23), r3 = x3 - f16_hi(f23);
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(l01) : "f"(r1), "f"(r0));
+  asm("{\n\t.reg .b16 t;\n\tcvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\tcvt.u32.u16 %0, t;\n\t}"
+      : "=r"(l23) : "f"(r3), "f"(r2));
+  lo = l01 | (l23 << 16);
+}
+
 // Tensor-core (mma.sync m16n8k16) build of the decode kernel: bf16 caches
 // (head_dim 64 or 128) and E4M3 caches of head_dim 128.  The GQA group's
 // rows (up to 16 per tile) are the M dimension of both contractions, so one
@@ -279,10 +315,15 @@ struct DecodeSmem {
   static constexpr int kRingBytes = kStageArea > kMergeBytes ? kStageArea : kMergeBytes;
   // CUDA-core build: q rows as fp32; tensor-core build: the tile's q rows as
   // loaded (bf16), rows padded by 16 bytes so the fragment reads of 8 rows
-  // hit distinct banks
+  // hit distinct banks, or (E4M3 cache, E4M3 contraction of K) the rows' hi
+  // codes, their lo codes (D + 16 bytes a row each) and a score scale per row
   static constexpr int kQRowBytes = D * 2 + 16;
+  static constexpr int kQCodeRowBytes = D + 16;
+  static constexpr int kQCodeBytes = C::kMma && kIsE4m3<T> ? 2 * R * kQCodeRowBytes + R * 4 : 0;
   static constexpr int kQOff = kRingBytes;
-  static constexpr int kPOff = kQOff + (C::kMma ? R * kQRowBytes : R * D * 4);
+  static constexpr int kQBytes =
+      C::kMma ? (kQCodeBytes > R * kQRowBytes ? kQCodeBytes : R * kQRowBytes) : R * D * 4;
+  static constexpr int kPOff = kQOff + kQBytes;
   static constexpr int kBarOff = kPOff + (C::kMma ? 0 : C::kWarps * kBlock * R * 8);
   // kfull[], vfull[], empty[], then per consumer warp the barrier and the
   // verdict of its speculative first block
@@ -585,6 +626,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   // metadata; reloaded below if the metadata puts the rows elsewhere, then
   // staged in shared memory, where each lane picks its fragment words.
   constexpr int kMT = kMma ? D / 16 : 1;               // k-steps of Q.K^T
+  // E4M3 cache: K's codes enter the MMAs as they are (m16n8k32 E4M3 against
+  // q split into two E4M3 terms) in unsplit launches of up to 8 rows a tile,
+  // where the per-block path dominates; split launches, latency-bound, keep
+  // the shorter q set-up of f16 MMAs over widened codes
+  constexpr bool kF8Mma = kMma && kIsE4m3<T> && !SPEC && R <= 8;
   constexpr bool kHi = R == 16;                        // M-rows 8..15 are tile rows
   constexpr int kHR = kHi ? 2 : 1;                     // M-row halves this lane holds
   constexpr int kQChunks = R * D / 8;                  // 16-byte pieces of the tile's q rows
@@ -773,11 +819,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   //      16-dim m-tile. ----
   constexpr int kMD = kMma ? D / 16 : 1;               // m-tiles of O^T (16 dims each)
   constexpr float kLag = 8.f;
-  uint32_t qa[kMT][2 * kHR];                           // [t][rows 8h + g8: k lo, k hi per h]
+  // B operands of S^T = K.Q^T: [t][rows 8h + g8: k lo, k hi per h]; E4M3
+  // cache: [u] the hi words and [kMT / 2 + u] the lo words of k32-step u
+  uint32_t qa[kMT][2 * kHR];
   float oacc[kMD][kHR][4];                             // O^T: dims g8 (c0, c1), g8 + 8 (c2, c3)
   float mm[kHR][2], ll[kHR][2], lr[kHR][2];
   int mlim[kHR][2], mlo[kHR][2];
-  float score_scale = a.scale_log2;
+  // log2-domain score scale of this lane's accumulator columns (rows
+  // 8h + 2kq + e); per row for E4M3 caches, whose q rows carry their own
+  // power-of-two scaling
+  float rs[kHR][2];
+#pragma unroll
+  for (int hr = 0; hr < kHR; ++hr)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) rs[hr][e] = a.scale_log2;
 #pragma unroll
   for (int hr = 0; hr < kHR; ++hr)
 #pragma unroll
@@ -892,17 +947,63 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
       // ---- q (loaded right after the wait): reloaded if the metadata puts
       //      the rows elsewhere, staged in shared memory, and each lane's B
       //      operand words picked for rows 8h + g8 (zero past the tile's
-      //      rows).  E4M3 cache: q is scaled by a power of two bringing
-      //      max|q| into [2^14, 2^15), where f16 holds every bf16 value
-      //      exactly, and the score scale takes the inverse. ----
+      //      rows).  E4M3 cache: each q row is scaled by a power of two
+      //      bringing its max|q| into [2^7, 2^8) and split exactly into two
+      //      E4M3 terms (hi + lo), so K's codes enter the MMAs as they are;
+      //      the row's score scale takes the inverse power. ----
       if (q0 != (prefix_pass ? 0 : q0_hint)) load_q(q0);
       uint8_t* qst = smem + Sm::kQOff;
+      if constexpr (kF8Mma) {
+        // E4M3 contraction: the 16 threads holding a row's 8-element chunks (a
+        // half-warp) find its max|q|, scale it by 2^-e into [2^7, 2^8) and
+        // split each chunk exactly into hi + lo E4M3 codes; a row past the
+        // tile's rows is zeros.  Code rows: hi at qst, lo R rows further,
+        // then the rows' log2-domain score scales.
+        static_assert(D / 8 == 16, "a q row is one half-warp's chunks");
+        float* rscale = reinterpret_cast<float*>(qst + 2 * R * Sm::kQCodeRowBytes);
 #pragma unroll
-      for (int u = 0; u < kQLd; ++u) {
-        const int idx = threadIdx.x + u * C::kConsumerThreads;
-        if (idx < kQChunks)
-          *reinterpret_cast<uint4*>(qst + (idx / (D / 8)) * Sm::kQRowBytes + (idx % (D / 8)) * 16) =
-              qld[u];
+        for (int u = 0; u < kQLd; ++u) {
+          const int idx = threadIdx.x + u * C::kConsumerThreads;
+          const bool in = idx < kQChunks;
+          const uint4 v = in ? qld[u] : make_uint4(0u, 0u, 0u, 0u);
+          const float x[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                              bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+          float mx = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(x[i]));
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (in) {
+            const int rho = idx / (D / 8), c = idx % (D / 8);
+            const int ex = (__float_as_int(mx) >> 23) & 0xff;
+            // max|q| in [2^E, 2^(E+1)): e = E - 7 (clamped so 2^-e and 2^e
+            // are normal floats; a zero row takes e = 0); a row holding an
+            // infinity or a NaN gets a NaN scale, so its scores are NaN
+            const int e = mx > 0.f ? max(-120, min(120, ex - 127 - 7)) : 0;
+            const float qs = __int_as_float((127 - e) << 23);      // 2^-e
+            uint32_t h0 = 0u, h1 = 0u, l0 = 0u, l1 = 0u;
+            if (rho < nrows) {
+              e4m3_split4(x[0] * qs, x[1] * qs, x[2] * qs, x[3] * qs, h0, l0);
+              e4m3_split4(x[4] * qs, x[5] * qs, x[6] * qs, x[7] * qs, h1, l1);
+            }
+            *reinterpret_cast<uint2*>(qst + rho * Sm::kQCodeRowBytes + 8 * c) =
+                make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(qst + (R + rho) * Sm::kQCodeRowBytes + 8 * c) =
+                make_uint2(l0, l1);
+            if (c == 0)
+              rscale[rho] = rho < nrows && ex == 0xff
+                                ? __int_as_float(0x7fc00000)
+                                : a.scale_log2 * __int_as_float((127 + (rho < nrows ? e : 0)) << 23);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kQLd; ++u) {
+          const int idx = threadIdx.x + u * C::kConsumerThreads;
+          if (idx < kQChunks)
+            *reinterpret_cast<uint4*>(qst + (idx / (D / 8)) * Sm::kQRowBytes + (idx % (D / 8)) * 16) =
+                qld[u];
+        }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(C::kConsumerThreads) : "memory");
       uint32_t qw[kHR][kMT][2];
@@ -912,8 +1013,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
         const uint8_t* qrow = qst + rho * Sm::kQRowBytes;
 #pragma unroll
         for (int t = 0; t < kMT; ++t) {
-          if (rho >= nrows) {
-            qw[hr][t][0] = qw[hr][t][1] = 0u;
+          if (kF8Mma || rho >= nrows) {
+            qw[hr][t][0] = qw[hr][t][1] = 0u;                // (kF8Mma: the code rows below)
           } else if constexpr (kIsE4m3<T>) {
             // dims 32kq + 4t .. +3
             const uint2 v = *reinterpret_cast<const uint2*>(qrow + (32 * kq + 4 * t) * 2);
@@ -926,7 +1027,43 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
           }
         }
       }
-      if constexpr (kIsE4m3<T>) {
+      if constexpr (kF8Mma) {
+        // the lane's B words: row 8h + g8, dims 32kq .. 32kq + 31 of the hi
+        // and lo code rows (word t: dims 32kq + 4t .. +3, k32-step t / 2, B
+        // register t % 2); the scales of its accumulator columns, rows
+        // 8h + 2kq + e
+        const float* rscale = reinterpret_cast<const float*>(qst + 2 * R * Sm::kQCodeRowBytes);
+#pragma unroll
+        for (int hr = 0; hr < kHR; ++hr) {
+          const int rho = g8 + 8 * hr;
+          uint4 w[2][2] = {{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)},
+                           {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)}};
+          if (rho < nrows) {
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2)
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                w[s2][h] = lds128(smem_u32(qst + (s2 * R + rho) * Sm::kQCodeRowBytes + 32 * kq + 16 * h));
+          }
+#pragma unroll
+          for (int t = 0; t < kMT; ++t) {
+#pragma unroll
+            for (int s2 = 0; s2 < 2; ++s2) {
+              const uint4& c4 = w[s2][t >> 2];
+              const uint32_t word = (t & 3) == 0 ? c4.x : (t & 3) == 1 ? c4.y : (t & 3) == 2 ? c4.z : c4.w;
+              qa[s2 * (kMT / 2) + (t >> 1)][2 * hr + (t & 1)] = word;
+            }
+          }
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int rc = 8 * hr + 2 * kq + e2;
+            rs[hr][e2] = rc < R ? rscale[rc] : a.scale_log2;
+          }
+        }
+      } else if constexpr (kIsE4m3<T>) {
+        // f16 contraction: q scaled by a power of two bringing max|q| into
+        // [2^14, 2^15), where f16 holds every bf16 value exactly; the score
+        // scale takes the inverse
         float mx = 0.f;
 #pragma unroll
         for (int hr = 0; hr < kHR; ++hr)
@@ -940,15 +1077,17 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
         if (mx > 0.f && mx <= 3.0e38f) e = ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14;
         e = max(-100, min(100, e));
         const float qs = __int_as_float((127 - e) << 23);          // 2^-e
-        score_scale = a.scale_log2 * __int_as_float((127 + e) << 23);
+        const float sscale = a.scale_log2 * __int_as_float((127 + e) << 23);
 #pragma unroll
-        for (int hr = 0; hr < kHR; ++hr)
+        for (int hr = 0; hr < kHR; ++hr) {
 #pragma unroll
           for (int t = 0; t < kMT; ++t)
 #pragma unroll
             for (int u = 0; u < 2; ++u)
               qa[t][2 * hr + u] =
                   pack_f16x2(bf16_lo(qw[hr][t][u]) * qs, bf16_hi(qw[hr][t][u]) * qs);
+          rs[hr][0] = rs[hr][1] = sscale;
+        }
       } else {
 #pragma unroll
         for (int hr = 0; hr < kHR; ++hr)
@@ -1087,9 +1226,38 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
             mma16816<kF16>(sc[t & 1][hr][0], sc[t & 1][hr][1], sc[t & 1][hr][2], sc[t & 1][hr][3],
                            a0, a1, a2, a3, qa[t][2 * hr], qa[t][2 * hr + 1]);
         };
-        if constexpr (kIsE4m3<T>) {
+        if constexpr (kF8Mma) {
           // lane's codes: key rows g8 and g8 + 8, bytes 32kq .. 32kq + 31
-          // (16-byte chunks 2kq, 2kq + 1, placed at chunk ^ (row % 8))
+          // (16-byte chunks 2kq, 2kq + 1, placed at chunk ^ (row % 8)).
+          // k32-step u takes words 2u (k 4kq..) and 2u + 1 (k 16 + 4kq..) of
+          // each row as they are: the codes are the A operand, against the hi
+          // and lo terms of q in two independent accumulator chains
+          uint4 kc[2][2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              kc[j][h] = lds128(ks_u + (g8 + 8 * j) * 128 + (((2 * kq + h) ^ g8) << 4));
+          auto word = [&](const uint4& c4, int w) {
+            return w == 0 ? c4.x : w == 1 ? c4.y : w == 2 ? c4.z : c4.w;
+          };
+#pragma unroll
+          for (int u = 0; u < kMT / 2; ++u) {
+            const int t0 = 2 * u, t1 = 2 * u + 1;
+            const uint32_t a0 = word(kc[0][t0 >> 2], t0 & 3), a1 = word(kc[1][t0 >> 2], t0 & 3);
+            const uint32_t a2 = word(kc[0][t1 >> 2], t1 & 3), a3 = word(kc[1][t1 >> 2], t1 & 3);
+#pragma unroll
+            for (int hr = 0; hr < kHR; ++hr) {
+              mma16832_e4m3(sc[0][hr][0], sc[0][hr][1], sc[0][hr][2], sc[0][hr][3], a0, a1, a2,
+                            a3, qa[u][2 * hr], qa[u][2 * hr + 1]);
+              mma16832_e4m3(sc[1][hr][0], sc[1][hr][1], sc[1][hr][2], sc[1][hr][3], a0, a1, a2,
+                            a3, qa[kMT / 2 + u][2 * hr], qa[kMT / 2 + u][2 * hr + 1]);
+            }
+          }
+        } else if constexpr (kIsE4m3<T>) {
+          // lane's codes: key rows g8 and g8 + 8, bytes 32kq .. 32kq + 31
+          // (16-byte chunks 2kq, 2kq + 1, placed at chunk ^ (row % 8)),
+          // widened to f16 k-step by k-step
           uint4 kc[2][2];
 #pragma unroll
           for (int j = 0; j < 2; ++j)
@@ -1135,7 +1303,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int e = c & 1, key = c < 2 ? kA : kB;
-            const float v = (sc[0][hr][c] + sc[1][hr][c]) * score_scale;
+            const float v = (sc[0][hr][c] + sc[1][hr][c]) * rs[hr][e];
             x[hr][c] = all_in || (key < mlim[hr][e] && key >= mlo[hr][e]) ? v : -INFINITY;
           }
         // ---- online softmax with a lagged reference max per row: a row's 16
