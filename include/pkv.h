@@ -297,12 +297,16 @@ pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const
  *   out[t, h, :] = v_scale * sum_j softmax_j(softmax_scale * k_scale *
  *                  q[t,h,:] . value(K code_j)) value(V code_j)
  * (lse_out: the natural-log log-sum-exp of those scaled scores).  At head_dim
- * 128 codes are widened exactly to f16 and contracted on tensor cores with q
- * scaled by a power of two (fp32 accumulation, P rounded to f16 for P.V): the
- * decode kernel's mma.sync tiles for decode rows, and for longer requests the
- * tcgen05 prefill tiles (codes widened in shared memory, each q row rewritten
- * as f16 scaled so its largest magnitude lies in [2^14, 2^15)); at head_dim
- * 64 they are widened to fp32 in registers on CUDA cores.
+ * 128 the contractions run on tensor cores with fp32 accumulation and P
+ * rounded to f16 for P.V.  V codes are widened exactly to f16.  K codes are
+ * widened too, with q scaled by a power of two into f16, in split decode
+ * launches; in unsplit ones (up to 8 rows a tile) they enter E4M3 MMAs as
+ * they are, against each q row scaled by a power of two and split exactly
+ * into two E4M3 terms.  That is the decode kernel's mma.sync tiles for decode
+ * rows; longer requests take the tcgen05 prefill tiles (codes widened in
+ * shared memory, each q row rewritten as f16 scaled so its largest magnitude
+ * lies in [2^14, 2^15)).  At head_dim 64 the codes are widened to fp32 in
+ * registers on CUDA cores.
  *   q, out            device bf16 [num_tokens, num_q_heads, head_dim].
  *   k_cache, v_cache  device uint8 [num_blocks, 16, num_kv_heads, head_dim].
  *   k_scale, v_scale  finite, > 0 (else PKV_ERR_INVALID_ARG).
