@@ -645,6 +645,33 @@ def run_gpu(args, rank, world, local_rank):
     roof["peak_source"] = peak_src
     roof["ms_per_launch"] = round(att_ms, 6)
 
+    # ---- the KV scatter alone (pkv_write / pkv_write_e4m3, steps that run it
+    #      as its own launch): GB/s on 2 x (read + write) bytes, K and V, each
+    #      call timed with events after an L2 flush ----
+    scatter = None
+    if not fused:
+        n_written = int((reps[0]["slot_mapping"] >= 0).sum().item())
+        src_es = common["k_new"].element_size()
+        moved = 2 * n_written * hkv * d * (src_es + esize)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(20)]
+        for i in range(3):
+            write(reps[i % len(reps)])
+        for i, (e0, e1) in enumerate(ev):
+            flush.fill_(i & 0xFF)
+            e0.record()
+            write(reps[i % len(reps)])
+            e1.record()
+        torch.cuda.synchronize()
+        us = sum(e0.elapsed_time(e1) for e0, e1 in ev) / len(ev) * 1e3
+        del flush
+        scatter = {"value": round(moved / 1e3 / us, 1), "unit": "GB/s", "us_per_call": round(us, 3),
+                   "bytes_per_call": moved, "tokens": n_written,
+                   "frac_of_hbm_peak": round(moved / 1e3 / us / float(peaks["hbm_gbs"]), 4),
+                   "timing": "20 calls, each after a 256 MB L2 flush, CUDA events around the call",
+                   "kernel": "kv_write_e4m3_kernel" if e4m3 else "kv_write_kernel"}
+
     # ---- end to end through the public API with host buffers ----
     if cascade:
         e2e = run_e2e_cascade(args, w, reps, common, csplits, cws, flag, bytes_step)
@@ -676,6 +703,8 @@ def run_gpu(args, rank, world, local_rank):
         result["mixed_roofline"] = mixed_roofline(w, hq, hkv, d, esize, ms_step, peaks)
     if cascade_info is not None:
         result["cascade"] = cascade_info
+    if scatter is not None:
+        result["scatter"] = scatter
     if clk is not None:
         result["clocks"] = clk
     return result, w
