@@ -52,6 +52,10 @@ WORKLOAD_TEXT = {
     "prefill_8k_e4m3": "prefill_8k over an 8-bit E4M3 KV cache (k_scale = v_scale = 0.5; q, new "
                        "K/V and out bf16): the write quantises the 8192 tokens into 512 "
                        "shuffled blocks",
+    "tiny_mixed_f32": "fp32, 2 q heads / 1 KV head, head_dim 64, 32-block pool: a 32-token "
+                      "prefill, a decode at context 40 and a 3-token tail on a 45-token prefix "
+                      "(a correctness case: the time is reported, the roofline fraction means "
+                      "nothing at this size)",
 }
 
 

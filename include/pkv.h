@@ -405,11 +405,12 @@ pkv_status pkv_attention_varlen_noalloc(const void* q, const void* k_cache, cons
  * row; the prefix is read from HBM once for all requests, split
  * prefix_splits ways over the key axis), each request over its own keys,
  * and a log-sum-exp merge of the prefix_splits + 1 partials per row.  The
- * prefix pass runs on the tensor cores for bf16, head_dim 64 or 128 and an even GQA
- * group that divides 128 (each 128-row tile holds 128 / group tokens with
- * their whole group, so one K/V tile feeds every head of the KV head) and a
- * positive softmax_scale, else on the split-KV kernel's CUDA-core tiles; the
- * own-key pass runs on the decode kernel and the merge on CUDA cores.
+ * prefix pass runs on the tensor cores for bf16 at head_dim 64 or 128 (E4M3
+ * caches at 128, pkv_cascade_attention_e4m3) with an even GQA group that
+ * divides 128 (each 128-row tile holds 128 / group tokens with their whole
+ * group, so one K/V tile feeds every head of the KV head) and a positive
+ * softmax_scale, else on the split-KV kernel's CUDA-core tiles; the own-key
+ * pass runs on the decode kernel and the merge on CUDA cores.
  */
 
 /* pkv_cascade_splits - prefix splits for num_tokens rows over shared_blocks
