@@ -1821,10 +1821,8 @@ __host__ __device__ __forceinline__ int combine_rows(int max_query_len) {
 // Log-sum-exp merge of the split partials: for each (request, decode row,
 // q head), M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s.
 // One CTA of 4 warps per row: warp w takes splits s = w, w + 4, ...; all of a
-// warp's partial loads are issued before any is used.  CASCADE: rows are
-// (token, q head) of the batch and the partials the shared-prefix splits
-// followed by each request's own-key partial.
-template <typename T, int D, bool CASCADE>
+// warp's partial loads are issued before any is used.
+template <typename T, int D>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   constexpr int kDPL = D / 32;
   __shared__ float red[4][D + 1];
@@ -1836,22 +1834,19 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   const int64_t item = blockIdx.x;
   const int h = static_cast<int>(item % a.hq);
   const int64_t ri = item / a.hq;
-  const int qrows = CASCADE ? 1 : combine_rows(a.max_query_len);
-  const int i = CASCADE ? 0 : static_cast<int>(ri % qrows);
-  const int r = CASCADE ? 0 : static_cast<int>(ri / qrows);
+  const int qrows = combine_rows(a.max_query_len);
+  const int i = static_cast<int>(ri % qrows);
+  const int r = static_cast<int>(ri / qrows);
   if (r >= a.num_seqs) return;
   const int S = a.num_splits;                          // <= kMaxSplits = 64
-  // workspace row of partial s: by (request, decode row), or by token
-  auto prow = [&](int sp) -> int64_t {
-    return CASCADE ? (static_cast<int64_t>(sp) * a.num_tokens + ri) * a.hq + h
-                   : ws_row(a, sp, r, i, h);
-  };
+  // workspace row of partial s, by (request, decode row)
+  auto prow = [&](int sp) -> int64_t { return ws_row(a, sp, r, i, h); };
   // Partials are loaded before the row is known to exist (rows of requests
   // that are not decode-class hold stale data and are simply not stored), so
   // the metadata and workspace loads are in flight together.
-  const int q0 = CASCADE ? static_cast<int>(ri) : __ldg(a.qsl + r);
-  const int q1 = CASCADE ? __ldg(a.qsl + a.num_seqs) : __ldg(a.qsl + r + 1);
-  const int L = CASCADE ? 1 : __ldg(a.seq_lens + r);
+  const int q0 = __ldg(a.qsl + r);
+  const int q1 = __ldg(a.qsl + r + 1);
+  const int L = __ldg(a.seq_lens + r);
   const float l0 = lane < S ? a.ws_lse[prow(lane)] : -INFINITY;
   const float l1 = lane + 32 < S ? a.ws_lse[prow(lane + 32)] : -INFINITY;
   constexpr int kMaxPer = kMaxSplits / 4;
@@ -1879,9 +1874,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
       }
     }
   }
-  if (CASCADE) {
-    if (q0 >= q1) return;                              // padding rows: no own-key partial
-  } else {
+  {
     const int n = q1 - q0;
     if (n <= 0 || n > kDecodeMaxQ || i >= n || q0 < 0 || q1 > a.num_tokens || n > L) return;
   }
@@ -1906,7 +1899,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   __syncthreads();
   if (warp != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const int64_t t = CASCADE ? ri : q0 + i;
+  const int64_t t = q0 + i;
 #pragma unroll
   for (int e = 0; e < kDPL; ++e) {
     const int col = lane * kDPL + e;
@@ -1915,6 +1908,84 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   }
   if (a.lse_out != nullptr && lane == 0)
     a.lse_out[t * a.hq + h] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
+}
+
+// The shared-prefix merge (cascade pass 3): for each (token, q head) row,
+// M = max_s lse_s, w_s = 2^(lse_s - M), o = sum_s w_s o_s / sum_s w_s over the
+// prefix splits' partials and the request's own-key partial.  One warp per
+// row, four rows per CTA: a row's few partials (prefix splits + 1) fit one
+// warp's registers, so there is no cross-warp reduction; the lane's slice of
+// every partial of a chunk is loaded before any is used.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_rows_kernel(const AttnArgs a) {
+  constexpr int kDPL = D / 32;
+  constexpr int kChunk = 16;                           // partial loads in flight per lane
+  pdl_launch_dependents();
+  pdl_wait_primary();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (item >= a.num_tokens * a.hq) return;
+  const int64_t tok = item / a.hq;
+  const int h = static_cast<int>(item % a.hq);
+  const int S = a.num_splits;                          // <= kMaxSplits = 64
+  auto prow = [&](int sp) -> int64_t {
+    return (static_cast<int64_t>(sp) * a.num_tokens + tok) * a.hq + h;
+  };
+  auto load = [&](int sp, float (&v)[kDPL]) {
+    const float* src = a.ws_o + prow(sp) * D + lane * kDPL;
+    if constexpr (kDPL == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(src);
+      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(src);
+      v[0] = x.x; v[1] = x.y;
+    }
+  };
+  const int q1 = __ldg(a.qsl + a.num_seqs);
+  const float l0 = lane < S ? a.ws_lse[prow(lane)] : -INFINITY;
+  const float l1 = lane + 32 < S ? a.ws_lse[prow(lane + 32)] : -INFINITY;
+  float part[kChunk][kDPL];
+#pragma unroll
+  for (int u = 0; u < kChunk; ++u)
+    if (u < S) load(u, part[u]);
+  if (tok >= q1) return;                               // padding rows: no own-key partial
+  const float M = warp_max(fmaxf(l0, l1));
+  const float w0 = M == -INFINITY ? 0.f : ex2(l0 - M);
+  const float w1 = M == -INFINITY ? 0.f : ex2(l1 - M);
+  const float wsum = warp_sum(w0 + w1);
+  float o[kDPL];
+#pragma unroll
+  for (int e = 0; e < kDPL; ++e) o[e] = 0.f;
+  for (int c0 = 0; c0 < S; c0 += kChunk) {
+    if (c0 > 0) {
+#pragma unroll
+      for (int u = 0; u < kChunk; ++u)
+        if (c0 + u < S) load(c0 + u, part[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kChunk; ++u) {
+      const int sp = c0 + u;
+      if (sp < S) {
+        const float f = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+#pragma unroll
+        for (int e = 0; e < kDPL; ++e) o[e] = fmaf(f, part[u][e], o[e]);
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int64_t base = (tok * a.hq + h) * D + lane * kDPL;
+  if constexpr (sizeof(T) == 2 && kDPL == 4) {
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + base) =
+        make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
+  } else if constexpr (sizeof(T) == 2) {
+    *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + base) =
+        pack_bf16x2(o[0] * inv, o[1] * inv);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kDPL; ++e) store_elem<T>(a.out, base + e, o[e] * inv);
+  }
+  if (a.lse_out != nullptr && lane == 0)
+    a.lse_out[tok * a.hq + h] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------
@@ -2038,18 +2109,20 @@ cudaError_t launch_combine(const AttnArgs& a, ElemType et, int head_dim, cudaStr
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (a.cascade == 3) {
+    // one warp per (token, head) row, four rows per CTA
+    cfg.gridDim = dim3(static_cast<unsigned>((items + 3) / 4));
     if (et != ElemType::kF32)
-      return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128, true>, a)
-                             : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64, true>, a);
-    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 128, true>, a)
-                           : cudaLaunchKernelEx(&cfg, combine_kernel<float, 64, true>, a);
+      return head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_rows_kernel<__nv_bfloat16, 128>, a)
+                             : cudaLaunchKernelEx(&cfg, merge_rows_kernel<__nv_bfloat16, 64>, a);
+    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_rows_kernel<float, 128>, a)
+                           : cudaLaunchKernelEx(&cfg, merge_rows_kernel<float, 64>, a);
   }
   if (et != ElemType::kF32) {
-    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128, false>, a)
-                           : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64, false>, a);
+    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 128>, a)
+                           : cudaLaunchKernelEx(&cfg, combine_kernel<__nv_bfloat16, 64>, a);
   }
-  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 128, false>, a)
-                         : cudaLaunchKernelEx(&cfg, combine_kernel<float, 64, false>, a);
+  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<float, 128>, a)
+                         : cudaLaunchKernelEx(&cfg, combine_kernel<float, 64>, a);
 }
 
 }  // namespace pkv
