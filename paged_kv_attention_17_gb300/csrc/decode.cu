@@ -1825,7 +1825,8 @@ __host__ __device__ __forceinline__ int combine_rows(int max_query_len) {
 template <typename T, int D>
 __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   constexpr int kDPL = D / 32;
-  __shared__ float red[4][D + 1];
+  // per-warp sums, rows padded to keep each lane's slice 16-byte aligned
+  __shared__ __align__(16) float red[4][D + 4];
   // the next kernel may launch at once; its dependency wait still returns only
   // after this grid completes
   pdl_launch_dependents();
@@ -1900,11 +1901,31 @@ __global__ void __launch_bounds__(128) combine_kernel(const AttnArgs a) {
   if (warp != 0) return;
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   const int64_t t = q0 + i;
+  const int64_t base = (t * a.hq + h) * D + lane * kDPL;
+  float v[kDPL];
+  if constexpr (kDPL == 4) {
+    float4 s4 = *reinterpret_cast<const float4*>(&red[0][lane * 4]);
 #pragma unroll
-  for (int e = 0; e < kDPL; ++e) {
-    const int col = lane * kDPL + e;
-    const float v = red[0][col] + red[1][col] + red[2][col] + red[3][col];
-    store_elem<T>(a.out, (t * a.hq + h) * D + col, v * inv);
+    for (int w = 1; w < 4; ++w) {
+      const float4 x = *reinterpret_cast<const float4*>(&red[w][lane * 4]);
+      s4.x += x.x; s4.y += x.y; s4.z += x.z; s4.w += x.w;
+    }
+    v[0] = s4.x * inv; v[1] = s4.y * inv; v[2] = s4.z * inv; v[3] = s4.w * inv;
+  } else {
+#pragma unroll
+    for (int e = 0; e < kDPL; ++e) {
+      const int col = lane * kDPL + e;
+      v[e] = (red[0][col] + red[1][col] + red[2][col] + red[3][col]) * inv;
+    }
+  }
+  if constexpr (sizeof(T) == 2 && kDPL == 4) {
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + base) =
+        make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+  } else if constexpr (sizeof(T) == 2 && kDPL == 2) {
+    *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + base) = pack_bf16x2(v[0], v[1]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < kDPL; ++e) store_elem<T>(a.out, base + e, v[e]);
   }
   if (a.lse_out != nullptr && lane == 0)
     a.lse_out[t * a.hq + h] = wsum > 0.f ? (M + lg2(wsum)) * kLn2 : -INFINITY;
