@@ -843,7 +843,7 @@ def run_secondary(name, local_rank, steps, warmup, cpu_seconds):
     res, _ = run_gpu(args, 0, 1, local_rank)
     torch.cuda.synchronize()
     keep = ("value", "unit", "steps", "warmup", "ms_per_step", "ms_per_step_p10_p50_p90",
-            "roofline", "e2e", "clocks", "mixed_roofline", "gpu_launches", "dtype")
+            "roofline", "e2e", "clocks", "mixed_roofline", "gpu_launches", "dtype", "scatter")
     out = {"workload": res["config"]["workload"], "num_splits": res["config"]["num_splits"],
            "step": res["config"]["step"], "l2": res["config"]["l2"]}
     out.update({k: res[k] for k in keep if k in res})
