@@ -300,9 +300,10 @@ pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const
  * 128 the contractions run on tensor cores with fp32 accumulation and P
  * rounded to f16 for P.V.  V codes are widened exactly to f16.  K codes are
  * widened too, with q scaled by a power of two into f16, in split decode
- * launches; in unsplit ones (up to 8 rows a tile) they enter E4M3 MMAs as
- * they are, against each q row scaled by a power of two and split exactly
- * into two E4M3 terms.  That is the decode kernel's mma.sync tiles for decode
+ * launches without a window (the latency-bound form, which fetches each
+ * split's first block speculatively) and in tiles of 16 rows; otherwise they
+ * enter E4M3 MMAs as they are, against each q row scaled by a power of two
+ * and split exactly into two E4M3 terms.  That is the decode kernel's mma.sync tiles for decode
  * rows; longer requests take the tcgen05 prefill tiles (codes widened in
  * shared memory, each q row rewritten as f16 scaled so its largest magnitude
  * lies in [2^14, 2^15)).  At head_dim 64 the codes are widened to fp32 in
