@@ -627,9 +627,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
   // staged in shared memory, where each lane picks its fragment words.
   constexpr int kMT = kMma ? D / 16 : 1;               // k-steps of Q.K^T
   // E4M3 cache: K's codes enter the MMAs as they are (m16n8k32 E4M3 against
-  // q split into two E4M3 terms) in unsplit launches of up to 8 rows a tile,
-  // where the per-block path dominates; split launches, latency-bound, keep
-  // the shorter q set-up of f16 MMAs over widened codes
+  // q split into two E4M3 terms) in tiles of up to 8 rows, where the
+  // per-block path dominates; the speculative form (split launches without
+  // a window: latency-bound) keeps the shorter q set-up of f16 MMAs over
+  // widened codes
   constexpr bool kF8Mma = kMma && kIsE4m3<T> && !SPEC && R <= 8;
   constexpr bool kHi = R == 16;                        // M-rows 8..15 are tile rows
   constexpr int kHR = kHi ? 2 : 1;                     // M-row halves this lane holds
