@@ -346,9 +346,9 @@ static pkv_status attention(const void* q, const void* k_cache, const void* v_ca
 
 }  // namespace
 
-// The prefix split count: splits of whole 128-key tiles over the
-// tensor-core prefix pass's 256-row tiles (tc), or of >= 8 blocks over the
-// CUDA-core pass's 16-row tiles, filling 7/8 of the SMs.
+// The prefix split count: splits of at least four whole 128-key tiles over
+// the tensor-core prefix pass's 256-row tiles (tc), or of >= 8 blocks over
+// the CUDA-core pass's 16-row tiles, filling 7/8 of the SMs.
 static int cascade_split_rule(int64_t num_tokens, int shared_blocks, int num_q_heads,
                               int num_kv_heads, int head_dim, bool tc, int device) {
   if (num_tokens < 1 || shared_blocks < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
@@ -358,15 +358,17 @@ static int cascade_split_rule(int64_t num_tokens, int shared_blocks, int num_q_h
   const int sms = device_sms(device);
   if (sms <= 0) return -1;
   const int group = num_q_heads / num_kv_heads;
-  // tensor-core prefix pass: 256 (token, head) rows per CTA, splits of whole
-  // 128-key tiles; CUDA-core pass: 16-row tiles, splits of >= 8 blocks
+  // tensor-core prefix pass: 256 (token, head) rows per CTA, splits of at
+  // least four whole 128-key tiles (fewer tiles per CTA leave its pipeline
+  // short of its steady state); CUDA-core pass: 16-row tiles, splits of >= 8
+  // blocks
   (void)head_dim;
   const int rows = tc ? 256 : kCascadeRows;
   const int64_t tiles = static_cast<int64_t>(num_kv_heads) * ((group * num_tokens + rows - 1) / rows);
   const int64_t target =
       static_cast<int64_t>(sms) * 7 / 8;
   int64_t s = target / tiles;
-  int64_t by_len = tc ? (shared_blocks + 7) / 8 : shared_blocks / kMinBlocksPerSplit;
+  int64_t by_len = tc ? (shared_blocks + 31) / 32 : shared_blocks / kMinBlocksPerSplit;
   if (s > by_len) s = by_len;
   if (s > kMaxSplits - 1) s = kMaxSplits - 1;        // + the own-key partial <= kMaxSplits
   return static_cast<int>(s < 1 ? 1 : s);
