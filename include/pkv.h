@@ -415,14 +415,14 @@ pkv_status pkv_attention_varlen_noalloc(const void* q, const void* k_cache, cons
  */
 
 /* pkv_cascade_splits - prefix splits for num_tokens rows over shared_blocks
- * blocks.  Tensor-core prefix pass (bf16, head_dim 64 or 128, even GQA group
- * dividing 128): U = num_kv_heads x ceil(group x num_tokens / 256) row tiles,
- * T = floor(7 x SMs / 8), min(max(1, floor(T / U)), ceil(shared_blocks / 32),
- * 63) - each split at least four 128-key tiles (fewer leave the pass short of
- * its pipelined steady state).  CUDA-core pass (otherwise):
- * U = num_kv_heads x ceil(group x num_tokens / 16), T as for pkv_num_splits,
- * min(max(1, floor(T / U)), shared_blocks / 8, 63).  0 when shared_blocks ==
- * 0; -1 for invalid arguments or device. */
+ * blocks: max(1, min(floor(T / U), cap, 63)) with T = floor(7 x SMs / 8).
+ * Tensor-core prefix pass (bf16, head_dim 64 or 128, even GQA group dividing
+ * 128): U = num_kv_heads x ceil(group x num_tokens / 256) row tiles, cap =
+ * ceil(shared_blocks / 32) - each split at least four 128-key tiles (fewer
+ * leave the pass short of its pipelined steady state).  CUDA-core pass
+ * (otherwise): U = num_kv_heads x ceil(group x num_tokens / 16), cap =
+ * floor(shared_blocks / 8).  0 when shared_blocks == 0; -1 for invalid
+ * arguments or device. */
 int pkv_cascade_splits(int64_t num_tokens, int shared_blocks, int num_q_heads, int num_kv_heads,
                        int head_dim, pkv_dtype dtype, int device);
 

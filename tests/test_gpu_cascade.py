@@ -162,6 +162,37 @@ def test_cascade_over_e4m3_cache(prefix_splits, shared_blocks, hq, hkv, d):
     _check(out, lse, w, "bf16")
 
 
+def test_cascade_split_rule():
+    # pkv_cascade_splits as the header states it: T = floor(7 SMs / 8); the
+    # tensor-core pass (bf16, an even group dividing 128) over U = H_kv x
+    # ceil(group x tokens / 256) row tiles with at least four 128-key tiles a
+    # split, the CUDA-core pass over U = H_kv x ceil(group x tokens / 16) with
+    # at least 8 blocks a split; max(1, min(T // U, length cap, 63))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = sms * 7 // 8
+
+    def rule(n, blocks, hq, hkv, tc):
+        g = hq // hkv
+        U = hkv * -(-(g * n) // (256 if tc else 16))
+        cap = -(-blocks // 32) if tc else blocks // 8
+        return max(1, min(T // U, cap, 63))
+
+    cases = [  # (tokens, shared blocks, hq, hkv, dtype, tensor-core pass)
+        (64, 256, 32, 8, torch.bfloat16, True),       # the bench batch: 8 splits
+        (1, 4096, 32, 8, torch.bfloat16, True),       # a 64K-token prefix
+        (2048, 1024, 32, 8, torch.bfloat16, True),    # a full grid: one split
+        (64, 5, 32, 8, torch.bfloat16, True),         # under four tiles: one split
+        (64, 256, 12, 4, torch.bfloat16, False),      # odd group: CUDA-core pass
+        (64, 256, 32, 8, torch.float32, False),       # fp32: CUDA-core pass
+        (64, 5, 32, 8, torch.float32, False),         # under 8 blocks: one split
+        (3, 600, 8, 1, torch.bfloat16, True),         # group 8
+    ]
+    for n, blocks, hq, hkv, dt, tc in cases:
+        assert pkv.pkv_cascade_splits(n, blocks, hq, hkv, 128, dt) == rule(n, blocks, hq, hkv, tc), \
+            (n, blocks, hq, hkv, dt)
+    assert pkv.pkv_cascade_splits(64, 0, 32, 8, 128) == 0
+
+
 def test_cascade_e4m3_rejects_bad_scales():
     w = workloads.build_cascade("casc_e4m3_bad", "bf16", 8, 2, 128, 2, [(3, 1)], seed=1,
                                 kv_dtype="e4m3", k_scale=0.5, v_scale=0.5)
