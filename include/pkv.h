@@ -303,7 +303,8 @@ pkv_status pkv_attention_varlen_window(const void* q, const void* k_cache, const
  * launches without a window (the latency-bound form, which fetches each
  * split's first block speculatively) and in tiles of 16 rows; otherwise they
  * enter E4M3 MMAs as they are, against each q row scaled by a power of two
- * and split exactly into two E4M3 terms.  That is the decode kernel's mma.sync tiles for decode
+ * and split into two E4M3 terms (exact for every element within 2^9 of
+ * the row's largest).  That is the decode kernel's mma.sync tiles for decode
  * rows; longer requests take the tcgen05 prefill tiles (codes widened in
  * shared memory, each q row rewritten as f16 scaled so its largest magnitude
  * lies in [2^14, 2^15)).  At head_dim 64 the codes are widened to fp32 in

@@ -224,9 +224,10 @@ __device__ __forceinline__ void mma16832_e4m3(float& d0, float& d1, float& d2, f
 }
 
 // Four values x0..x3 (each with at most 8 significant bits, magnitudes below
-// 2^8) as two E4M3 words, hi + lo = x: hi is x rounded to E4M3, lo the
-// remainder (at most 4 significant bits: exact unless below E4M3's range,
-// 2^-9), element 0 in the low byte.
+// 2^8) as two E4M3 words, element 0 in the low byte: hi is x rounded to E4M3,
+// lo the remainder x - hi rounded to E4M3.  The remainder has at most 4
+// significant bits and x's last bit, so hi + lo = x exactly when that bit is
+// on E4M3's 2^-9 grid (|x| >= 2^-2); below, |hi + lo - x| <= 2^-10.
 __device__ __forceinline__ void e4m3_split4(float x0, float x1, float x2, float x3,
                                             uint32_t& hi, uint32_t& lo) {
   uint32_t h01, h23, l01, l23;
@@ -949,15 +950,17 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
       //      the rows elsewhere, staged in shared memory, and each lane's B
       //      operand words picked for rows 8h + g8 (zero past the tile's
       //      rows).  E4M3 cache: each q row is scaled by a power of two
-      //      bringing its max|q| into [2^7, 2^8) and split exactly into two
-      //      E4M3 terms (hi + lo), so K's codes enter the MMAs as they are;
-      //      the row's score scale takes the inverse power. ----
+      //      bringing its max|q| into [2^7, 2^8) and split into two E4M3
+      //      terms (hi + lo: exact for every element within 2^9 of the row's
+      //      largest, off by at most 2^-17 of it below that), so K's codes
+      //      enter the MMAs as they are; the row's score scale takes the
+      //      inverse power. ----
       if (q0 != (prefix_pass ? 0 : q0_hint)) load_q(q0);
       uint8_t* qst = smem + Sm::kQOff;
       if constexpr (kF8Mma) {
         // E4M3 contraction: the 16 threads holding a row's 8-element chunks (a
         // half-warp) find its max|q|, scale it by 2^-e into [2^7, 2^8) and
-        // split each chunk exactly into hi + lo E4M3 codes; a row past the
+        // split each chunk into hi + lo E4M3 codes; a row past the
         // tile's rows is zeros.  Code rows: hi at qst, lo R rows further,
         // then the rows' log2-domain score scales.
         static_assert(D / 8 == 16, "a q row is one half-warp's chunks");
