@@ -1065,9 +1065,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, R>::kThreads, DecodeCfg<T, D, 
           }
         }
       } else if constexpr (kIsE4m3<T>) {
-        // f16 contraction: q scaled by a power of two bringing max|q| into
-        // [2^14, 2^15), where f16 holds every bf16 value exactly; the score
-        // scale takes the inverse
+        // f16 contraction: the tile's q scaled by a power of two bringing its
+        // max|q| into [2^14, 2^15), where f16 holds every bf16 element within
+        // 2^31 of that maximum exactly; the score scale takes the inverse
         float mx = 0.f;
 #pragma unroll
         for (int hr = 0; hr < kHR; ++hr)
