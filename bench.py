@@ -832,6 +832,9 @@ def run_e2e(args, w, reps, common, splits, workspace, flag, device, bytes_step, 
 
 
 SECONDARY = ("batched_decode_64", "mixed_chunked", "prefill_8k", "prefill_8k_e4m3")
+# workloads whose CPU baseline also reports a one-thread figure (the small and
+# decode configurations of the measurement plan)
+ONE_THREAD_TOO = ("tiny_mixed_f32", "decode_8k", "batched_decode_64")
 
 
 def run_secondary(name, local_rank, steps, warmup, cpu_seconds):
@@ -849,6 +852,10 @@ def run_secondary(name, local_rank, steps, warmup, cpu_seconds):
     out.update({k: res[k] for k in keep if k in res})
     if cpu_seconds > 0:
         out["cpu_baseline"] = cpu_baseline(name, cpu_seconds)
+        if name in ONE_THREAD_TOO:
+            one = cpu_baseline_one_thread(name, cpu_seconds / 2)
+            if one is not None:
+                out["cpu_baseline"]["one_thread"] = one
     return out
 
 
@@ -991,7 +998,7 @@ def main(argv=None):
                 for n in SECONDARY}
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
-            if args.workload in ("decode_8k", "batched_decode_64"):
+            if args.workload in ONE_THREAD_TOO:
                 one = cpu_baseline_one_thread(args.workload, args.cpu_seconds / 2)
                 if one is not None:
                     result["cpu_baseline"]["one_thread"] = one
