@@ -40,3 +40,14 @@ def test_driver_configuration():
     # 8 rotating tables -> graphs of 8 and 4 steps, and of 5 for the warm-up
     assert bench.graph_sizes(20, 8) == [8, 4]
     assert bench.precapture_sizes(5, 20, 8) == [4, 5, 8]
+
+
+def test_every_named_workload_is_defined_and_selectable():
+    # the headline, its secondary lines and the one-thread baselines name
+    # workloads that workloads.NAMED builds and --workload accepts
+    import workloads
+    names = {bench.HEADLINE, *bench.SECONDARY, *bench.ONE_THREAD_TOO}
+    assert names <= set(workloads.NAMED)
+    assert names <= set(bench.WORKLOAD_TEXT)
+    for n in names:
+        assert bench.parse_args(["--workload", n]).workload == n
